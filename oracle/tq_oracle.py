@@ -100,7 +100,7 @@ def lloyd_max_gaussian(bits: int, d: int, tol: float = 1e-13, max_iter: int = 20
     centroids; each centroid is the conditional mean of its cell,
     sigma * (phi(a/sigma) - phi(b/sigma)) / (Phi(b/sigma) - Phi(a/sigma));
     start from the N(0, 1) quantile midpoints; stop when no centroid moves by
-    more than tol * sigma.
+    more than tol * sigma; finally make the codebook exactly odd-symmetric.
 
     Returns (centroids [2^bits], boundaries [2^bits - 1]) ascending, fp64.
     """
@@ -120,6 +120,10 @@ def lloyd_max_gaussian(bits: int, d: int, tol: float = 1e-13, max_iter: int = 20
         c = c_new
         if moved < tol:
             break
+    # N(0, 1/d) is symmetric, so the optimal quantiser is odd: c[L-1-k] = -c[k]
+    # (reading).  Mirroring removes rounding asymmetry so the middle boundary
+    # is exactly 0 and a zero coordinate takes the upper index on any machine.
+    c = 0.5 * (c - c[::-1])
     c = c * sigma
     return c, 0.5 * (c[:-1] + c[1:])
 

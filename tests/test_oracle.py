@@ -122,6 +122,7 @@ def test_codebook_mse_monte_carlo(bits):
 def test_codebook_symmetric_and_fp32():
     for bits in (1, 2, 3):
         c, b = O.codebook(bits, 128)
+        assert b[len(b) // 2] == 0.0
         np.testing.assert_array_equal(c, -c[::-1])
         np.testing.assert_array_equal(c.astype(np.float32).astype(np.float64), c)
         np.testing.assert_array_equal(b.astype(np.float32).astype(np.float64), b)
