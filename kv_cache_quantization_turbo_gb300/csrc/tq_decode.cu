@@ -1,0 +1,373 @@
+// Decode attention over the compressed cache.
+//
+//   1. prologue (one warp per query head): q' = scale * H diag(s) q  and
+//      Sq' = S q'  for turbo K ("rotate q once"); q' = scale * q for q8_0 K.
+//   2. split-K attention: each CTA takes one (split of the context, KV head,
+//      layer x sequence) and all G query heads of that KV head; it scores the
+//      packed K against q' and Sq',
+//        s_j = n_j <q', c[idx_j]> + rnorm_j sqrt(pi/2)/d <Sq', 2 sigma_j - 1>,
+//      keeps an online softmax (running max m, sum l), accumulates V in the
+//      rotated space as exp(s_j - m) n_j c_V[idx_j] unless that weight is below
+//      skip_threshold ("TurboQuant+: 3.8x compression ...", core content item
+//      4, Sparse V), and writes the partial (m, l, acc).
+//   3. combine (one warp per query head): log-sum-exp merge of the partials,
+//      acc / l, then diag(s) H back to the original space for turbo V.
+#include <cmath>
+
+#include <cuda_fp16.h>
+
+#include "tq_device.cuh"
+
+namespace tq {
+
+static int next_pow2(long long v) {
+  int p = 1;
+  while (p < v && p < (1 << 30)) p <<= 1;
+  return p;
+}
+
+DecodePlan plan_decode(int sm_count, int d, int n_layers, int batch, int n_q_heads, int max_ctx) {
+  DecodePlan p{};
+  const long long per_sm = ((long long)max_ctx * n_layers * batch + 2LL * sm_count - 1) / (2LL * sm_count);
+  int st = next_pow2(per_sm);
+  st = st < 256 ? 256 : (st > 4096 ? 4096 : st);
+  p.split_tokens = st;
+  p.n_splits = max_ctx > 0 ? (max_ctx + st - 1) / st : 1;
+  const long long rows = (long long)n_layers * batch * n_q_heads;
+  p.qprep_floats = (size_t)rows * 2 * d;
+  p.partial_floats = (size_t)rows * p.n_splits * (d + 4);
+  auto al = [](size_t b) { return (b + 255) / 256 * 256; };
+  p.bytes = al(p.qprep_floats * 4) + al(p.partial_floats * 4);
+  return p;
+}
+
+namespace {
+
+struct DecodeKernelArgs {
+  DecodeArgs a;
+  DevTables tab;
+  int split_tokens, n_splits, G;
+  float* qprep;     // [rows][2d]
+  float* partial;   // [rows][n_splits][d + 4]: m, l, -, -, acc[d]
+};
+
+// ---------------------------------------------------------------------------
+// 1. query prologue
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(32) qprep_kernel(DecodeKernelArgs ka) {
+  constexpr int E = D / 32;
+  const DecodeArgs& a = ka.a;
+  const int lane = threadIdx.x;
+  const long long row = blockIdx.x;  // (layer, batch, q head)
+  __shared__ float q_s[D];
+  float x[E];
+  if (a.q_is_fp16) {
+    const __half* q = static_cast<const __half*>(a.q) + row * D;
+#pragma unroll
+    for (int e = 0; e < E; ++e) x[e] = __half2float(q[E * lane + e]);
+  } else {
+    const float* q = static_cast<const float*>(a.q) + row * D;
+#pragma unroll
+    for (int e = 0; e < E; ++e) x[e] = q[E * lane + e];
+  }
+  float* dst = ka.qprep + row * 2 * D;
+  if (a.k.format == TQ_FMT_Q8_0) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) dst[E * lane + e] = x[e] * a.softmax_scale;
+    return;
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) x[e] *= (float)ka.tab.signs[E * lane + e];
+  warp_wht<D>(x, lane);
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    x[e] *= a.softmax_scale;
+    q_s[E * lane + e] = x[e];
+    dst[E * lane + e] = x[e];
+  }
+  __syncwarp();
+  float sq[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) sq[e] = 0.f;
+  for (int i = 0; i < D; ++i) {
+    const float qi = q_s[i];
+#pragma unroll
+    for (int e = 0; e < E; ++e) sq[e] = fmaf(__ldg(ka.tab.S_T + i * D + E * lane + e), qi, sq[e]);
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) dst[D + E * lane + e] = sq[e];
+}
+
+// ---------------------------------------------------------------------------
+// token addressing shared by the attention kernels
+// ---------------------------------------------------------------------------
+struct SeqInfo {
+  int len;  // clamped sequence length
+};
+
+__device__ __forceinline__ int clamp_seq_len(const DecodeArgs& a, int b, uint32_t* status) {
+  int len = a.seq_lens[b];
+  if (len < 0) len = 0;
+  if (len > a.max_ctx) {
+    if (threadIdx.x == 0) atomicOr(status, kFlagSeqLen);
+    len = a.max_ctx;
+  }
+  return len;
+}
+
+// Vector index of token j of sequence b (head kvh, layer) in view V, or -1.
+__device__ __forceinline__ long long token_vector(const DecodeArgs& a, const DevView& V, int layer, int b, int j,
+                                                  int kvh, uint32_t* status) {
+  long long page;
+  if (a.block_table) {
+    page = a.block_table[(long long)b * a.max_blocks_per_seq + j / V.page_size];
+    if (page < 0 || page >= V.num_pages) {
+      atomicOr(status, kFlagBlockTable);
+      return -1;
+    }
+  } else {
+    page = b;
+  }
+  const long long p = j % V.page_size;
+  return (((long long)layer * V.num_pages + page) * V.H + kvh) * V.page_size + p;
+}
+
+// ---------------------------------------------------------------------------
+// 2. split-K attention, generic form (any supported format and head_dim):
+//    one warp per CTA; lane = token while scoring, lane = coordinates while
+//    accumulating V.
+// ---------------------------------------------------------------------------
+constexpr int kGMax = 16;
+
+template <int D>
+__global__ void __launch_bounds__(32) attend_generic_kernel(DecodeKernelArgs ka) {
+  constexpr int E = D / 32;
+  const DecodeArgs& a = ka.a;
+  const int lane = threadIdx.x;
+  const int split = blockIdx.x, kvh = blockIdx.y;
+  const int lb = blockIdx.z, layer_rel = lb / a.batch, b = lb % a.batch;
+  const int layer = a.layer_begin + layer_rel;
+  const int G = ka.G;
+  const int Hq = a.n_q_heads;
+  // dynamic shared memory: q' [G][D], Sq' [G][D], acc [G][D], two codebooks
+  extern __shared__ __align__(16) float dsm[];
+  float (*qs)[D] = reinterpret_cast<float (*)[D]>(dsm);
+  float (*sqs)[D] = reinterpret_cast<float (*)[D]>(dsm + ka.G * D);
+  float (*acc_s)[D] = reinterpret_cast<float (*)[D]>(dsm + 2 * ka.G * D);
+  float* cbk = dsm + 3 * ka.G * D;
+  float* cbv = cbk + 8;
+
+  const long long row0 = (long long)lb * Hq + (long long)kvh * G;  // first q row of this KV head
+  for (int i = lane; i < G * D; i += 32) {
+    const int g = i / D, k = i % D;
+    qs[g][k] = ka.qprep[(row0 + g) * 2 * D + k];
+    sqs[g][k] = ka.qprep[(row0 + g) * 2 * D + D + k];
+    acc_s[g][k] = 0.f;
+  }
+  const bool k_turbo = a.k.format != TQ_FMT_Q8_0, v_turbo = a.v.format != TQ_FMT_Q8_0;
+  if (lane < 8) {
+    cbk[lane] = k_turbo ? ka.tab.centroids[(a.k.idx_bits - 1) * 8 + lane] : 0.f;
+    cbv[lane] = v_turbo ? ka.tab.centroids[(a.v.idx_bits - 1) * 8 + lane] : 0.f;
+  }
+  __syncwarp();
+
+  const int len = clamp_seq_len(a, b, ka.tab.status);
+  const int t0 = split * ka.split_tokens;
+  const int t1 = min(t0 + ka.split_tokens, len);
+  float m[kGMax], l[kGMax];
+#pragma unroll
+  for (int g = 0; g < kGMax; ++g) { m[g] = -INFINITY; l[g] = 0.f; }
+  const float qjl_k = kSqrtHalfPi / (float)D;
+  const int kb = a.k.idx_bits, kw = a.k.code_bits, vb = a.v.idx_bits, vw = a.v.code_bits;
+
+  for (int tb = t0; tb < t1; tb += 32) {
+    const int j = tb + lane;
+    const bool valid_tok = j < t1;
+    float s[kGMax];
+#pragma unroll
+    for (int g = 0; g < kGMax; ++g) s[g] = -INFINITY;
+    long long kv = valid_tok ? token_vector(a, a.k, layer, b, j, kvh, ka.tab.status) : -1;
+    if (kv >= 0) {
+      const unsigned char* hdr = a.k.header + kv * a.k.hdr_bytes;
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(a.k.payload + kv * a.k.pay_bytes);
+      float am[kGMax], aq[kGMax];
+#pragma unroll
+      for (int g = 0; g < kGMax; ++g) { am[g] = 0.f; aq[g] = 0.f; }
+      if (k_turbo) {
+        for (int i = 0; i < D; ++i) {
+          const uint32_t c = stream_code(w, i, kw);
+          const float cv = cbk[c & ((1u << kb) - 1u)];
+          const bool pos = (c >> kb) & 1u;
+#pragma unroll
+          for (int g = 0; g < kGMax; ++g) {
+            if (g < G) {
+              am[g] = fmaf(qs[g][i], cv, am[g]);
+              aq[g] += pos ? sqs[g][i] : -sqs[g][i];
+            }
+          }
+        }
+        const float n = __half2float(reinterpret_cast<const __half*>(hdr)[0]);
+        const float rn = a.k.has_qjl ? __half2float(reinterpret_cast<const __half*>(hdr)[1]) : 0.f;
+#pragma unroll
+        for (int g = 0; g < kGMax; ++g) s[g] = n * am[g] + rn * qjl_k * aq[g];
+      } else {
+        const int8_t* q8 = reinterpret_cast<const int8_t*>(w);
+        const __half* dl = reinterpret_cast<const __half*>(hdr);
+        for (int blk = 0; blk < D / 32; ++blk) {
+#pragma unroll
+          for (int g = 0; g < kGMax; ++g) aq[g] = 0.f;
+          for (int i = 32 * blk; i < 32 * blk + 32; ++i) {
+            const float qv = (float)q8[i];
+#pragma unroll
+            for (int g = 0; g < kGMax; ++g)
+              if (g < G) aq[g] = fmaf(qs[g][i], qv, aq[g]);
+          }
+          const float delta = __half2float(dl[blk]);
+#pragma unroll
+          for (int g = 0; g < kGMax; ++g) am[g] = fmaf(delta, aq[g], am[g]);
+        }
+#pragma unroll
+        for (int g = 0; g < kGMax; ++g) s[g] = am[g];
+      }
+    }
+    // online softmax over this chunk of 32 tokens
+    float p[kGMax];
+#pragma unroll
+    for (int g = 0; g < kGMax; ++g) {
+      if (g < G) {
+        const float cm = warp_max(s[g]);
+        const float mn = fmaxf(m[g], cm);
+        const float alpha = (mn == -INFINITY) ? 1.f : expf(m[g] - mn);
+        p[g] = (s[g] == -INFINITY) ? 0.f : expf(s[g] - mn);
+        l[g] = l[g] * alpha + warp_sum(p[g]);
+        m[g] = mn;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc_s[g][E * lane + e] *= alpha;
+      } else {
+        p[g] = 0.f;
+      }
+    }
+    // V accumulation, token by token (lane = coordinates)
+    const int nt = min(32, t1 - tb);
+    for (int jj = 0; jj < nt; ++jj) {
+      float pj[kGMax];
+      bool keep = false;
+#pragma unroll
+      for (int g = 0; g < kGMax; ++g) {
+        pj[g] = __shfl_sync(kFull, p[g], jj);
+        keep |= (g < G) && pj[g] > 0.f && pj[g] >= a.skip_threshold;
+      }
+      if (!keep) continue;  // warp-uniform: every V term of this token is below the threshold
+      const long long vv = token_vector(a, a.v, layer, b, tb + jj, kvh, ka.tab.status);
+      if (vv < 0) continue;
+      const unsigned char* hdr = a.v.header + vv * a.v.hdr_bytes;
+      const unsigned char* pay = a.v.payload + vv * a.v.pay_bytes;
+      float val[E];
+      if (v_turbo) {
+        const float n = __half2float(reinterpret_cast<const __half*>(hdr)[0]);
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          val[e] = n * cbv[stream_code(reinterpret_cast<const uint32_t*>(pay), E * lane + e, vw) & ((1u << vb) - 1u)];
+      } else {
+        const float delta = __half2float(reinterpret_cast<const __half*>(hdr)[(E * lane) / 32]);
+#pragma unroll
+        for (int e = 0; e < E; ++e) val[e] = (float)reinterpret_cast<const int8_t*>(pay)[E * lane + e] * delta;
+      }
+#pragma unroll
+      for (int g = 0; g < kGMax; ++g) {
+        if (g < G && pj[g] > 0.f && pj[g] >= a.skip_threshold) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc_s[g][E * lane + e] = fmaf(pj[g], val[e], acc_s[g][E * lane + e]);
+        }
+      }
+    }
+  }
+  // write the partial of every query head of this KV head
+  for (int g = 0; g < G; ++g) {
+    float* dst = ka.partial + ((row0 + g) * ka.n_splits + split) * (D + 4);
+    if (lane == 0) { dst[0] = m[g]; dst[1] = l[g]; }
+#pragma unroll
+    for (int e = 0; e < E; ++e) dst[4 + E * lane + e] = acc_s[g][E * lane + e];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. combine
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(32) combine_kernel(DecodeKernelArgs ka) {
+  constexpr int E = D / 32;
+  const DecodeArgs& a = ka.a;
+  const int lane = threadIdx.x;
+  const long long row = blockIdx.x;
+  const float* part = ka.partial + row * ka.n_splits * (D + 4);
+  float M = -INFINITY;
+  for (int s = 0; s < ka.n_splits; ++s) M = fmaxf(M, part[s * (D + 4)]);
+  float x[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) x[e] = 0.f;
+  float L = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < ka.n_splits; ++s) {
+      const float ms = part[s * (D + 4)];
+      if (ms == -INFINITY) continue;
+      const float w = expf(ms - M);
+      L = fmaf(part[s * (D + 4) + 1], w, L);
+#pragma unroll
+      for (int e = 0; e < E; ++e) x[e] = fmaf(part[s * (D + 4) + 4 + E * lane + e], w, x[e]);
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) x[e] *= inv;
+  if (a.v.format != TQ_FMT_Q8_0) {
+    warp_wht<D>(x, lane);
+#pragma unroll
+    for (int e = 0; e < E; ++e) x[e] *= (float)ka.tab.signs[E * lane + e];
+  }
+  float* dst = a.out + row * D;
+#pragma unroll
+  for (int e = 0; e < E; ++e) dst[E * lane + e] = x[e];
+}
+
+template <int D>
+cudaError_t launch_decode_dim(const DecodeKernelArgs& ka, cudaStream_t s) {
+  const DecodeArgs& a = ka.a;
+  const unsigned rows = (unsigned)((long long)a.n_layers * a.batch * a.n_q_heads);
+  qprep_kernel<D><<<rows, 32, 0, s>>>(ka);
+  dim3 grid(ka.n_splits, a.k.H, a.n_layers * a.batch);
+  const size_t smem = (3 * (size_t)ka.G * D + 16) * sizeof(float);
+  if (smem > 48 * 1024) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(attend_generic_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  attend_generic_kernel<D><<<grid, 32, smem, s>>>(ka);
+  combine_kernel<D><<<rows, 32, 0, s>>>(ka);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DevTables& t, const DecodeArgs& a, const DecodePlan& plan, void* workspace,
+                          int sm_count, cudaStream_t s) {
+  (void)sm_count;
+  DecodeKernelArgs ka;
+  ka.a = a;
+  ka.tab = t;
+  ka.split_tokens = plan.split_tokens;
+  ka.n_splits = plan.n_splits;
+  ka.G = a.n_q_heads / a.k.H;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  ka.qprep = reinterpret_cast<float*>(ws);
+  ka.partial = reinterpret_cast<float*>(ws + (plan.qprep_floats * 4 + 255) / 256 * 256);
+  switch (t.d) {
+    case 64: return launch_decode_dim<64>(ka, s);
+    case 128: return launch_decode_dim<128>(ka, s);
+    case 256: return launch_decode_dim<256>(ka, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace tq

@@ -1,0 +1,106 @@
+// Internal declarations shared by the host API (tq_api.cpp) and the CUDA
+// translation units.  Not part of the public ABI (see include/tq.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/tq.h"
+
+namespace tq {
+
+// Status-word bits written by kernels (documented in tq_get_status).
+enum : uint32_t { kFlagSeqLen = 1u, kFlagBlockTable = 2u, kFlagSlot = 4u };
+
+// Highest supported head_dim and codebook sizes.
+constexpr int kMaxDim = 256;
+constexpr int kMaxLevels = 8;  // turbo stage 1 uses at most 3 bits
+
+// Plain-old-data description of a cache view, passed by value to kernels.
+struct DevView {
+  int format;       // tq_format
+  int d;            // head_dim
+  int H;            // n_kv_heads
+  int page_size;
+  long long num_pages;
+  int n_layers;
+  int idx_bits;     // stage-1 index bits (turbo), or minmax bits, or 8 (q8_0)
+  int code_bits;    // bits per coordinate in the payload (turbo K: idx_bits + 1)
+  int has_qjl;      // turbo K formats
+  int pay_bytes;    // payload bytes per vector
+  int hdr_bytes;    // header bytes per vector
+  unsigned char* payload;
+  unsigned char* header;
+};
+
+// Device tables owned by a context.
+struct DevTables {
+  int d;
+  const int8_t* signs;       // [d]
+  const float* S;            // [d][d], row j = projection j
+  const float* S_T;          // [d][d], S_T[i][j] = S[j][i]
+  const float* centroids;    // [3][8]  (bits 1, 2, 3)
+  const float* boundaries;   // [3][7]
+  uint32_t* status;          // device status word
+};
+
+bool format_is_turbo(int f);
+bool format_has_qjl(int f);
+int format_idx_bits(int f, int minmax_bits);
+
+// Fills a DevView from a public view; returns false if the view is invalid.
+bool make_dev_view(const tq_cache_view* v, DevView* out);
+
+// ---- launchers (defined in the .cu files); all return cudaGetLastError() ----
+cudaError_t launch_encode(const DevTables& t, const DevView& view, const __half* x, int layer_begin,
+                          int n_layers, int n_tokens, long long layer_stride, long long token_stride,
+                          const long long* slots, long long slot_begin, int sm_count, cudaStream_t s);
+
+cudaError_t launch_dequant(const DevTables& t, const DevView& view, int layer, const long long* slots,
+                           long long slot_begin, int n, int include_qjl, float* out, cudaStream_t s);
+
+struct DecodeArgs {
+  const void* q;
+  int q_is_fp16;
+  int n_layers, batch, n_q_heads;
+  DevView k, v;
+  int layer_begin;
+  const int32_t* seq_lens;
+  int max_ctx;
+  const int32_t* block_table;
+  int max_blocks_per_seq;
+  float softmax_scale, skip_threshold;
+  float* out;
+};
+
+// Split-K plan for a decode call: tokens per split and the number of splits.
+struct DecodePlan {
+  int split_tokens;
+  int n_splits;
+  size_t partial_floats;   // floats of split-K partials
+  size_t qprep_floats;     // floats of prepared queries
+  size_t bytes;            // total workspace bytes (256-byte aligned parts)
+};
+DecodePlan plan_decode(int sm_count, int d, int n_layers, int batch, int n_q_heads, int max_ctx);
+
+cudaError_t launch_decode(const DevTables& t, const DecodeArgs& a, const DecodePlan& plan,
+                          void* workspace, int sm_count, cudaStream_t s);
+
+}  // namespace tq
+
+struct tq_context {
+  int device;
+  int d;
+  int sm_count;
+  // host copies
+  int8_t signs_h[tq::kMaxDim];
+  float centroids_h[3][8];
+  float boundaries_h[3][7];
+  float* S_h;  // [d*d]
+  // device allocations
+  void* dev_block;  // one allocation holding every table
+  tq::DevTables tables;
+};
