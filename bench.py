@@ -56,6 +56,24 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
 
 
+def reduce_max(values, device=None):
+    """Elementwise max of per-rank timings over the default process group (identity
+    without one).  Timing only: the data path has no collective (weak scaling)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def weak_scaling_value(bytes_per_rank, world, seconds_max):
+    """Whole-job throughput: the bytes every rank processed over the slowest rank's time."""
+    return world * bytes_per_rank / seconds_max / 1e9
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -310,11 +328,7 @@ def main():
     t_enc = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps / 1e3
     t_dec = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps / 1e3
     t_step = sum(e[0].elapsed_time(e[2]) for e in ev) / args.steps / 1e3
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([t_enc, t_dec, t_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_enc, t_dec, t_step = tt.tolist()
+    t_enc, t_dec, t_step = reduce_max([t_enc, t_dec, t_step], dev)
 
     # end to end through the C ABI with pinned host buffers
     k_host = w["k_chunk"].cpu().pin_memory()
@@ -340,11 +354,7 @@ def main():
     e1.record(stream)
     barrier()
     t_e2e = e0.elapsed_time(e1) / e2e_steps / 1e3
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([t_e2e], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = tt.item()
+    t_e2e = reduce_max([t_e2e], dev)[0]
     ok, flags = tq.tq_get_status(w["ctx"])
     assert ok == tq.TQ_OK, f"device status flags {flags}"
 
@@ -354,7 +364,7 @@ def main():
         return
     peaks, peak_src = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    value = world * dbytes / t_dec / 1e9
+    value = weak_scaling_value(dbytes, world, t_dec)
     achieved = dbytes / t_dec / 1e9
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -384,7 +394,7 @@ def main():
                                "over all 32 layers",
                      "traffic": profiled_traffic(os.path.join(ROOT, "kv_cache_quantization_turbo_gb300", "csrc",
                                                               "tq_decode.cu"))},
-        "e2e": {"value": round(world * dbytes / t_e2e / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(weak_scaling_value(dbytes, world, t_e2e), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 3),
                 "what": "per step: H2D of the 4096-token K/V chunk (all layers) and q, encode, decode, D2H of out;"
                         " value = decode bytes / full step time"},

@@ -43,13 +43,7 @@ DecodePlan plan_decode(int sm_count, int d, int n_layers, int batch, int n_q_hea
 
 namespace {
 
-struct DecodeKernelArgs {
-  DecodeArgs a;
-  DevTables tab;
-  int split_tokens, n_splits, G;
-  float* qprep;     // [rows][2d]
-  float* partial;   // [rows][n_splits][d + 4]: m, l, -, -, acc[d]
-};
+using DecodeKernelArgs = DecodeLaunch;
 
 // ---------------------------------------------------------------------------
 // 1. query prologue
@@ -100,12 +94,8 @@ __global__ void __launch_bounds__(32) qprep_kernel(DecodeKernelArgs ka) {
 }
 
 // ---------------------------------------------------------------------------
-// token addressing shared by the attention kernels
+// token addressing of the generic kernel
 // ---------------------------------------------------------------------------
-struct SeqInfo {
-  int len;  // clamped sequence length
-};
-
 __device__ __forceinline__ int clamp_seq_len(const DecodeArgs& a, int b, uint32_t* status) {
   int len = a.seq_lens[b];
   if (len < 0) len = 0;
@@ -332,10 +322,16 @@ __global__ void __launch_bounds__(32) combine_kernel(DecodeKernelArgs ka) {
 }
 
 template <int D>
-cudaError_t launch_decode_dim(const DecodeKernelArgs& ka, cudaStream_t s) {
+cudaError_t launch_decode_dim(const DecodeKernelArgs& ka, int sm_count, cudaStream_t s) {
   const DecodeArgs& a = ka.a;
   const unsigned rows = (unsigned)((long long)a.n_layers * a.batch * a.n_q_heads);
   qprep_kernel<D><<<rows, 32, 0, s>>>(ka);
+  if (attend_fast_supported(ka)) {
+    const cudaError_t e = launch_attend_fast(ka, sm_count, s);
+    if (e != cudaSuccess) return e;
+    combine_kernel<D><<<rows, 32, 0, s>>>(ka);
+    return cudaGetLastError();
+  }
   dim3 grid(ka.n_splits, a.k.H, a.n_layers * a.batch);
   const size_t smem = (3 * (size_t)ka.G * D + 16) * sizeof(float);
   if (smem > 48 * 1024) {
@@ -352,7 +348,6 @@ cudaError_t launch_decode_dim(const DecodeKernelArgs& ka, cudaStream_t s) {
 
 cudaError_t launch_decode(const DevTables& t, const DecodeArgs& a, const DecodePlan& plan, void* workspace,
                           int sm_count, cudaStream_t s) {
-  (void)sm_count;
   DecodeKernelArgs ka;
   ka.a = a;
   ka.tab = t;
@@ -363,9 +358,9 @@ cudaError_t launch_decode(const DevTables& t, const DecodeArgs& a, const DecodeP
   ka.qprep = reinterpret_cast<float*>(ws);
   ka.partial = reinterpret_cast<float*>(ws + (plan.qprep_floats * 4 + 255) / 256 * 256);
   switch (t.d) {
-    case 64: return launch_decode_dim<64>(ka, s);
-    case 128: return launch_decode_dim<128>(ka, s);
-    case 256: return launch_decode_dim<256>(ka, s);
+    case 64: return launch_decode_dim<64>(ka, sm_count, s);
+    case 128: return launch_decode_dim<128>(ka, sm_count, s);
+    case 256: return launch_decode_dim<256>(ka, sm_count, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -89,6 +89,20 @@ DecodePlan plan_decode(int sm_count, int d, int n_layers, int batch, int n_q_hea
 cudaError_t launch_decode(const DevTables& t, const DecodeArgs& a, const DecodePlan& plan,
                           void* workspace, int sm_count, cudaStream_t s);
 
+// Everything the decode kernels receive (by value).
+struct DecodeLaunch {
+  DecodeArgs a;
+  DevTables tab;
+  int split_tokens, n_splits, G;
+  float* qprep;    // [rows][2d]: q' then Sq'
+  float* partial;  // [rows][n_splits][d + 4]: m (natural log units), l, -, -, acc[d]
+};
+
+// Fast split-K attention (tensor-core contraction over LUT-dequantised tiles)
+// for the formats and shapes it covers; the generic kernel handles the rest.
+bool attend_fast_supported(const DecodeLaunch& k);
+cudaError_t launch_attend_fast(const DecodeLaunch& k, int sm_count, cudaStream_t s);
+
 }  // namespace tq
 
 struct tq_context {

@@ -1,0 +1,181 @@
+"""Parity at the benchmark recipes' full sizes, on sampled outputs the oracle can compute.
+
+Each test builds the whole workload on the GPU (all layers, full context) and
+runs decode attention in one launch set over all layers, as bench.py does; the
+oracle then recomputes sampled (layer, KV head) slices from the same fp16
+inputs (regenerated from their seeds on the same device and copied to the
+host) and the outputs of every query head of those slices must agree within
+2e-3.  Encoded codes are also checked bit-exactly on sampled slices.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from kv_cache_quantization_turbo_gb300 import tq
+from kv_cache_quantization_turbo_gb300 import workloads as W
+from oracle import tq_oracle as O
+import gpu_common as C
+
+pytestmark = pytest.mark.gpu
+
+
+def _slice_attention(q_rows, k16, v16, kfmt, vfmt, signs, S, d, tau=0.0):
+    """Oracle attention of one KV head: q_rows [G, d], k16/v16 [T, d] fp16."""
+    ek = C.oracle_encode(kfmt, k16[:, None, :], signs, S)
+    ev = C.oracle_encode(vfmt, v16[:, None, :], signs, S)
+    kt = C.oracle_dequant(kfmt, ek, signs, S)
+    vt = C.oracle_dequant(vfmt, ev, signs, S)
+    o_full, o_skip = O.decode_attention(q_rows.astype(np.float64), kt, vt, 1.0 / math.sqrt(d), tau)
+    return o_full, o_skip, ek
+
+
+def test_llama3_8b_32k_turbo4_bench_configuration():
+    """32 layers x 8 KV heads x 32768 tokens, d 128, 32 query heads, turbo4 / turbo4_mse,
+    built and decoded exactly as bench.py does (one decode call over all layers)."""
+    C.require_cuda()
+    import bench
+    dev = torch.device("cuda", 0)
+    w = bench.build_workload(tq, W, torch, dev)
+    wl = w["wl"]
+    try:
+        stream = torch.cuda.current_stream()
+        bench.encode_step(tq, w, w["k_chunk"], w["v_chunk"], stream)
+        bench.decode_step(tq, w, w["q"], w["out"], stream)
+        torch.cuda.synchronize()
+        st, flags = tq.tq_get_status(w["ctx"])
+        assert st == tq.TQ_OK, flags
+        G = wl.n_q_heads // wl.n_kv_heads
+        for layer, kvh in ((0, 3), (31, 6)):
+            k = W.kv_tensor(wl.ctx, wl.n_kv_heads, wl.head_dim, seed=wl.seed * 1000 + 2 * layer, device=dev,
+                            outlier_frac=wl.outlier_frac)[:, kvh].cpu().numpy()
+            v = W.kv_tensor(wl.ctx, wl.n_kv_heads, wl.head_dim, seed=wl.seed * 1000 + 2 * layer + 1, device=dev,
+                            outlier_frac=wl.outlier_frac)[:, kvh].cpu().numpy()
+            q = w["q"][layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
+            o_full, _, ek = _slice_attention(q, k, v, wl.k_format, wl.v_format, w["signs"], w["S"], wl.head_dim,
+                                             1e-6)
+            got = w["out"][layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
+            assert C.rel_err_per_head(got, o_full).max() < C.ATTN_RTOL
+            # codes of this slice (the last 4096 tokens were re-encoded by the timed step)
+            pay, hdr = C.read_vectors(w["kview"], layer)
+            C.check_turbo_codes(wl.k_format, wl.head_dim, pay[0, kvh][:, None], hdr[0, kvh][:, None],
+                                {k_: v_ for k_, v_ in ek.items()})
+    finally:
+        tq.tq_context_destroy(w["ctx"])
+
+
+def test_llama_70b_128k_turbo4_sampled():
+    """80 layers x 8 KV heads x 131072 tokens (9.9 GB compressed), 64 query heads (GQA 8),
+    generated layer by layer; one decode call over all 80 layers."""
+    C.require_cuda()
+    wl = W.WORKLOADS["llama-70b-128k-turbo4"]
+    L, H, d, T, Hq = wl.n_layers, wl.n_kv_heads, wl.head_dim, wl.ctx, wl.n_q_heads
+    ctx = C.Ctx(d, wl.wht_seed, wl.qjl_seed)
+    try:
+        kview = tq.alloc_view(wl.k_format, d, H, page_size=T, num_pages=1, n_layers=L)
+        vview = tq.alloc_view(wl.v_format, d, H, page_size=T, num_pages=1, n_layers=L)
+        for l in range(L):
+            k = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * l, device="cuda", outlier_frac=wl.outlier_frac)
+            v = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * l + 1, device="cuda", outlier_frac=wl.outlier_frac)
+            st = tq.tq_encode_kv(ctx.h, kview, k, vview, v, l, 1, T, T * H * d, H * d)
+            assert st == tq.TQ_OK
+            del k, v
+        q = W.normal_tensor((L, 1, Hq, d), seed=wl.seed * 1000 + 999, device="cuda")
+        out = C.decode(ctx, q, kview, vview, [T], T, tau=1e-6)
+        G = Hq // H
+        for layer, kvh in ((40, 5),):
+            k = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * layer, device="cuda",
+                            outlier_frac=wl.outlier_frac)[:, kvh].cpu().numpy()
+            v = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * layer + 1, device="cuda",
+                            outlier_frac=wl.outlier_frac)[:, kvh].cpu().numpy()
+            qs = q[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
+            o_full, _, _ = _slice_attention(qs, k, v, wl.k_format, wl.v_format, ctx.signs, ctx.S, d, 1e-6)
+            got = out[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
+            assert C.rel_err_per_head(got, o_full).max() < C.ATTN_RTOL
+    finally:
+        ctx.close()
+
+
+def test_asymmetric_boundary_layers_needles_sampled():
+    """64 layers x 4 KV heads x 32768 tokens, 32 query heads (GQA 8): K q8_0; V turbo2_mse
+    except the first 2 and last 2 layers (q8_0); queries aligned with 16 needles x8;
+    skip threshold 1e-6.  One decode call per V-format group."""
+    C.require_cuda()
+    wl = W.WORKLOADS["asym-q8k-turbo2v-needles"]
+    L, H, d, T, Hq = wl.n_layers, wl.n_kv_heads, wl.head_dim, wl.ctx, wl.n_q_heads
+    G = Hq // H
+    boundary = sorted(wl.v_format_layers)
+    middle = [l for l in range(L) if l not in wl.v_format_layers]
+    ctx = C.Ctx(d, wl.wht_seed, wl.qjl_seed)
+    try:
+        kb = tq.alloc_view("q8_0", d, H, page_size=T, num_pages=1, n_layers=len(boundary))
+        vb = tq.alloc_view("q8_0", d, H, page_size=T, num_pages=1, n_layers=len(boundary))
+        km = tq.alloc_view("q8_0", d, H, page_size=T, num_pages=1, n_layers=len(middle))
+        vm = tq.alloc_view(wl.v_format, d, H, page_size=T, num_pages=1, n_layers=len(middle))
+        qs = torch.empty((L, 1, Hq, d), dtype=torch.float32, device="cuda")
+        for l in range(L):
+            k, q, _ = W.needle_workload(T, H, Hq, d, seed=wl.seed * 1000 + 2 * l, device="cuda")
+            v = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * l + 1, device="cuda")
+            qs[l, 0] = q
+            if l in wl.v_format_layers:
+                st = tq.tq_encode_kv(ctx.h, kb, k, vb, v, boundary.index(l), 1, T, T * H * d, H * d)
+            else:
+                st = tq.tq_encode_kv(ctx.h, km, k, vm, v, middle.index(l), 1, T, T * H * d, H * d)
+            assert st == tq.TQ_OK
+        out_b = C.decode(ctx, qs[boundary], kb, vb, [T], T, tau=1e-6)
+        out_m = C.decode(ctx, qs[middle], km, vm, [T], T, tau=1e-6)
+        for layer, kvh in ((1, 2), (30, 0)):
+            k, _, _ = W.needle_workload(T, H, Hq, d, seed=wl.seed * 1000 + 2 * layer, device="cuda")
+            v = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * layer + 1, device="cuda")
+            vfmt = wl.v_format_layers.get(layer, wl.v_format)
+            q_rows = qs[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
+            o_full, o_skip, _ = _slice_attention(q_rows, k[:, kvh].cpu().numpy(), v[:, kvh].cpu().numpy(), "q8_0",
+                                                 vfmt, ctx.signs, ctx.S, d, 1e-6)
+            got = (out_b[boundary.index(layer)] if layer in wl.v_format_layers else out_m[middle.index(layer)])
+            got = got[0, kvh * G:(kvh + 1) * G].cpu().numpy()
+            assert C.rel_err_per_head(got, o_full).max() < C.ATTN_RTOL
+    finally:
+        ctx.close()
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_paged_batch64_turbo3_sampled(d):
+    """64 sequences with context ~ U[1K, 16K], 32 layers x 8 KV heads, 32 query heads,
+    turbo3 / turbo3_mse in 16-token pages with a shuffled block table."""
+    C.require_cuda()
+    wl = W.WORKLOADS["paged-batch64-turbo3"]
+    L, H, Hq, B, P = wl.n_layers, wl.n_kv_heads, wl.n_q_heads, wl.batch, wl.page_size
+    G = Hq // H
+    lens = W.seq_lens_uniform(B, 1024, 16384, wl.seed)
+    bt, npages = W.shuffled_block_table(lens, P, wl.seed)
+    ctx = C.Ctx(d, wl.wht_seed, wl.qjl_seed)
+    try:
+        kview = tq.alloc_view(wl.k_format, d, H, page_size=P, num_pages=npages, n_layers=L)
+        vview = tq.alloc_view(wl.v_format, d, H, page_size=P, num_pages=npages, n_layers=L)
+        # slot of every (sequence, token): block_table page * P + in-page offset
+        slots = np.concatenate([bt[b, np.arange(lens[b]) // P] * P + np.arange(lens[b]) % P for b in range(B)])
+        slots_d = torch.as_tensor(slots.astype(np.int64), device="cuda")
+        T_all = int(lens.sum())
+        for l in range(L):
+            k = W.kv_tensor(T_all, H, d, seed=wl.seed * 1000 + 2 * l, device="cuda")
+            v = W.kv_tensor(T_all, H, d, seed=wl.seed * 1000 + 2 * l + 1, device="cuda")
+            st = tq.tq_encode_kv(ctx.h, kview, k, vview, v, l, 1, T_all, T_all * H * d, H * d, slots_d)
+            assert st == tq.TQ_OK
+            del k, v
+        q = W.normal_tensor((L, B, Hq, d), seed=wl.seed * 1000 + 999, device="cuda")
+        out = C.decode(ctx, q, kview, vview, lens, int(lens.max()), block_table=bt, max_blocks=bt.shape[1])
+        offs = np.concatenate([[0], np.cumsum(lens)])
+        for layer, b, kvh in ((3, 0, 1), (17, 37, 7)):
+            k = W.kv_tensor(T_all, H, d, seed=wl.seed * 1000 + 2 * layer, device="cuda")[offs[b]:offs[b + 1], kvh]
+            v = W.kv_tensor(T_all, H, d, seed=wl.seed * 1000 + 2 * layer + 1, device="cuda")[offs[b]:offs[b + 1],
+                                                                                                 kvh]
+            q_rows = q[layer, b, kvh * G:(kvh + 1) * G].cpu().numpy()
+            o_full, _, _ = _slice_attention(q_rows, k.cpu().numpy(), v.cpu().numpy(), wl.k_format, wl.v_format,
+                                            ctx.signs, ctx.S, d)
+            got = out[layer, b, kvh * G:(kvh + 1) * G].cpu().numpy()
+            assert C.rel_err_per_head(got, o_full).max() < C.ATTN_RTOL
+        st, flags = tq.tq_get_status(ctx.h)
+        assert st == tq.TQ_OK, flags
+    finally:
+        ctx.close()

@@ -81,16 +81,23 @@ def test_encode_scattered_slots_multi_layer(ctx128, fmt):
 
 
 def test_encode_zero_and_single_vectors(ctx128):
+    """Zero vectors (every rotated coordinate exactly 0: the tie rule decides, identically on
+    both sides), a basis vector, and the all-ones vector, whose rotated coordinates are
+    multiples of 1/d and so often sit exactly on the middle boundary (band rule)."""
     d, H = 128, 2
     x = torch.zeros((3, H, d), dtype=torch.float16, device="cuda")
     x[1, 0, 5] = 1.0
     x[2, 1] = 1.0
+    zero = np.array([[True, True], [False, True], [True, False]])
     for fmt in ("turbo3", "turbo2_mse"):
         view = tq.alloc_view(fmt, d, H, page_size=3, num_pages=1)
         C.encode(ctx128, view, x, is_k=fmt in TURBO_K)
         pay, hdr = C.read_vectors(view)
         enc = O.turbo_encode(x.cpu().numpy(), fmt, ctx128.signs, ctx128.S)
-        C.check_turbo_codes(fmt, d, pay[0].transpose(1, 0, 2), hdr[0].transpose(1, 0, 2), enc, exact=True)
+        pay, hdr = pay[0].transpose(1, 0, 2), hdr[0].transpose(1, 0, 2)
+        C.check_turbo_codes(fmt, d, pay[zero], hdr[zero], {k: v[zero] for k, v in enc.items()}, exact=True)
+        C.check_turbo_codes(fmt, d, pay[~zero], hdr[~zero], {k: v[~zero] for k, v in enc.items()},
+                            band_limit=False)
 
 
 def test_encode_q8_0_bit_exact(ctx):
