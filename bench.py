@@ -48,6 +48,8 @@ def parse():
     p.add_argument("--impl", default="tq", choices=["tq", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target seconds of timed oracle work")
+    p.add_argument("--layers", type=int, default=0,
+                   help="use only this many layers (small cases for profiler captures; 0 = all)")
     return p.parse_args()
 
 
@@ -155,8 +157,11 @@ class ClockSampler:
 # workload construction (device)
 # ---------------------------------------------------------------------------
 
-def build_workload(tq, W, torch, dev):
+def build_workload(tq, W, torch, dev, layers=0):
+    import dataclasses
     wl = W.WORKLOADS[WORKLOAD]
+    if layers:
+        wl = dataclasses.replace(wl, n_layers=layers)
     L, H, d, T, Hq, chunk = wl.n_layers, wl.n_kv_heads, wl.head_dim, wl.ctx, wl.n_q_heads, wl.encode_chunk
     signs, S = W.wht_signs(wl.wht_seed, d), W.qjl_matrix(wl.qjl_seed, d)
     ctx = tq.tq_context_create(d, wl.wht_seed, wl.qjl_seed, signs, S)
@@ -299,7 +304,7 @@ def main():
     from kv_cache_quantization_turbo_gb300 import tq
     from kv_cache_quantization_turbo_gb300 import workloads as W
 
-    w = build_workload(tq, W, torch, dev)
+    w = build_workload(tq, W, torch, dev, args.layers)
     wl = w["wl"]
     stream = torch.cuda.current_stream(dev)
     dbytes = decode_bytes(tq, wl)
@@ -381,7 +386,8 @@ def main():
                    "q_heads": wl.n_q_heads, "head_dim": wl.head_dim, "ctx": wl.ctx, "batch": 1,
                    "k_format": wl.k_format, "v_format": wl.v_format, "encode_chunk": wl.encode_chunk,
                    "skip_threshold": 1e-6, "decode_bytes_per_step": dbytes,
-                   "l2": "inputs larger than L2: each decode step sweeps all 32 layers (0.99 GB)"},
+                   "l2": f"inputs larger than L2: each decode step sweeps all {wl.n_layers} layers "
+                         f"({dbytes / 1e9:.2f} GB > 129 MB)"},
         "pct_hbm_peak": {"measured": round(100 * achieved / hbm, 2), "nominal": round(100 * achieved /
                                                                                        NOMINAL_HBM_GBS, 2)},
         "decode_tokens_per_s": round(world / t_dec, 2),
@@ -391,7 +397,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "peak_source": f"{peak_src} hbm_gbs",
                      "kernel": "decode attention call (prologue + split-K attention + combine), one launch set "
-                               "over all 32 layers",
+                               f"over all {wl.n_layers} layers",
                      "traffic": profiled_traffic(os.path.join(ROOT, "kv_cache_quantization_turbo_gb300", "csrc",
                                                               "tq_decode.cu"))},
         "e2e": {"value": round(weak_scaling_value(dbytes, world, t_e2e), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,

@@ -164,6 +164,32 @@ tq_status tq_codebook_build(int bits, int head_dim, float* centroids, float* bou
   return TQ_OK;
 }
 
+// Scale lambda in [1, 2) that makes every lambda * |centroid| (an fp32 product)
+// round to fp16 with the smallest worst relative error.  The tensor-core decode
+// kernel keeps codebook values in fp16 tables; plain rounding errs by up to
+// 2^-11 relative, the same for every token with the same index, so it does not
+// average out.  With lambda chosen over 2^20 candidates the worst error is
+// ~1e-5; the kernel divides lambda back out of the per-token norm.
+static float best_f16_scale(const float* c, int L) {
+  float best = 1.0f;
+  double best_err = 1e30;
+  for (int i = 0; i < (1 << 20); ++i) {
+    const float lam = 1.0f + (float)i * 0x1.0p-20f;
+    double worst = 0.0;
+    for (int k = L / 2; k < L; ++k) {
+      const float p = lam * c[k];
+      const float h = __half2float(__float2half_rn(p));
+      worst = std::fmax(worst, std::fabs((double)h - (double)p) / std::fabs((double)p));
+      if (worst >= best_err) break;
+    }
+    if (worst < best_err) {
+      best_err = worst;
+      best = lam;
+    }
+  }
+  return best;
+}
+
 // ---------------------------------------------------------------------------
 // default random tables (SplitMix64, counter based)
 // ---------------------------------------------------------------------------
@@ -223,16 +249,20 @@ tq_status tq_context_create(int head_dim, uint32_t wht_seed, uint32_t qjl_seed, 
   else tq_qjl_matrix_generate(qjl_seed, d, ctx->S_h);
   std::memset(ctx->centroids_h, 0, sizeof(ctx->centroids_h));
   std::memset(ctx->boundaries_h, 0, sizeof(ctx->boundaries_h));
-  for (int b = 1; b <= 3; ++b) tq_codebook_build(b, d, ctx->centroids_h[b - 1], ctx->boundaries_h[b - 1]);
+  for (int b = 1; b <= 3; ++b) {
+    tq_codebook_build(b, d, ctx->centroids_h[b - 1], ctx->boundaries_h[b - 1]);
+    ctx->f16_scale_h[b - 1] = best_f16_scale(ctx->centroids_h[b - 1], 1 << b);
+  }
 
-  // one device block: status | signs | centroids | boundaries | S | S_T
+  // one device block: status | signs | centroids | boundaries | f16 scales | S | S_T
   const size_t off_signs = 256, off_cent = off_signs + 256, off_bnd = off_cent + 256,
-               off_S = off_bnd + 256, off_ST = off_S + sizeof(float) * d * d,
+               off_scale = off_bnd + 256, off_S = off_scale + 256, off_ST = off_S + sizeof(float) * d * d,
                total = off_ST + sizeof(float) * d * d;
   std::vector<unsigned char> host(total, 0);
   std::memcpy(host.data() + off_signs, ctx->signs_h, d);
   std::memcpy(host.data() + off_cent, ctx->centroids_h, sizeof(ctx->centroids_h));
   std::memcpy(host.data() + off_bnd, ctx->boundaries_h, sizeof(ctx->boundaries_h));
+  std::memcpy(host.data() + off_scale, ctx->f16_scale_h, sizeof(ctx->f16_scale_h));
   std::memcpy(host.data() + off_S, ctx->S_h, sizeof(float) * d * d);
   float* st = reinterpret_cast<float*>(host.data() + off_ST);
   for (int j = 0; j < d; ++j)
@@ -254,6 +284,7 @@ tq_status tq_context_create(int head_dim, uint32_t wht_seed, uint32_t qjl_seed, 
   ctx->tables.signs = reinterpret_cast<const int8_t*>(base + off_signs);
   ctx->tables.centroids = reinterpret_cast<const float*>(base + off_cent);
   ctx->tables.boundaries = reinterpret_cast<const float*>(base + off_bnd);
+  ctx->tables.f16_scale = reinterpret_cast<const float*>(base + off_scale);
   ctx->tables.S = reinterpret_cast<const float*>(base + off_S);
   ctx->tables.S_T = reinterpret_cast<const float*>(base + off_ST);
   *out = ctx;

@@ -44,6 +44,7 @@ struct DevTables {
   const float* S_T;          // [d][d], S_T[i][j] = S[j][i]
   const float* centroids;    // [3][8]  (bits 1, 2, 3)
   const float* boundaries;   // [3][7]
+  const float* f16_scale;    // [3]: lambda per bit width, so that lambda * centroid is (nearly) an fp16 value
   uint32_t* status;          // device status word
 };
 
@@ -113,6 +114,7 @@ struct tq_context {
   int8_t signs_h[tq::kMaxDim];
   float centroids_h[3][8];
   float boundaries_h[3][7];
+  float f16_scale_h[3];
   float* S_h;  // [d*d]
   // device allocations
   void* dev_block;  // one allocation holding every table

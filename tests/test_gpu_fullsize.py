@@ -21,14 +21,24 @@ import gpu_common as C
 pytestmark = pytest.mark.gpu
 
 
-def _slice_attention(q_rows, k16, v16, kfmt, vfmt, signs, S, d, tau=0.0):
-    """Oracle attention of one KV head: q_rows [G, d], k16/v16 [T, d] fp16."""
+def _slice_attention(q_rows, k16, v16, kfmt, vfmt, signs, S, d, tau=0.0, want_bound=False):
+    """Oracle attention of one KV head: q_rows [G, d], k16/v16 [T, d] fp16.
+
+    With want_bound, also returns per query head the weighted norm of the V terms the
+    oracle's Sparse-V rule drops, sum_{p_j < tau} p_j ||v~_j||."""
     ek = C.oracle_encode(kfmt, k16[:, None, :], signs, S)
     ev = C.oracle_encode(vfmt, v16[:, None, :], signs, S)
     kt = C.oracle_dequant(kfmt, ek, signs, S)
     vt = C.oracle_dequant(vfmt, ev, signs, S)
     o_full, o_skip = O.decode_attention(q_rows.astype(np.float64), kt, vt, 1.0 / math.sqrt(d), tau)
-    return o_full, o_skip, ek
+    if not want_bound:
+        return o_full, o_skip, ek
+    s = (q_rows.astype(np.float64) @ kt[:, 0, :].T) / math.sqrt(d)
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    vn = np.linalg.norm(vt[:, 0, :], axis=-1)
+    bound = np.sum(np.where(p < tau, p, 0.0) * vn[None, :], axis=1)
+    return o_full, o_skip, ek, bound
 
 
 def test_llama3_8b_32k_turbo4_bench_configuration():
@@ -47,16 +57,29 @@ def test_llama3_8b_32k_turbo4_bench_configuration():
         st, flags = tq.tq_get_status(w["ctx"])
         assert st == tq.TQ_OK, flags
         G = wl.n_q_heads // wl.n_kv_heads
+        out_skip = w["out"].clone()
+        # the same call without Sparse V, for the 2e-3 parity check
+        out_full = torch.empty_like(w["out"])
+        st = tq.tq_decode_attention(w["ctx"], w["q"], 0, wl.n_layers, 1, wl.n_q_heads, w["kview"], w["vview"], 0,
+                                    w["seq_lens"], wl.ctx, None, 0, 1.0 / math.sqrt(wl.head_dim), 0.0, w["ws"],
+                                    w["ws_bytes"], out_full)
+        assert st == tq.TQ_OK
+        torch.cuda.synchronize()
         for layer, kvh in ((0, 3), (31, 6)):
             k = W.kv_tensor(wl.ctx, wl.n_kv_heads, wl.head_dim, seed=wl.seed * 1000 + 2 * layer, device=dev,
                             outlier_frac=wl.outlier_frac)[:, kvh].cpu().numpy()
             v = W.kv_tensor(wl.ctx, wl.n_kv_heads, wl.head_dim, seed=wl.seed * 1000 + 2 * layer + 1, device=dev,
                             outlier_frac=wl.outlier_frac)[:, kvh].cpu().numpy()
             q = w["q"][layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
-            o_full, _, ek = _slice_attention(q, k, v, wl.k_format, wl.v_format, w["signs"], w["S"], wl.head_dim,
-                                             1e-6)
-            got = w["out"][layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
+            o_full, _, ek, bound = _slice_attention(q, k, v, wl.k_format, wl.v_format, w["signs"], w["S"],
+                                                    wl.head_dim, 1e-6, want_bound=True)
+            got = out_full[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
             assert C.rel_err_per_head(got, o_full).max() < C.ATTN_RTOL
+            # Sparse V (threshold 1e-6, the timed configuration): the kernel drops a subset of the
+            # terms the oracle's rule drops, so it stays within their weighted norm of o_full
+            got_skip = out_skip[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
+            dev_ = np.linalg.norm(got_skip - o_full, axis=-1)
+            assert np.all(dev_ <= bound + C.ATTN_RTOL * np.linalg.norm(o_full, axis=-1))
             # codes of this slice (the last 4096 tokens were re-encoded by the timed step)
             pay, hdr = C.read_vectors(w["kview"], layer)
             C.check_turbo_codes(wl.k_format, wl.head_dim, pay[0, kvh][:, None], hdr[0, kvh][:, None],
@@ -82,7 +105,7 @@ def test_llama_70b_128k_turbo4_sampled():
             assert st == tq.TQ_OK
             del k, v
         q = W.normal_tensor((L, 1, Hq, d), seed=wl.seed * 1000 + 999, device="cuda")
-        out = C.decode(ctx, q, kview, vview, [T], T, tau=1e-6)
+        out = C.decode(ctx, q, kview, vview, [T], T, tau=0.0)
         G = Hq // H
         for layer, kvh in ((40, 5),):
             k = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * layer, device="cuda",
