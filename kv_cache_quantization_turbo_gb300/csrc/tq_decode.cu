@@ -28,8 +28,11 @@ static int next_pow2(long long v) {
 
 DecodePlan plan_decode(int sm_count, int d, int n_layers, int batch, int n_q_heads, int max_ctx) {
   DecodePlan p{};
-  const long long per_sm = ((long long)max_ctx * n_layers * batch + 2LL * sm_count - 1) / (2LL * sm_count);
-  int st = next_pow2(per_sm);
+  // Split size: aim at ~6 work items per warp of the fast kernel (16 warps per SM,
+  // query heads shared by about 4 per KV head), between 256 and 4096 tokens.
+  const long long work = (long long)max_ctx * n_layers * batch * n_q_heads;
+  const long long per_item = (work + 4LL * 16 * 6 * sm_count - 1) / (4LL * 16 * 6 * sm_count);
+  int st = next_pow2(per_item);
   st = st < 256 ? 256 : (st > 4096 ? 4096 : st);
   p.split_tokens = st;
   p.n_splits = max_ctx > 0 ? (max_ctx + st - 1) / st : 1;
@@ -37,7 +40,7 @@ DecodePlan plan_decode(int sm_count, int d, int n_layers, int batch, int n_q_hea
   p.qprep_floats = (size_t)rows * 2 * d;
   p.partial_floats = (size_t)rows * p.n_splits * (d + 4);
   auto al = [](size_t b) { return (b + 255) / 256 * 256; };
-  p.bytes = al(p.qprep_floats * 4) + al(p.partial_floats * 4);
+  p.bytes = al(p.qprep_floats * 4) + al(p.partial_floats * 4) + 256;  // + work counter
   return p;
 }
 
@@ -54,6 +57,7 @@ __global__ void __launch_bounds__(32) qprep_kernel(DecodeKernelArgs ka) {
   const DecodeArgs& a = ka.a;
   const int lane = threadIdx.x;
   const long long row = blockIdx.x;  // (layer, batch, q head)
+  if (row == 0 && lane == 0) *ka.counter = 0u;  // work counter of the attention kernel that follows
   __shared__ float q_s[D];
   float x[E];
   if (a.q_is_fp16) {
@@ -357,6 +361,8 @@ cudaError_t launch_decode(const DevTables& t, const DecodeArgs& a, const DecodeP
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   ka.qprep = reinterpret_cast<float*>(ws);
   ka.partial = reinterpret_cast<float*>(ws + (plan.qprep_floats * 4 + 255) / 256 * 256);
+  ka.counter = reinterpret_cast<unsigned int*>(ws + (plan.qprep_floats * 4 + 255) / 256 * 256 +
+                                               (plan.partial_floats * 4 + 255) / 256 * 256);
   switch (t.d) {
     case 64: return launch_decode_dim<64>(ka, sm_count, s);
     case 128: return launch_decode_dim<128>(ka, sm_count, s);

@@ -52,11 +52,13 @@ struct EncArgs {
 // Global vector id -> (input layer, token, head) and the destination index
 // in the view (-1 if the slot is out of range; the status word is flagged).
 __device__ __forceinline__ long long enc_locate(const EncArgs& a, long long gv, const __half** src) {
-  const int H = a.view.H;
-  const int h = (int)(gv % H);
-  const long long lt = gv / H;
-  const int t = (int)(lt % a.n_tokens);
-  const int l = (int)(lt / a.n_tokens);
+  // vector counts stay below 2^32 (checked on the host): 32-bit division is enough
+  const unsigned int H = (unsigned int)a.view.H, v32 = (unsigned int)gv;
+  const unsigned int lt = v32 / H;
+  const int h = (int)(v32 - lt * H);
+  const unsigned int l32 = lt / (unsigned int)a.n_tokens;
+  const int t = (int)(lt - l32 * (unsigned int)a.n_tokens);
+  const int l = (int)l32;
   *src = a.x + l * a.layer_stride + t * a.token_stride + (long long)h * a.view.d;
   const long long slot = a.slots ? a.slots[t] : a.slot_begin + t;
   const long long v = view_vector_index(a.view, a.layer_begin + l, slot, h);
@@ -94,8 +96,9 @@ __device__ __forceinline__ float stage1_rotate(float (&x)[D / 32], const int8_t*
 #pragma unroll
   for (int e = 0; e < E; ++e) ss = fmaf(x[e], x[e], ss);
   const float n = sqrtf(warp_sum(ss));
+  const float inv = n > 0.f ? 1.0f / n : 0.f;
 #pragma unroll
-  for (int e = 0; e < E; ++e) x[e] = n > 0.f ? (x[e] / n) * (float)signs_s[E * lane + e] : 0.f;
+  for (int e = 0; e < E; ++e) x[e] = (x[e] * inv) * (float)signs_s[E * lane + e];
   warp_wht<D>(x, lane);
   return n;
 }

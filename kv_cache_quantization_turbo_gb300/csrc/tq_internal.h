@@ -97,6 +97,7 @@ struct DecodeLaunch {
   int split_tokens, n_splits, G;
   float* qprep;    // [rows][2d]: q' then Sq'
   float* partial;  // [rows][n_splits][d + 4]: m (natural log units), l, -, -, acc[d]
+  unsigned int* counter;  // work-item counter (zeroed by the prologue kernel)
 };
 
 // Fast split-K attention (tensor-core contraction over LUT-dequantised tiles)

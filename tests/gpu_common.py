@@ -171,3 +171,18 @@ def rel_err_per_head(got, want):
     num = np.linalg.norm(got - want, axis=-1)
     den = np.maximum(np.linalg.norm(want, axis=-1), 1e-30)
     return num / den
+
+
+def codes_agree(fmt, d, gpu_pay, enc):
+    """Per vector: do the GPU's stored codes equal the oracle's (indices and QJL signs)?
+
+    Codes may legitimately differ inside the 1e-6 boundary band (check_turbo_codes
+    enforces that); attention parity is then judged only where they agree, because
+    one flipped code of a heavily weighted token moves that head's output."""
+    codes = unpack_codes(gpu_pay, d, code_bits(fmt))
+    idx, sigma = split_turbo(codes, fmt)
+    ok = np.all(idx == enc["idx"], axis=-1)
+    if sigma is not None:
+        ok &= np.all(sigma == enc["sigma"], axis=-1)
+    return ok
+
