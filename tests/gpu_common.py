@@ -109,8 +109,9 @@ def check_turbo_codes(fmt, d, gpu_pay, gpu_hdr, enc, exact=False, band_limit=Tru
     return out
 
 
-def write_oracle_codes(view, enc, fmt, slots, layer=0):
-    """Packs oracle-encoded vectors [n_slots, H, ...] into a view at the given slots."""
+def write_oracle_codes(view, enc, fmt, slots, layer=0, head=None):
+    """Packs oracle-encoded vectors [n_slots, H, ...] into a view at the given slots;
+    with head=h, enc holds one head ([n_slots, 1, ...]) written to KV head h only."""
     torch.cuda.synchronize()
     d, H, P = view.head_dim, view.n_kv_heads, view.page_size
     pb = tq.tq_payload_bytes(fmt, d)
@@ -119,19 +120,20 @@ def write_oracle_codes(view, enc, fmt, slots, layer=0):
     pay = view.payload.view(view.n_layers, n, pb)[layer].cpu().numpy().reshape(view.num_pages, H, P, pb)
     hdr = view.header.view(view.n_layers, n, hb)[layer].cpu().numpy().reshape(view.num_pages, H, P, hb)
     slots = np.asarray(slots)
+    hs = slice(None) if head is None else slice(head, head + 1)
     if fmt == "q8_0":
         q, dl = enc
-        pay[slots // P, :, slots % P] = q.view(np.uint8)
-        hdr[slots // P, :, slots % P] = dl.astype(np.float16).view(np.uint8).reshape(dl.shape[:-1] + (-1,))
+        pay[slots // P, hs, slots % P] = q.view(np.uint8)
+        hdr[slots // P, hs, slots % P] = dl.astype(np.float16).view(np.uint8).reshape(dl.shape[:-1] + (-1,))
     else:
         bits, has_qjl = O.TURBO_FORMATS[fmt]
         codes = join_turbo(enc["idx"], enc.get("sigma"), fmt)
-        pay[slots // P, :, slots % P] = pack_codes(codes, code_bits(fmt))
+        pay[slots // P, hs, slots % P] = pack_codes(codes, code_bits(fmt))
         if has_qjl:
             h = np.stack([enc["n16"], enc["rnorm16"]], axis=-1).astype(np.float16)
         else:
             h = enc["n16"][..., None].astype(np.float16)
-        hdr[slots // P, :, slots % P] = h.view(np.uint8)
+        hdr[slots // P, hs, slots % P] = h.view(np.uint8)
     view.payload.view(view.n_layers, n * pb)[layer].copy_(torch.from_numpy(pay.reshape(-1)))
     view.header.view(view.n_layers, n * hb)[layer].copy_(torch.from_numpy(hdr.reshape(-1)))
 

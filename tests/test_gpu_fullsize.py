@@ -1,11 +1,15 @@
-"""Parity at the benchmark recipes' full sizes, on sampled outputs the oracle can compute.
+"""Parity at the benchmark recipes' full sizes, on sampled (layer, KV head) slices.
 
-Each test builds the whole workload on the GPU (all layers, full context) and
-runs decode attention in one launch set over all layers, as bench.py does; the
-oracle then recomputes sampled (layer, KV head) slices from the same fp16
-inputs (regenerated from their seeds on the same device and copied to the
-host) and the outputs of every query head of those slices must agree within
-2e-3.  Encoded codes are also checked bit-exactly on sampled slices.
+Each test builds the whole workload on the GPU (all layers, full context) with
+the library's encoder and checks the codes of sampled slices against the oracle
+(bit-exact outside the 1e-6 boundary band, headers within 1 ulp).  At these
+sizes every slice holds a few coordinates inside the band, where the two sides
+may legitimately decide differently, and one flipped code of a heavily weighted
+token moves its head's output; so attention parity is judged on identical codes:
+the oracle's codes are written into the sampled slices, decode attention runs
+over all layers in one call (the benchmark's launch configuration), and the
+sampled heads must agree with the oracle's fp64 attention within 2e-3.  Inputs
+are regenerated from their seeds on the same device and copied to the host.
 """
 import math
 
@@ -21,88 +25,83 @@ import gpu_common as C
 pytestmark = pytest.mark.gpu
 
 
-def _slice_attention(q_rows, k16, v16, kfmt, vfmt, signs, S, d, tau=0.0, want_bound=False):
-    """Oracle attention of one KV head: q_rows [G, d], k16/v16 [T, d] fp16.
+def _check_and_replace(view, layer, fmt, x16, kvh, slot_ids, signs, S):
+    """Checks the GPU codes of one slice against the oracle, then writes the oracle's codes
+    there.  x16: fp16 [n, d] of KV head kvh at the given slots.  Returns the oracle encoding."""
+    enc = C.oracle_encode(fmt, x16[:, None, :], signs, S)
+    pay, hdr = C.read_vectors(view, layer)
+    pay = C.slot_major(pay, slot_ids, view.page_size)[:, kvh][:, None]
+    hdr = C.slot_major(hdr, slot_ids, view.page_size)[:, kvh][:, None]
+    if fmt == "q8_0":
+        np.testing.assert_array_equal(pay.view(np.int8), enc[0])
+        np.testing.assert_array_equal(hdr.view(np.float16), enc[1])
+    else:
+        C.check_turbo_codes(fmt, view.head_dim, pay, hdr, enc)
+    C.write_oracle_codes(view, enc, fmt, slot_ids, layer=layer, head=kvh)
+    return enc
 
-    With want_bound, also returns per query head the weighted norm of the V terms the
-    oracle's Sparse-V rule drops, sum_{p_j < tau} p_j ||v~_j||."""
-    ek = C.oracle_encode(kfmt, k16[:, None, :], signs, S)
-    ev = C.oracle_encode(vfmt, v16[:, None, :], signs, S)
+
+def _attention(q_rows, ek, ev, kfmt, vfmt, signs, S, d, tau=0.0):
+    """Oracle attention of one KV head on its codes, q_rows [G, d]; also, per query head,
+    the weighted norm of the V terms the oracle's Sparse-V rule drops,
+    sum over p_j < tau of p_j ||v~_j||."""
     kt = C.oracle_dequant(kfmt, ek, signs, S)
     vt = C.oracle_dequant(vfmt, ev, signs, S)
-    o_full, o_skip = O.decode_attention(q_rows.astype(np.float64), kt, vt, 1.0 / math.sqrt(d), tau)
-    if not want_bound:
-        return o_full, o_skip, ek
-    s = (q_rows.astype(np.float64) @ kt[:, 0, :].T) / math.sqrt(d)
+    q64 = q_rows.astype(np.float64)
+    o_full, _ = O.decode_attention(q64, kt, vt, 1.0 / math.sqrt(d), tau)
+    s = (q64 @ kt[:, 0, :].T) / math.sqrt(d)
     p = np.exp(s - s.max(axis=1, keepdims=True))
     p /= p.sum(axis=1, keepdims=True)
-    vn = np.linalg.norm(vt[:, 0, :], axis=-1)
-    bound = np.sum(np.where(p < tau, p, 0.0) * vn[None, :], axis=1)
-    return o_full, o_skip, ek, bound
+    bound = np.sum(np.where(p < tau, p, 0.0) * np.linalg.norm(vt[:, 0, :], axis=-1)[None, :], axis=1)
+    return o_full, bound
 
 
-def _agrees(view, layer, fmt, enc, slot_ids, kvh):
-    """Whether the GPU codes of one (layer, KV head) slice at the given slots equal the oracle's."""
-    if fmt == "q8_0":
-        return True  # q8_0 is compared bit-exactly elsewhere; no boundary band
-    pay, _ = C.read_vectors(view, layer)
-    pay = C.slot_major(pay, slot_ids, view.page_size)[:, kvh][:, None]
-    return bool(C.codes_agree(fmt, view.head_dim, pay, enc).all())
+def _within_skip_bound(got, o_full, bound):
+    """Sparse V drops a subset of the terms the oracle's rule drops, so the output stays
+    within their weighted norm of the full attention (plus the parity tolerance)."""
+    dev = np.linalg.norm(np.asarray(got, np.float64) - o_full, axis=-1)
+    return bool(np.all(dev <= bound + C.ATTN_RTOL * np.linalg.norm(o_full, axis=-1)))
 
 
 def test_llama3_8b_32k_turbo4_bench_configuration():
     """32 layers x 8 KV heads x 32768 tokens, d 128, 32 query heads, turbo4 / turbo4_mse,
-    built and decoded exactly as bench.py does (one decode call over all layers)."""
+    built, re-encoded and decoded exactly as bench.py does (one decode call over all layers)."""
     C.require_cuda()
     import bench
     dev = torch.device("cuda", 0)
     w = bench.build_workload(tq, W, torch, dev)
     wl = w["wl"]
+    d, H, T = wl.head_dim, wl.n_kv_heads, wl.ctx
+    G = wl.n_q_heads // H
     try:
         stream = torch.cuda.current_stream()
-        bench.encode_step(tq, w, w["k_chunk"], w["v_chunk"], stream)
-        bench.decode_step(tq, w, w["q"], w["out"], stream)
+        bench.encode_step(tq, w, w["k_chunk"], w["v_chunk"], stream)  # the timed encode (last 4096 tokens)
         torch.cuda.synchronize()
-        st, flags = tq.tq_get_status(w["ctx"])
-        assert st == tq.TQ_OK, flags
-        G = wl.n_q_heads // wl.n_kv_heads
+        assert tq.tq_get_status(w["ctx"])[0] == tq.TQ_OK
+        refs = {}
+        for layer, kvh in ((0, 3), (31, 6)):
+            k = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * layer, device=dev,
+                            outlier_frac=wl.outlier_frac)[:, kvh].cpu().numpy()
+            v = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * layer + 1, device=dev,
+                            outlier_frac=wl.outlier_frac)[:, kvh].cpu().numpy()
+            ek = _check_and_replace(w["kview"], layer, wl.k_format, k, kvh, np.arange(T), w["signs"], w["S"])
+            ev = _check_and_replace(w["vview"], layer, wl.v_format, v, kvh, np.arange(T), w["signs"], w["S"])
+            q = w["q"][layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
+            refs[layer, kvh] = _attention(q, ek, ev, wl.k_format, wl.v_format, w["signs"], w["S"], d, 1e-6)
+        bench.decode_step(tq, w, w["q"], w["out"], stream)  # the timed decode: Sparse V at 1e-6
+        torch.cuda.synchronize()
         out_skip = w["out"].clone()
-        # the same call without Sparse V, for the 2e-3 parity check
         out_full = torch.empty_like(w["out"])
         st = tq.tq_decode_attention(w["ctx"], w["q"], 0, wl.n_layers, 1, wl.n_q_heads, w["kview"], w["vview"], 0,
-                                    w["seq_lens"], wl.ctx, None, 0, 1.0 / math.sqrt(wl.head_dim), 0.0, w["ws"],
-                                    w["ws_bytes"], out_full)
+                                    w["seq_lens"], T, None, 0, 1.0 / math.sqrt(d), 0.0, w["ws"], w["ws_bytes"],
+                                    out_full)
         assert st == tq.TQ_OK
         torch.cuda.synchronize()
-        checked = 0
-        for layer, kvh in ((0, 3), (31, 6), (7, 0), (19, 5), (25, 2)):
-            if checked == 2:
-                break
-            k = W.kv_tensor(wl.ctx, wl.n_kv_heads, wl.head_dim, seed=wl.seed * 1000 + 2 * layer, device=dev,
-                            outlier_frac=wl.outlier_frac)[:, kvh].cpu().numpy()
-            v = W.kv_tensor(wl.ctx, wl.n_kv_heads, wl.head_dim, seed=wl.seed * 1000 + 2 * layer + 1, device=dev,
-                            outlier_frac=wl.outlier_frac)[:, kvh].cpu().numpy()
-            q = w["q"][layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
-            o_full, _, ek, bound = _slice_attention(q, k, v, wl.k_format, wl.v_format, w["signs"], w["S"],
-                                                    wl.head_dim, 1e-6, want_bound=True)
-            # codes of this slice: bit-exact outside the band (the last 4096 tokens were re-encoded
-            # by the timed step); attention parity is judged on slices whose codes all agree
-            pay, hdr = C.read_vectors(w["kview"], layer)
-            C.check_turbo_codes(wl.k_format, wl.head_dim, pay[0, kvh][:, None], hdr[0, kvh][:, None], ek)
-            ev = C.oracle_encode(wl.v_format, v[:, None, :], w["signs"], None)
-            vpay, _ = C.read_vectors(w["vview"], layer)
-            if not (C.codes_agree(wl.k_format, wl.head_dim, pay[0, kvh][:, None], ek).all() and
-                    C.codes_agree(wl.v_format, wl.head_dim, vpay[0, kvh][:, None], ev).all()):
-                continue
-            checked += 1
+        assert tq.tq_get_status(w["ctx"])[0] == tq.TQ_OK
+        for (layer, kvh), (o_full, bound) in refs.items():
             got = out_full[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
             assert C.rel_err_per_head(got, o_full).max() < C.ATTN_RTOL
-            # Sparse V (threshold 1e-6, the timed configuration): the kernel drops a subset of the
-            # terms the oracle's rule drops, so it stays within their weighted norm of o_full
-            got_skip = out_skip[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
-            dev_ = np.linalg.norm(got_skip - o_full, axis=-1)
-            assert np.all(dev_ <= bound + C.ATTN_RTOL * np.linalg.norm(o_full, axis=-1))
-        assert checked == 2
+            assert _within_skip_bound(out_skip[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy(), o_full, bound)
     finally:
         tq.tq_context_destroy(w["ctx"])
 
@@ -113,6 +112,7 @@ def test_llama_70b_128k_turbo4_sampled():
     C.require_cuda()
     wl = W.WORKLOADS["llama-70b-128k-turbo4"]
     L, H, d, T, Hq = wl.n_layers, wl.n_kv_heads, wl.head_dim, wl.ctx, wl.n_q_heads
+    G = Hq // H
     ctx = C.Ctx(d, wl.wht_seed, wl.qjl_seed)
     try:
         kview = tq.alloc_view(wl.k_format, d, H, page_size=T, num_pages=1, n_layers=L)
@@ -124,27 +124,21 @@ def test_llama_70b_128k_turbo4_sampled():
             assert st == tq.TQ_OK
             del k, v
         q = W.normal_tensor((L, 1, Hq, d), seed=wl.seed * 1000 + 999, device="cuda")
-        out = C.decode(ctx, q, kview, vview, [T], T, tau=0.0)
-        G = Hq // H
-        checked = 0
-        for layer, kvh in ((40, 5), (79, 1), (3, 6)):
-            if checked == 1:
-                break
+        refs = {}
+        for layer, kvh in ((40, 5), (79, 1)):
             k = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * layer, device="cuda",
                             outlier_frac=wl.outlier_frac)[:, kvh].cpu().numpy()
             v = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * layer + 1, device="cuda",
                             outlier_frac=wl.outlier_frac)[:, kvh].cpu().numpy()
-            qs = q[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
-            o_full, _, ek = _slice_attention(qs, k, v, wl.k_format, wl.v_format, ctx.signs, ctx.S, d, 1e-6)
-            ev = C.oracle_encode(wl.v_format, v[:, None, :], ctx.signs, None)
-            slots = np.arange(T)
-            if not (_agrees(kview, layer, wl.k_format, ek, slots, kvh) and
-                    _agrees(vview, layer, wl.v_format, ev, slots, kvh)):
-                continue
-            checked += 1
+            ek = _check_and_replace(kview, layer, wl.k_format, k, kvh, np.arange(T), ctx.signs, ctx.S)
+            ev = _check_and_replace(vview, layer, wl.v_format, v, kvh, np.arange(T), ctx.signs, ctx.S)
+            refs[layer, kvh] = _attention(q[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy(), ek, ev, wl.k_format,
+                                          wl.v_format, ctx.signs, ctx.S, d)[0]
+        out = C.decode(ctx, q, kview, vview, [T], T, tau=0.0)
+        for (layer, kvh), o_full in refs.items():
             got = out[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
             assert C.rel_err_per_head(got, o_full).max() < C.ATTN_RTOL
-        assert checked == 1
+        assert tq.tq_get_status(ctx.h)[0] == tq.TQ_OK
     finally:
         ctx.close()
 
@@ -175,27 +169,24 @@ def test_asymmetric_boundary_layers_needles_sampled():
             else:
                 st = tq.tq_encode_kv(ctx.h, km, k, vm, v, middle.index(l), 1, T, T * H * d, H * d)
             assert st == tq.TQ_OK
-        out_b = C.decode(ctx, qs[boundary], kb, vb, [T], T, tau=1e-6)
-        out_m = C.decode(ctx, qs[middle], km, vm, [T], T, tau=1e-6)
-        checked = 0
-        for layer, kvh in ((1, 2), (30, 0), (40, 3), (62, 1)):
-            if checked == 2:
-                break
+        refs = {}
+        for layer, kvh in ((1, 2), (30, 0)):
             k, _, _ = W.needle_workload(T, H, Hq, d, seed=wl.seed * 1000 + 2 * layer, device="cuda")
             v = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * layer + 1, device="cuda")
             vfmt = wl.v_format_layers.get(layer, wl.v_format)
-            q_rows = qs[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
-            o_full, o_skip, _ = _slice_attention(q_rows, k[:, kvh].cpu().numpy(), v[:, kvh].cpu().numpy(), "q8_0",
-                                                 vfmt, ctx.signs, ctx.S, d, 1e-6)
-            if vfmt != "q8_0":
-                ev = C.oracle_encode(vfmt, v[:, kvh].cpu().numpy()[:, None, :], ctx.signs, None)
-                if not _agrees(vm, middle.index(layer), vfmt, ev, np.arange(T), kvh):
-                    continue
-            checked += 1
-            got = (out_b[boundary.index(layer)] if layer in wl.v_format_layers else out_m[middle.index(layer)])
+            kv_, vv_, li = (kb, vb, boundary.index(layer)) if vfmt == "q8_0" else (km, vm, middle.index(layer))
+            ek = _check_and_replace(kv_, li, "q8_0", k[:, kvh].cpu().numpy(), kvh, np.arange(T), ctx.signs, ctx.S)
+            ev = _check_and_replace(vv_, li, vfmt, v[:, kvh].cpu().numpy(), kvh, np.arange(T), ctx.signs, ctx.S)
+            refs[layer, kvh] = _attention(qs[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy(), ek, ev, "q8_0", vfmt,
+                                          ctx.signs, ctx.S, d, 1e-6)
+        out_b = C.decode(ctx, qs[boundary], kb, vb, [T], T, tau=1e-6)
+        out_m = C.decode(ctx, qs[middle], km, vm, [T], T, tau=1e-6)
+        for (layer, kvh), (o_full, bound) in refs.items():
+            got = out_b[boundary.index(layer)] if layer in wl.v_format_layers else out_m[middle.index(layer)]
             got = got[0, kvh * G:(kvh + 1) * G].cpu().numpy()
+            # peaked softmax: what Sparse V drops is far below the parity tolerance
             assert C.rel_err_per_head(got, o_full).max() < C.ATTN_RTOL
-        assert checked == 2
+            assert _within_skip_bound(got, o_full, bound)
     finally:
         ctx.close()
 
@@ -225,27 +216,21 @@ def test_paged_batch64_turbo3_sampled(d):
             assert st == tq.TQ_OK
             del k, v
         q = W.normal_tensor((L, B, Hq, d), seed=wl.seed * 1000 + 999, device="cuda")
-        out = C.decode(ctx, q, kview, vview, lens, int(lens.max()), block_table=bt, max_blocks=bt.shape[1])
         offs = np.concatenate([[0], np.cumsum(lens)])
-        checked = 0
-        for layer, b, kvh in ((3, 0, 1), (17, 37, 7), (30, 12, 4), (9, 55, 2)):
-            if checked == 2:
-                break
+        refs = {}
+        for layer, b, kvh in ((3, 0, 1), (17, 37, 7)):
+            sl = slots[offs[b]:offs[b + 1]]
             k = W.kv_tensor(T_all, H, d, seed=wl.seed * 1000 + 2 * layer, device="cuda")[offs[b]:offs[b + 1], kvh]
             v = W.kv_tensor(T_all, H, d, seed=wl.seed * 1000 + 2 * layer + 1, device="cuda")[offs[b]:offs[b + 1],
                                                                                                  kvh]
-            q_rows = q[layer, b, kvh * G:(kvh + 1) * G].cpu().numpy()
-            o_full, _, ek = _slice_attention(q_rows, k.cpu().numpy(), v.cpu().numpy(), wl.k_format, wl.v_format,
-                                             ctx.signs, ctx.S, d)
-            ev = C.oracle_encode(wl.v_format, v.cpu().numpy()[:, None, :], ctx.signs, None)
-            sl = slots[offs[b]:offs[b + 1]]
-            if not (_agrees(kview, layer, wl.k_format, ek, sl, kvh) and
-                    _agrees(vview, layer, wl.v_format, ev, sl, kvh)):
-                continue
-            checked += 1
+            ek = _check_and_replace(kview, layer, wl.k_format, k.cpu().numpy(), kvh, sl, ctx.signs, ctx.S)
+            ev = _check_and_replace(vview, layer, wl.v_format, v.cpu().numpy(), kvh, sl, ctx.signs, ctx.S)
+            refs[layer, b, kvh] = _attention(q[layer, b, kvh * G:(kvh + 1) * G].cpu().numpy(), ek, ev, wl.k_format,
+                                             wl.v_format, ctx.signs, ctx.S, d)[0]
+        out = C.decode(ctx, q, kview, vview, lens, int(lens.max()), block_table=bt, max_blocks=bt.shape[1])
+        for (layer, b, kvh), o_full in refs.items():
             got = out[layer, b, kvh * G:(kvh + 1) * G].cpu().numpy()
             assert C.rel_err_per_head(got, o_full).max() < C.ATTN_RTOL
-        assert checked == 2
         st, flags = tq.tq_get_status(ctx.h)
         assert st == tq.TQ_OK, flags
     finally:
