@@ -246,6 +246,32 @@ tq_status tq_decode_attention(const tq_context* ctx,
                               void* workspace, size_t workspace_bytes,
                               float* out, tq_stream_t stream);
 
+/*
+ * tq_decode_attention without a caller workspace, for callers that cannot
+ * allocate device memory when they run decode attention (a process whose
+ * device memory is all reserved by its own pool, code inside an allocator
+ * callback, a plug-in that only receives its inputs and outputs).  The paper
+ * has no counterpart: this is a deployment variant of the same computation.
+ *
+ * Same arguments and result as tq_decode_attention minus the workspace pair.
+ * The workspace is a fixed 16 MiB array inside libtq.so (every GPU that loads
+ * the library keeps it until exit); a call whose tq_decode_workspace_bytes()
+ * exceeds 16 MiB returns TQ_ERR_WORKSPACE and launches nothing.  The first call
+ * on a device looks the array's device address up (with that device current)
+ * and should come before any stream capture.  All calls share the array: calls
+ * that overlap on the GPU race.  The context's device must be current.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+tq_status tq_decode_attention_static(const tq_context* ctx,
+                                     const void* q, int q_is_fp16,
+                                     int n_layers, int batch, int n_q_heads,
+                                     const tq_cache_view* k_view, const tq_cache_view* v_view,
+                                     int layer_begin,
+                                     const int32_t* seq_lens, int max_ctx,
+                                     const int32_t* block_table, int max_blocks_per_seq,
+                                     float softmax_scale, float skip_threshold,
+                                     float* out, tq_stream_t stream);
+
 /* ---- dequantize (reconstruction; test and debugging path) ---- */
 
 /*

@@ -61,6 +61,7 @@ _SIGS = {
     "tq_decode_attention": (_I, [_P, _P, _I, _I, _I, _I, _VP, _VP, _I, _P, _I, _P, _I, _F, _F, _P, _SZ,
                                  _P, _P]),
     "tq_dequantize": (_I, [_P, _VP, _I, _P, _I64, _I, _I, _P, _P]),
+    "tq_decode_attention_static": (_I, [_P, _P, _I, _I, _I, _I, _VP, _VP, _I, _P, _I, _P, _I, _F, _F, _P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -263,6 +264,17 @@ def tq_decode_attention(ctx: int, q, q_is_fp16: int, n_layers: int, batch: int, 
                                     _ptr(seq_lens), max_ctx, _ptr(block_table), max_blocks_per_seq,
                                     softmax_scale, skip_threshold, _ptr(workspace), workspace_bytes, _ptr(out),
                                     _stream(stream))
+
+
+def tq_decode_attention_static(ctx: int, q, q_is_fp16: int, n_layers: int, batch: int, n_q_heads: int, k_view,
+                               v_view, layer_begin: int, seq_lens, max_ctx: int, block_table,
+                               max_blocks_per_seq: int, softmax_scale: float, skip_threshold: float, out,
+                               stream=None) -> int:
+    ka, va = _view_arg(k_view), _view_arg(v_view)
+    return _lib.tq_decode_attention_static(ctx, _ptr(q), q_is_fp16, n_layers, batch, n_q_heads, ka[0], va[0],
+                                           layer_begin, _ptr(seq_lens), max_ctx, _ptr(block_table),
+                                           max_blocks_per_seq, softmax_scale, skip_threshold, _ptr(out),
+                                           _stream(stream))
 
 
 def tq_dequantize(ctx: int, view, layer: int, slots, slot_begin: int, n: int, include_qjl: int, out,
