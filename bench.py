@@ -399,7 +399,7 @@ def main():
                      "kernel": "decode attention call (prologue + split-K attention + combine), one launch set "
                                f"over all {wl.n_layers} layers",
                      "traffic": profiled_traffic(os.path.join(ROOT, "kv_cache_quantization_turbo_gb300", "csrc",
-                                                              "tq_decode.cu"))},
+                                                              "tq_decode_fast.cu"))},
         "e2e": {"value": round(weak_scaling_value(dbytes, world, t_e2e), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 3),
                 "what": "per step: H2D of the 4096-token K/V chunk (all layers) and q, encode, decode, D2H of out;"
