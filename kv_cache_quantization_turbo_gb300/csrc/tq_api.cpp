@@ -254,10 +254,10 @@ tq_status tq_context_create(int head_dim, uint32_t wht_seed, uint32_t qjl_seed, 
     ctx->f16_scale_h[b - 1] = best_f16_scale(ctx->centroids_h[b - 1], 1 << b);
   }
 
-  // one device block: status | signs | centroids | boundaries | f16 scales | S | S_T
+  // one device block: status | signs | centroids | boundaries | f16 scales | S | S_T | S fragments
   const size_t off_signs = 256, off_cent = off_signs + 256, off_bnd = off_cent + 256,
                off_scale = off_bnd + 256, off_S = off_scale + 256, off_ST = off_S + sizeof(float) * d * d,
-               total = off_ST + sizeof(float) * d * d;
+               off_SF = off_ST + sizeof(float) * d * d, total = off_SF + sizeof(uint32_t) * d * d;
   std::vector<unsigned char> host(total, 0);
   std::memcpy(host.data() + off_signs, ctx->signs_h, d);
   std::memcpy(host.data() + off_cent, ctx->centroids_h, sizeof(ctx->centroids_h));
@@ -267,6 +267,30 @@ tq_status tq_context_create(int head_dim, uint32_t wht_seed, uint32_t qjl_seed, 
   float* st = reinterpret_cast<float*>(host.data() + off_ST);
   for (int j = 0; j < d; ++j)
     for (int i = 0; i < d; ++i) st[i * d + j] = ctx->S_h[j * d + i];
+  {
+    // hi/lo fp16 split of S in B-fragment order (tensor-core projection of the encoder)
+    uint32_t* sf = reinterpret_cast<uint32_t*>(host.data() + off_SF);
+    auto pair = [&](int row, int col, bool lo) -> uint32_t {
+      uint32_t r = 0;
+      for (int k = 0; k < 2; ++k) {
+        const float v = ctx->S_h[row * d + col + k];
+        const __half h = __float2half_rn(v);
+        const __half x = lo ? __float2half_rn(v - __half2float(h)) : h;
+        r |= (uint32_t)__half_as_ushort(x) << (16 * k);
+      }
+      return r;
+    };
+    for (int nb = 0; nb < d / 8; ++nb)
+      for (int ks = 0; ks < d / 16; ++ks)
+        for (int lane = 0; lane < 32; ++lane) {
+          const int row = 8 * nb + lane / 4, col = 16 * ks + 2 * (lane % 4);
+          uint32_t* e = sf + 4 * ((size_t)(nb * (d / 16) + ks) * 32 + lane);
+          e[0] = pair(row, col, false);
+          e[1] = pair(row, col + 8, false);
+          e[2] = pair(row, col, true);
+          e[3] = pair(row, col + 8, true);
+        }
+  }
   if (cudaMalloc(&ctx->dev_block, total) != cudaSuccess) {
     std::free(ctx->S_h);
     delete ctx;
@@ -287,6 +311,7 @@ tq_status tq_context_create(int head_dim, uint32_t wht_seed, uint32_t qjl_seed, 
   ctx->tables.f16_scale = reinterpret_cast<const float*>(base + off_scale);
   ctx->tables.S = reinterpret_cast<const float*>(base + off_S);
   ctx->tables.S_T = reinterpret_cast<const float*>(base + off_ST);
+  ctx->tables.S_frag = reinterpret_cast<const uint4*>(base + off_SF);
   *out = ctx;
   return TQ_OK;
 }

@@ -10,12 +10,21 @@
 //
 // Work decomposition
 //   - one warp per vector for everything but the QJL projection; lane l holds
-//     the E = d/32 consecutive coordinates [E l, E l + E);
+//     the E = d/32 consecutive coordinates [E l, E l + E); the sign flips, the
+//     codebook boundaries and the WHT butterfly signs live in registers;
+//   - the Lloyd-Max index is a binary search over the sorted boundaries (the
+//     count of boundaries <= y, ties included as the definition has it);
+//   - codes are packed by warp shuffles: lane l forms the E w-bit codes of its
+//     coordinates as one chunk, and lane j gathers the chunks that overlap
+//     32-bit word j of the little-endian stream;
 //   - turbo K: a CTA encodes a batch of NV = 8192/d vectors: phase A (warps:
-//     stage 1 and the residual r into shared memory), phase B (the whole CTA:
-//     the d x d projection S r for every vector of the batch, each thread a
-//     register tile of 8 vectors x 4 projections streaming S^T rows through
-//     the L1 cache), phase C (warps: pack codes and store);
+//     stage 1, the residual r into shared memory), phase B (the whole CTA: the
+//     d x d projection S r on mma.sync m16n8k16, f16 inputs split into high and
+//     low parts, r_hi s_hi + r_lo s_hi + r_hi s_lo accumulated in fp32, which
+//     leaves an error near 1e-7 of |r|, far inside the 1e-6 sign band), phase C
+//     (warps: pack codes and store);
+//   - vector ids -> (layer, token, head) and slots -> (page, offset) use
+//     multiply-shift division by invariant divisors;
 //   - grids are persistent: min(work, resident CTAs) CTAs loop over batches.
 #include <cuda_fp16.h>
 
@@ -28,14 +37,33 @@ enum EncKind { kTurboK = 0, kTurboV = 1, kQ8 = 2, kMinMax = 3 };
 
 constexpr int kEncThreads = 256;
 constexpr int kEncWarps = kEncThreads / 32;
-constexpr int kVPT = 8;  // vectors per thread in the projection tile
+constexpr float kRScale = 16384.0f;  // residual scale before the fp16 split (only signs are kept)
+
+// Unsigned division by an invariant divisor (Granlund-Montgomery, round-up multiplier).
+struct FastDiv {
+  uint32_t d, m;
+  uint32_t s1, s2;
+};
+
+FastDiv make_fastdiv(uint32_t d) {
+  if (d == 0) d = 1;  // never used with 0 (empty calls return before launching)
+  int l = 0;
+  while ((1ull << l) < d) ++l;
+  const uint64_t m = ((1ull << 32) * ((1ull << l) - d)) / d + 1;
+  return FastDiv{d, (uint32_t)m, l ? 1u : 0u, l ? (uint32_t)(l - 1) : 0u};
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+  const uint32_t t = __umulhi(n, f.m);
+  return (t + ((n - t) >> f.s1)) >> f.s2;
+}
 
 template <int D>
 struct EncShape {
   static constexpr int E = D / 32;
-  static constexpr int JG = D / 4;                 // thread groups over projections
-  static constexpr int VG = kEncThreads / JG;      // thread groups over vectors
-  static constexpr int NV = VG * kVPT;             // vectors per batch (turbo K)
+  static constexpr int NV = 8192 / D;   // vectors per batch (turbo K)
+  static constexpr int RS = D + 8;      // row stride of the residual tile (floats)
+  static constexpr int KS = D / 16;     // k steps of the projection
 };
 
 struct EncArgs {
@@ -46,24 +74,38 @@ struct EncArgs {
   long long layer_stride, token_stride;
   const long long* slots;
   long long slot_begin;
-  long long n_vectors;  // n_layers * n_tokens * H
+  long long n_vectors;  // n_layers * n_tokens * H (< 2^32)
+  FastDiv div_h, div_t, div_p;
+  int slot32;           // slot capacity below 2^32: the page division is 32-bit
 };
 
 // Global vector id -> (input layer, token, head) and the destination index
 // in the view (-1 if the slot is out of range; the status word is flagged).
 __device__ __forceinline__ long long enc_locate(const EncArgs& a, long long gv, const __half** src) {
-  // vector counts stay below 2^32 (checked on the host): 32-bit division is enough
-  const unsigned int H = (unsigned int)a.view.H, v32 = (unsigned int)gv;
-  const unsigned int lt = v32 / H;
-  const int h = (int)(v32 - lt * H);
-  const unsigned int l32 = lt / (unsigned int)a.n_tokens;
-  const int t = (int)(lt - l32 * (unsigned int)a.n_tokens);
+  const uint32_t v32 = (uint32_t)gv;
+  const uint32_t lt = fdiv(v32, a.div_h);
+  const int h = (int)(v32 - lt * (uint32_t)a.view.H);
+  const uint32_t l32 = fdiv(lt, a.div_t);
+  const int t = (int)(lt - l32 * (uint32_t)a.n_tokens);
   const int l = (int)l32;
   *src = a.x + l * a.layer_stride + t * a.token_stride + (long long)h * a.view.d;
   const long long slot = a.slots ? a.slots[t] : a.slot_begin + t;
-  const long long v = view_vector_index(a.view, a.layer_begin + l, slot, h);
-  if (v < 0 && h == 0) atomicOr(a.tab.status, kFlagSlot);
-  return v;
+  const DevView& V = a.view;
+  const long long cap = V.num_pages * (long long)V.page_size;
+  if (slot < 0 || slot >= cap) {
+    if (h == 0) atomicOr(a.tab.status, kFlagSlot);
+    return -1;
+  }
+  long long page, p;
+  if (a.slot32) {
+    const uint32_t s32 = (uint32_t)slot, pg = fdiv(s32, a.div_p);
+    page = pg;
+    p = s32 - pg * (uint32_t)V.page_size;
+  } else {
+    page = slot / V.page_size;
+    p = slot - page * V.page_size;
+  }
+  return (((long long)(a.layer_begin + l) * V.num_pages + page) * V.H + h) * V.page_size + p;
 }
 
 template <int D>
@@ -88,47 +130,140 @@ __device__ __forceinline__ void load_vec(const __half* src, float (&x)[D / 32], 
   }
 }
 
-// Stage 1 for one vector held by a warp: returns n and leaves y = H diag(s) x_hat in x.
+// Per-lane constants of stage 1: sign flips of the lane's coordinates and the
+// butterfly signs of the five shuffle stages (-1 on the upper lane of a pair).
 template <int D>
-__device__ __forceinline__ float stage1_rotate(float (&x)[D / 32], const int8_t* signs_s, int lane) {
+struct Stage1Consts {
+  float sgn[D / 32];
+  float bfly[5];
+  __device__ __forceinline__ void init(const int8_t* signs, int lane) {
+    constexpr int E = D / 32;
+#pragma unroll
+    for (int e = 0; e < E; ++e) sgn[e] = (float)signs[E * lane + e];
+#pragma unroll
+    for (int s = 0; s < 5; ++s) bfly[s] = (lane >> s) & 1 ? -1.f : 1.f;
+  }
+};
+
+// Stage 1 for one vector held by a warp: returns n and leaves y = H diag(s) x / n in x
+// (orthonormal H: the butterflies run unscaled and 1/(n sqrt(d)) is applied once).
+template <int D>
+__device__ __forceinline__ float stage1_rotate(float (&x)[D / 32], const Stage1Consts<D>& c) {
   constexpr int E = D / 32;
   float ss = 0.f;
 #pragma unroll
-  for (int e = 0; e < E; ++e) ss = fmaf(x[e], x[e], ss);
-  const float n = sqrtf(warp_sum(ss));
-  const float inv = n > 0.f ? 1.0f / n : 0.f;
+  for (int e = 0; e < E; ++e) {
+    ss = fmaf(x[e], x[e], ss);
+    x[e] *= c.sgn[e];
+  }
 #pragma unroll
-  for (int e = 0; e < E; ++e) x[e] = (x[e] * inv) * (float)signs_s[E * lane + e];
-  warp_wht<D>(x, lane);
+  for (int s = 1; s < E; s <<= 1) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      if ((i & s) == 0) {
+        const float u = x[i], v = x[i + s];
+        x[i] = u + v;
+        x[i + s] = u - v;
+      }
+    }
+  }
+  ss = warp_sum(ss);
+#pragma unroll
+  for (int st = 0; st < 5; ++st) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const float o = __shfl_xor_sync(kFull, x[i], 1 << st);
+      x[i] = fmaf(x[i], c.bfly[st], o);  // lower lane: x + o, upper lane: o - x
+    }
+  }
+  const float n = sqrtf(ss);
+  const float f = n > 0.f ? inv_sqrt_dim<D>() / n : 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) x[e] *= f;
   return n;
 }
 
-template <int D, int KIND>
+// Lloyd-Max index of y: the number of sorted boundaries bnd[k] <= y (b bits, 2^b - 1 boundaries).
+template <int B>
+__device__ __forceinline__ uint32_t lloyd_index(float y, const float (&bnd)[7]) {
+  if constexpr (B == 1) {
+    return y >= bnd[0] ? 1u : 0u;
+  } else if constexpr (B == 2) {
+    const bool s1 = y >= bnd[1];
+    const float t0 = s1 ? bnd[2] : bnd[0];
+    return (s1 ? 2u : 0u) + (y >= t0 ? 1u : 0u);
+  } else {
+    const bool s2 = y >= bnd[3];
+    const float t1 = s2 ? bnd[5] : bnd[1];
+    const bool s1 = y >= t1;
+    const float u = s2 ? bnd[4] : bnd[0], v = s2 ? bnd[6] : bnd[2];
+    const float t0 = s1 ? v : u;
+    return (s2 ? 4u : 0u) + (s1 ? 2u : 0u) + (y >= t0 ? 1u : 0u);
+  }
+}
+
+// Stores the packed stream of one vector: lane l holds the E = D/32 codes of its
+// coordinates as chunk = sum_e code_e << (W e) (bits [C l, C l + C) of the stream,
+// C = E W); lane j < E W writes 32-bit word j.
+template <int D, int W>
+__device__ __forceinline__ void pack_store(uint32_t chunk, uint32_t* dst, int lane) {
+  constexpr int E = D / 32, C = E * W, NW = E * W;
+  constexpr int MAXL = (32 + C - 1) / C + 1;
+  const int lfirst = (32 * lane) / C;
+  uint32_t word = 0;
+#pragma unroll
+  for (int k = 0; k < MAXL; ++k) {
+    const int src = lfirst + k;
+    const uint32_t v = __shfl_sync(kFull, chunk, src & 31);
+    const int sh = C * src - 32 * lane;
+    if (src < 32 && sh < 32) word |= sh >= 0 ? (v << sh) : (v >> -sh);
+  }
+  if (lane < NW) dst[lane] = word;
+}
+
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// High and low fp16 parts of a float pair (low element in the low half).
+__device__ __forceinline__ void split_pair(float2 v, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(v.x, v.y);
+  const float2 hf = __half22float2(h);
+  hi = h2u(h);
+  lo = h2u(__floats2half2_rn(v.x - hf.x, v.y - hf.y));
+}
+
+// B = stage-1 index bits (turbo K: the stored code adds the QJL sign as bit B).
+template <int D, int KIND, int B>
 __global__ void __launch_bounds__(kEncThreads) encode_kernel(EncArgs a) {
   using Sh = EncShape<D>;
   constexpr int E = Sh::E;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   extern __shared__ __align__(16) unsigned char smem[];
-  int8_t* signs_s = reinterpret_cast<int8_t*>(smem);                    // [D]
-  float* cb_s = reinterpret_cast<float*>(smem + 256);                  // centroids [8]
-  float* bd_s = cb_s + 8;                                              // boundaries [7]
-  unsigned char* dyn = smem + 512;
+  float* cb_s = reinterpret_cast<float*>(smem);  // centroids [8]
+  unsigned char* dyn = smem + 64;
 
   const DevView& V = a.view;
-  const int b = V.idx_bits;
-  for (int i = threadIdx.x; i < D; i += blockDim.x) signs_s[i] = a.tab.signs[i];
+  Stage1Consts<D> c1;
+  float bnd[7];
   if (KIND == kTurboK || KIND == kTurboV) {
-    if (threadIdx.x < 8) cb_s[threadIdx.x] = a.tab.centroids[(b - 1) * 8 + threadIdx.x];
-    if (threadIdx.x < 7) bd_s[threadIdx.x] = a.tab.boundaries[(b - 1) * 7 + threadIdx.x];
+    c1.init(a.tab.signs, lane);
+#pragma unroll
+    for (int k = 0; k < 7; ++k) bnd[k] = k < (1 << B) - 1 ? a.tab.boundaries[(B - 1) * 7 + k] : 0.f;
+    if (threadIdx.x < 8) cb_s[threadIdx.x] = a.tab.centroids[(B - 1) * 8 + threadIdx.x];
   }
   __syncthreads();
-  const int nb = (1 << b) - 1;
 
   if constexpr (KIND == kTurboK) {
-    constexpr int NV = Sh::NV;
-    float* r_s = reinterpret_cast<float*>(dyn);                            // [NV][D]
-    uint8_t* codes_s = dyn + NV * D * 4;                                   // [NV][D]
+    constexpr int NV = Sh::NV, RS = Sh::RS, KS = Sh::KS;
+    float* r_s = reinterpret_cast<float*>(dyn);                            // [NV][RS] residual x kRScale
+    uint8_t* codes_s = dyn + NV * RS * 4;                                  // [NV][D]
     long long* vid_s = reinterpret_cast<long long*>(codes_s + NV * D);     // [NV]
     const long long n_batches = (a.n_vectors + NV - 1) / NV;
     for (long long bt = blockIdx.x; bt < n_batches; bt += gridDim.x) {
@@ -146,74 +281,91 @@ __global__ void __launch_bounds__(kEncThreads) encode_kernel(EncArgs a) {
 #pragma unroll
           for (int e = 0; e < E; ++e) x[e] = 0.f;
         }
-        const float n = stage1_rotate<D>(x, signs_s, lane);
+        const float n = stage1_rotate<D>(x, c1);
         float rr = 0.f;
+        uint32_t cw[E / 4 > 0 ? E / 4 : 1] = {};
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-          int idx = 0;
-          for (int k = 0; k < nb; ++k) idx += (x[e] >= bd_s[k]) ? 1 : 0;
+          const uint32_t idx = lloyd_index<B>(x[e], bnd);
           const float r = x[e] - cb_s[idx];
           rr = fmaf(r, r, rr);
-          r_s[v * D + E * lane + e] = r;
-          codes_s[v * D + E * lane + e] = (uint8_t)idx;
+          x[e] = r * kRScale;
+          cw[e / 4] |= idx << (8 * (e % 4));
+        }
+        float* rp = r_s + v * RS + E * lane;
+        uint8_t* cp = codes_s + v * D + E * lane;
+        if constexpr (E == 2) {
+          *reinterpret_cast<float2*>(rp) = make_float2(x[0], x[1]);
+          *reinterpret_cast<uint16_t*>(cp) = (uint16_t)cw[0];
+        } else if constexpr (E == 4) {
+          *reinterpret_cast<float4*>(rp) = make_float4(x[0], x[1], x[2], x[3]);
+          *reinterpret_cast<uint32_t*>(cp) = cw[0];
+        } else {
+          *reinterpret_cast<float4*>(rp) = make_float4(x[0], x[1], x[2], x[3]);
+          *reinterpret_cast<float4*>(rp + 4) = make_float4(x[4], x[5], x[6], x[7]);
+          *reinterpret_cast<uint2*>(cp) = make_uint2(cw[0], cw[1]);
         }
         const float rnorm = n * sqrtf(warp_sum(rr));
         if (lane == 0) {
           vid_s[v] = vid;
           if (vid >= 0) {
-            __half2 hd = __halves2half2(__float2half_rn(n), __float2half_rn(rnorm));
+            const __half2 hd = __halves2half2(__float2half_rn(n), __float2half_rn(rnorm));
             *reinterpret_cast<__half2*>(V.header + vid * V.hdr_bytes) = hd;
           }
         }
       }
       __syncthreads();
-      // ---- phase B: sigma_j = [(S r)_j > 0] for the batch ----
+      // ---- phase B: sigma_j = [(S r)_j > 0] for the batch on tensor cores ----
+      // warp: vectors [16 mt, 16 mt + 16) x projections [64 pg, 64 pg + 64)
       {
-        const int tj = threadIdx.x % Sh::JG, tv = threadIdx.x / Sh::JG;
-        float acc[kVPT][4];
+        constexpr int MT = NV / 16;
+        const int mt = warp % MT, pg = warp / MT;
+        const int g = lane >> 2, t = lane & 3;
+        float acc[8][4];
 #pragma unroll
-        for (int v = 0; v < kVPT; ++v)
+        for (int nb = 0; nb < 8; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
+        const float* ra = r_s + (16 * mt + g) * RS + 2 * t;
+        const uint4* sf = a.tab.S_frag + (size_t)(8 * pg) * KS * 32 + lane;
+#pragma unroll 1
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t ahi[4], alo[4];
+          split_pair(*reinterpret_cast<const float2*>(ra + 16 * ks), ahi[0], alo[0]);
+          split_pair(*reinterpret_cast<const float2*>(ra + 8 * RS + 16 * ks), ahi[1], alo[1]);
+          split_pair(*reinterpret_cast<const float2*>(ra + 16 * ks + 8), ahi[2], alo[2]);
+          split_pair(*reinterpret_cast<const float2*>(ra + 8 * RS + 16 * ks + 8), ahi[3], alo[3]);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) acc[v][j] = 0.f;
-        const float* st = a.tab.S_T + 4 * tj;
-        const float* rb = r_s + (kVPT * tv) * D;
-#pragma unroll 2
-        for (int i4 = 0; i4 < D / 4; ++i4) {
-          float4 s4[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) s4[k] = __ldg(reinterpret_cast<const float4*>(st + (4 * i4 + k) * D));
-#pragma unroll
-          for (int v = 0; v < kVPT; ++v) {
-            const float4 r4 = *reinterpret_cast<const float4*>(rb + v * D + 4 * i4);
-            acc[v][0] = fmaf(r4.x, s4[0].x, acc[v][0]); acc[v][1] = fmaf(r4.x, s4[0].y, acc[v][1]);
-            acc[v][2] = fmaf(r4.x, s4[0].z, acc[v][2]); acc[v][3] = fmaf(r4.x, s4[0].w, acc[v][3]);
-            acc[v][0] = fmaf(r4.y, s4[1].x, acc[v][0]); acc[v][1] = fmaf(r4.y, s4[1].y, acc[v][1]);
-            acc[v][2] = fmaf(r4.y, s4[1].z, acc[v][2]); acc[v][3] = fmaf(r4.y, s4[1].w, acc[v][3]);
-            acc[v][0] = fmaf(r4.z, s4[2].x, acc[v][0]); acc[v][1] = fmaf(r4.z, s4[2].y, acc[v][1]);
-            acc[v][2] = fmaf(r4.z, s4[2].z, acc[v][2]); acc[v][3] = fmaf(r4.z, s4[2].w, acc[v][3]);
-            acc[v][0] = fmaf(r4.w, s4[3].x, acc[v][0]); acc[v][1] = fmaf(r4.w, s4[3].y, acc[v][1]);
-            acc[v][2] = fmaf(r4.w, s4[3].z, acc[v][2]); acc[v][3] = fmaf(r4.w, s4[3].w, acc[v][3]);
+          for (int nb = 0; nb < 8; ++nb) {
+            const uint4 b = __ldg(sf + ((size_t)nb * KS + ks) * 32);
+            mma_16816(acc[nb], alo, b.x, b.y);
+            mma_16816(acc[nb], ahi, b.z, b.w);
+            mma_16816(acc[nb], ahi, b.x, b.y);
           }
         }
-        const uint8_t sbit = (uint8_t)(1u << b);
+        const uint8_t sbit = (uint8_t)(1u << B);
+        uint8_t* c0 = codes_s + (16 * mt + g) * D + 64 * pg + 2 * t;
 #pragma unroll
-        for (int v = 0; v < kVPT; ++v)
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (acc[v][j] > 0.f) codes_s[(kVPT * tv + v) * D + 4 * tj + j] |= sbit;
+        for (int nb = 0; nb < 8; ++nb) {
+          if (acc[nb][0] > 0.f) c0[8 * nb] |= sbit;
+          if (acc[nb][1] > 0.f) c0[8 * nb + 1] |= sbit;
+          if (acc[nb][2] > 0.f) c0[8 * D + 8 * nb] |= sbit;
+          if (acc[nb][3] > 0.f) c0[8 * D + 8 * nb + 1] |= sbit;
+        }
       }
       __syncthreads();
       // ---- phase C: pack and store ----
       for (int v = warp; v < NV; v += kEncWarps) {
         const long long vid = vid_s[v];
-        if (vid >= 0)
-          warp_pack_store<D>(codes_s + v * D, V.code_bits,
-                             reinterpret_cast<uint32_t*>(V.payload + vid * V.pay_bytes), lane);
+        if (vid < 0) continue;  // warp-uniform
+        const uint8_t* cp = codes_s + v * D + E * lane;
+        uint32_t chunk = 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) chunk |= (uint32_t)cp[e] << ((B + 1) * e);
+        pack_store<D, B + 1>(chunk, reinterpret_cast<uint32_t*>(V.payload + vid * V.pay_bytes), lane);
       }
       __syncthreads();
     }
   } else {
-    uint8_t* codes_s = dyn + warp * D;  // [warps][D]
+    uint8_t* codes_s = dyn + warp * D;  // [warps][D] (min-max packing)
     const long long gw = (long long)blockIdx.x * kEncWarps + warp;
     const long long nw = (long long)gridDim.x * kEncWarps;
     for (long long gv = gw; gv < a.n_vectors; gv += nw) {
@@ -225,16 +377,12 @@ __global__ void __launch_bounds__(kEncThreads) encode_kernel(EncArgs a) {
       unsigned char* pay = V.payload + vid * V.pay_bytes;
       unsigned char* hdr = V.header + vid * V.hdr_bytes;
       if constexpr (KIND == kTurboV) {
-        const float n = stage1_rotate<D>(x, signs_s, lane);
+        const float n = stage1_rotate<D>(x, c1);
+        uint32_t chunk = 0;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          int idx = 0;
-          for (int k = 0; k < nb; ++k) idx += (x[e] >= bd_s[k]) ? 1 : 0;
-          codes_s[E * lane + e] = (uint8_t)idx;
-        }
+        for (int e = 0; e < E; ++e) chunk |= lloyd_index<B>(x[e], bnd) << (B * e);
         if (lane == 0) *reinterpret_cast<__half*>(hdr) = __float2half_rn(n);
-        __syncwarp();
-        warp_pack_store<D>(codes_s, V.code_bits, reinterpret_cast<uint32_t*>(pay), lane);
+        pack_store<D, B>(chunk, reinterpret_cast<uint32_t*>(pay), lane);
       } else if constexpr (KIND == kQ8) {
         // block of 32 coordinates = 32/E consecutive lanes
         float amax = 0.f;
@@ -268,6 +416,7 @@ __global__ void __launch_bounds__(kEncThreads) encode_kernel(EncArgs a) {
           mn = fminf(mn, __shfl_xor_sync(kFull, mn, m));
           mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, m));
         }
+        const int b = V.idx_bits;
         const int qmax = (1 << b) - 1;
         const float scale = __fdiv_rn(__fsub_rn(mx, mn), (float)qmax);
 #pragma unroll
@@ -291,19 +440,19 @@ __global__ void __launch_bounds__(kEncThreads) encode_kernel(EncArgs a) {
   }
 }
 
-template <int D, int KIND>
+template <int D, int KIND, int B>
 cudaError_t launch_kind(const EncArgs& a, int sm_count, cudaStream_t s) {
-  size_t smem = 512;
+  size_t smem = 64;
   long long work;
   if (KIND == kTurboK) {
-    constexpr int NV = EncShape<D>::NV;
-    smem += (size_t)NV * D * 5 + NV * 8;
-    work = (a.n_vectors + NV - 1) / NV;
+    using Sh = EncShape<D>;
+    smem += (size_t)Sh::NV * Sh::RS * 4 + (size_t)Sh::NV * D + Sh::NV * 8;
+    work = (a.n_vectors + Sh::NV - 1) / Sh::NV;
   } else {
     smem += (size_t)kEncWarps * D;
     work = (a.n_vectors + kEncWarps - 1) / kEncWarps;
   }
-  auto kern = encode_kernel<D, KIND>;
+  auto kern = encode_kernel<D, KIND, B>;
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -317,13 +466,23 @@ cudaError_t launch_kind(const EncArgs& a, int sm_count, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <int D, int KIND>
+cudaError_t launch_bits(const EncArgs& a, int sm_count, cudaStream_t s) {
+  switch (a.view.idx_bits) {
+    case 1: return launch_kind<D, KIND, 1>(a, sm_count, s);
+    case 2: return launch_kind<D, KIND, 2>(a, sm_count, s);
+    case 3: return launch_kind<D, KIND, 3>(a, sm_count, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
 template <int D>
 cudaError_t launch_dim(const EncArgs& a, int sm_count, cudaStream_t s) {
   const int f = a.view.format;
-  if (f == TQ_FMT_Q8_0) return launch_kind<D, kQ8>(a, sm_count, s);
-  if (f == TQ_FMT_MINMAX) return launch_kind<D, kMinMax>(a, sm_count, s);
-  if (a.view.has_qjl) return launch_kind<D, kTurboK>(a, sm_count, s);
-  return launch_kind<D, kTurboV>(a, sm_count, s);
+  if (f == TQ_FMT_Q8_0) return launch_kind<D, kQ8, 1>(a, sm_count, s);
+  if (f == TQ_FMT_MINMAX) return launch_kind<D, kMinMax, 1>(a, sm_count, s);
+  if (a.view.has_qjl) return launch_bits<D, kTurboK>(a, sm_count, s);
+  return launch_bits<D, kTurboV>(a, sm_count, s);
 }
 
 }  // namespace
@@ -343,6 +502,11 @@ cudaError_t launch_encode(const DevTables& t, const DevView& view, const __half*
   a.slots = slots;
   a.slot_begin = slot_begin;
   a.n_vectors = (long long)n_layers * n_tokens * view.H;
+  a.div_h = make_fastdiv((uint32_t)view.H);
+  a.div_t = make_fastdiv((uint32_t)n_tokens);
+  const long long cap = view.num_pages * (long long)view.page_size;
+  a.slot32 = cap <= 0xffffffffLL ? 1 : 0;
+  a.div_p = make_fastdiv((uint32_t)view.page_size);
   switch (view.d) {
     case 64: return launch_dim<64>(a, sm_count, s);
     case 128: return launch_dim<128>(a, sm_count, s);

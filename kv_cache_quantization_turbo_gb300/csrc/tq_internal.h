@@ -42,6 +42,10 @@ struct DevTables {
   const int8_t* signs;       // [d]
   const float* S;            // [d][d], row j = projection j
   const float* S_T;          // [d][d], S_T[i][j] = S[j][i]
+  // S split into high and low fp16 parts (S = hi + lo to ~22 bits) in mma.sync m16n8k16
+  // B-fragment order: entry ((nb * d/16 + ks) * 32 + lane) = {hi(b0), hi(b1), lo(b0), lo(b1)}
+  // with b0 = S[8nb + lane/4][16ks + 2(lane%4) + {0,1}], b1 = the same at + 8 coordinates
+  const uint4* S_frag;
   const float* centroids;    // [3][8]  (bits 1, 2, 3)
   const float* boundaries;   // [3][7]
   const float* f16_scale;    // [3]: lambda per bit width, so that lambda * centroid is (nearly) an fp16 value
