@@ -79,55 +79,88 @@ struct EncArgs {
   int slot32;           // slot capacity below 2^32: the page division is 32-bit
 };
 
-// Global vector id -> (input layer, token, head) and the destination index
-// in the view (-1 if the slot is out of range; the status word is flagged).
-__device__ __forceinline__ long long enc_locate(const EncArgs& a, long long gv, const __half** src) {
-  const uint32_t v32 = (uint32_t)gv;
-  const uint32_t lt = fdiv(v32, a.div_h);
-  const int h = (int)(v32 - lt * (uint32_t)a.view.H);
-  const uint32_t l32 = fdiv(lt, a.div_t);
-  const int t = (int)(lt - l32 * (uint32_t)a.n_tokens);
-  const int l = (int)l32;
-  *src = a.x + l * a.layer_stride + t * a.token_stride + (long long)h * a.view.d;
-  const long long slot = a.slots ? a.slots[t] : a.slot_begin + t;
-  const DevView& V = a.view;
-  const long long cap = V.num_pages * (long long)V.page_size;
-  if (slot < 0 || slot >= cap) {
-    if (h == 0) atomicOr(a.tab.status, kFlagSlot);
-    return -1;
-  }
-  long long page, p;
-  if (a.slot32) {
-    const uint32_t s32 = (uint32_t)slot, pg = fdiv(s32, a.div_p);
-    page = pg;
-    p = s32 - pg * (uint32_t)V.page_size;
-  } else {
-    page = slot / V.page_size;
-    p = slot - page * V.page_size;
-  }
-  return (((long long)(a.layer_begin + l) * V.num_pages + page) * V.H + h) * V.page_size + p;
-}
+// Location of one vector: input address and destination index (-1: skipped).
+struct Loc {
+  const __half* src;
+  long long vid;
+};
 
-template <int D>
-__device__ __forceinline__ void load_vec(const __half* src, float (&x)[D / 32], int lane) {
-  constexpr int E = D / 32;
-  const __half* p = src + E * lane;
-  if constexpr (E == 2) {
-    const __half2 h = *reinterpret_cast<const __half2*>(p);
-    x[0] = __low2float(h); x[1] = __high2float(h);
-  } else if constexpr (E == 4) {
-    const uint2 u = *reinterpret_cast<const uint2*>(p);
-    const __half2 h0 = *reinterpret_cast<const __half2*>(&u.x), h1 = *reinterpret_cast<const __half2*>(&u.y);
-    x[0] = __low2float(h0); x[1] = __high2float(h0); x[2] = __low2float(h1); x[3] = __high2float(h1);
-  } else {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const __half2 h = *reinterpret_cast<const __half2*>(&w[k]);
-      x[2 * k] = __low2float(h); x[2 * k + 1] = __high2float(h);
+// The H vectors of a token share everything but the head: the token's input address and
+// destination (head 0) are kept and reused while consecutive vectors stay in that token.
+struct TokenCache {
+  uint32_t lt = 0xffffffffu;  // layer * n_tokens + token of the cached entry
+  const __half* src0 = nullptr;
+  long long vid0 = -1;
+};
+
+__device__ __forceinline__ Loc locate(const EncArgs& a, uint32_t gv, TokenCache& c, int lane) {
+  const uint32_t lt = fdiv(gv, a.div_h);
+  const uint32_t h = gv - lt * (uint32_t)a.view.H;
+  if (lt != c.lt) {
+    c.lt = lt;
+    const uint32_t l = fdiv(lt, a.div_t);
+    const uint32_t t = lt - l * (uint32_t)a.n_tokens;
+    c.src0 = a.x + (long long)l * a.layer_stride + (long long)t * a.token_stride;
+    const long long slot = a.slots ? a.slots[t] : a.slot_begin + t;
+    const DevView& V = a.view;
+    const long long cap = V.num_pages * (long long)V.page_size;
+    if (slot < 0 || slot >= cap) {
+      if (lane == 0) atomicOr(a.tab.status, kFlagSlot);
+      c.vid0 = -1;
+    } else {
+      long long page, p;
+      if (a.slot32) {
+        const uint32_t s32 = (uint32_t)slot, pg = fdiv(s32, a.div_p);
+        page = pg;
+        p = s32 - pg * (uint32_t)V.page_size;
+      } else {
+        page = slot / V.page_size;
+        p = slot - page * V.page_size;
+      }
+      c.vid0 = (((long long)(a.layer_begin + (int)l) * V.num_pages + page) * V.H) * V.page_size + p;
     }
   }
+  Loc r;
+  r.src = c.src0 + (long long)h * a.view.d;
+  r.vid = c.vid0 < 0 ? -1 : c.vid0 + (long long)h * a.view.page_size;
+  return r;
+}
+
+// Raw fp16 coordinates of one lane (E = D/32 halves), loaded ahead of their use.
+template <int D>
+struct RawVec {
+  static constexpr int E = D / 32;
+  uint32_t w[E / 2];
+  __device__ __forceinline__ void load(const __half* src, int lane) {
+    const __half* p = src + E * lane;
+    if constexpr (E == 2) {
+      w[0] = *reinterpret_cast<const uint32_t*>(p);
+    } else if constexpr (E == 4) {
+      const uint2 u = *reinterpret_cast<const uint2*>(p);
+      w[0] = u.x; w[1] = u.y;
+    } else {
+      const uint4 u = *reinterpret_cast<const uint4*>(p);
+      w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+    }
+  }
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int k = 0; k < E / 2; ++k) w[k] = 0u;
+  }
+  __device__ __forceinline__ void to_float(float (&x)[E]) const {
+#pragma unroll
+    for (int k = 0; k < E / 2; ++k) {
+      const __half2 h = *reinterpret_cast<const __half2*>(&w[k]);
+      x[2 * k] = __low2float(h);
+      x[2 * k + 1] = __high2float(h);
+    }
+  }
+};
+
+// Spreads bits 0..3 of x to bits 0, 2, 4, 6.
+__device__ __forceinline__ uint32_t spread4(uint32_t x) {
+  x = (x | (x << 2)) & 0x33u;
+  return (x | (x << 1)) & 0x55u;
 }
 
 // Per-lane constants of stage 1: sign flips of the lane's coordinates and the
@@ -177,7 +210,7 @@ __device__ __forceinline__ float stage1_rotate(float (&x)[D / 32], const Stage1C
     }
   }
   const float n = sqrtf(ss);
-  const float f = n > 0.f ? inv_sqrt_dim<D>() / n : 0.f;
+  const float f = n > 0.f ? __fdividef(inv_sqrt_dim<D>(), n) : 0.f;  // ~2 ulp: far inside the code band
 #pragma unroll
   for (int e = 0; e < E; ++e) x[e] *= f;
   return n;
@@ -240,7 +273,7 @@ __device__ __forceinline__ void split_pair(float2 v, uint32_t& hi, uint32_t& lo)
 
 // B = stage-1 index bits (turbo K: the stored code adds the QJL sign as bit B).
 template <int D, int KIND, int B>
-__global__ void __launch_bounds__(kEncThreads) encode_kernel(EncArgs a) {
+__global__ void __launch_bounds__(kEncThreads, KIND == kTurboK ? 3 : 4) encode_kernel(EncArgs a) {
   using Sh = EncShape<D>;
   constexpr int E = Sh::E;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -259,60 +292,67 @@ __global__ void __launch_bounds__(kEncThreads) encode_kernel(EncArgs a) {
     if (threadIdx.x < 8) cb_s[threadIdx.x] = a.tab.centroids[(B - 1) * 8 + threadIdx.x];
   }
   __syncthreads();
+  TokenCache tc;
 
   if constexpr (KIND == kTurboK) {
-    constexpr int NV = Sh::NV, RS = Sh::RS, KS = Sh::KS;
+    constexpr int NV = Sh::NV, RS = Sh::RS, KS = Sh::KS, W = B + 1;
+    constexpr int VPW = NV / kEncWarps;                                    // vectors per warp in phases A, C
     float* r_s = reinterpret_cast<float*>(dyn);                            // [NV][RS] residual x kRScale
-    uint8_t* codes_s = dyn + NV * RS * 4;                                  // [NV][D]
-    long long* vid_s = reinterpret_cast<long long*>(codes_s + NV * D);     // [NV]
+    uint32_t* chunk_s = reinterpret_cast<uint32_t*>(dyn + NV * RS * 4);    // [NV][32] index chunks
+    uint32_t* sig_s = chunk_s + NV * 32;                                   // [NV][D/32] QJL sign bits
+    long long* vid_s = reinterpret_cast<long long*>(sig_s + NV * (D / 32));  // [NV]
     const long long n_batches = (a.n_vectors + NV - 1) / NV;
     for (long long bt = blockIdx.x; bt < n_batches; bt += gridDim.x) {
-      const long long base = bt * NV;
-      // ---- phase A: stage 1 and the residual, one warp per vector ----
-      for (int v = warp; v < NV; v += kEncWarps) {
-        const long long gv = base + v;
-        float x[E];
-        long long vid = -1;
-        if (gv < a.n_vectors) {
-          const __half* src;
-          vid = enc_locate(a, gv, &src);
-          load_vec<D>(src, x, lane);
-        } else {
-#pragma unroll
-          for (int e = 0; e < E; ++e) x[e] = 0.f;
+      const long long base = bt * NV + warp * VPW;
+      // ---- phase A: stage 1 and the residual, one warp per vector (next vector's load in flight) ----
+      Loc cur{nullptr, -1};
+      RawVec<D> raw;
+      raw.zero();
+      if (base < a.n_vectors) {
+        cur = locate(a, (uint32_t)base, tc, lane);
+        if (cur.vid >= 0) raw.load(cur.src, lane);
+      }
+#pragma unroll 1
+      for (int i = 0; i < VPW; ++i) {
+        const int v = warp * VPW + i;
+        Loc nxt{nullptr, -1};
+        RawVec<D> rawn;
+        rawn.zero();
+        if (i + 1 < VPW && base + i + 1 < a.n_vectors) {
+          nxt = locate(a, (uint32_t)(base + i + 1), tc, lane);
+          if (nxt.vid >= 0) rawn.load(nxt.src, lane);
         }
+        float x[E];
+        raw.to_float(x);
         const float n = stage1_rotate<D>(x, c1);
         float rr = 0.f;
-        uint32_t cw[E / 4 > 0 ? E / 4 : 1] = {};
+        uint32_t chunk = 0;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
           const uint32_t idx = lloyd_index<B>(x[e], bnd);
           const float r = x[e] - cb_s[idx];
           rr = fmaf(r, r, rr);
           x[e] = r * kRScale;
-          cw[e / 4] |= idx << (8 * (e % 4));
+          chunk |= idx << (W * e);
         }
         float* rp = r_s + v * RS + E * lane;
-        uint8_t* cp = codes_s + v * D + E * lane;
         if constexpr (E == 2) {
           *reinterpret_cast<float2*>(rp) = make_float2(x[0], x[1]);
-          *reinterpret_cast<uint16_t*>(cp) = (uint16_t)cw[0];
-        } else if constexpr (E == 4) {
-          *reinterpret_cast<float4*>(rp) = make_float4(x[0], x[1], x[2], x[3]);
-          *reinterpret_cast<uint32_t*>(cp) = cw[0];
         } else {
           *reinterpret_cast<float4*>(rp) = make_float4(x[0], x[1], x[2], x[3]);
-          *reinterpret_cast<float4*>(rp + 4) = make_float4(x[4], x[5], x[6], x[7]);
-          *reinterpret_cast<uint2*>(cp) = make_uint2(cw[0], cw[1]);
+          if constexpr (E == 8) *reinterpret_cast<float4*>(rp + 4) = make_float4(x[4], x[5], x[6], x[7]);
         }
+        chunk_s[v * 32 + lane] = chunk;
         const float rnorm = n * sqrtf(warp_sum(rr));
         if (lane == 0) {
-          vid_s[v] = vid;
-          if (vid >= 0) {
+          vid_s[v] = cur.vid;
+          if (cur.vid >= 0) {
             const __half2 hd = __halves2half2(__float2half_rn(n), __float2half_rn(rnorm));
-            *reinterpret_cast<__half2*>(V.header + vid * V.hdr_bytes) = hd;
+            *reinterpret_cast<__half2*>(V.header + cur.vid * V.hdr_bytes) = hd;
           }
         }
+        cur = nxt;
+        raw = rawn;
       }
       __syncthreads();
       // ---- phase B: sigma_j = [(S r)_j > 0] for the batch on tensor cores ----
@@ -341,101 +381,145 @@ __global__ void __launch_bounds__(kEncThreads) encode_kernel(EncArgs a) {
             mma_16816(acc[nb], ahi, b.x, b.y);
           }
         }
-        const uint8_t sbit = (uint8_t)(1u << B);
-        uint8_t* c0 = codes_s + (16 * mt + g) * D + 64 * pg + 2 * t;
+        // sign bits by ballot: bit (4g + t) of ballot c of block nb is the sign of
+        // c0: (vector g, projection 8nb + 2t), c1: (g, 2t + 1), c2: (g + 8, 2t), c3: (g + 8, 2t + 1)
+        // lane: vector vv of the tile, projections 32 half + [0, 32) of the warp's 64
+        const int vv = lane & 15, half = lane >> 4, gg = vv & 7;
+        const bool upper = vv >= 8;
+        uint32_t word = 0;
 #pragma unroll
-        for (int nb = 0; nb < 8; ++nb) {
-          if (acc[nb][0] > 0.f) c0[8 * nb] |= sbit;
-          if (acc[nb][1] > 0.f) c0[8 * nb + 1] |= sbit;
-          if (acc[nb][2] > 0.f) c0[8 * D + 8 * nb] |= sbit;
-          if (acc[nb][3] > 0.f) c0[8 * D + 8 * nb + 1] |= sbit;
+        for (int q = 0; q < 4; ++q) {
+          uint32_t b0[4], b1[4];  // ballots of blocks q and 4 + q
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            b0[c] = __ballot_sync(kFull, acc[q][c] > 0.f);
+            b1[c] = __ballot_sync(kFull, acc[4 + q][c] > 0.f);
+          }
+          const uint32_t be = half ? (upper ? b1[2] : b1[0]) : (upper ? b0[2] : b0[0]);
+          const uint32_t bo = half ? (upper ? b1[3] : b1[1]) : (upper ? b0[3] : b0[1]);
+          const uint32_t byte = spread4((be >> (4 * gg)) & 15u) | (spread4((bo >> (4 * gg)) & 15u) << 1);
+          word |= byte << (8 * q);
         }
+        sig_s[(16 * mt + vv) * (D / 32) + 2 * pg + half] = word;
       }
       __syncthreads();
-      // ---- phase C: pack and store ----
-      for (int v = warp; v < NV; v += kEncWarps) {
+      // ---- phase C: codes = index | sign << B, pack and store ----
+#pragma unroll 1
+      for (int i = 0; i < VPW; ++i) {
+        const int v = warp * VPW + i;
         const long long vid = vid_s[v];
         if (vid < 0) continue;  // warp-uniform
-        const uint8_t* cp = codes_s + v * D + E * lane;
-        uint32_t chunk = 0;
+        const uint32_t sbits = (sig_s[v * (D / 32) + (E * lane) / 32] >> ((E * lane) % 32)) & ((1u << E) - 1u);
+        uint32_t chunk = chunk_s[v * 32 + lane];
 #pragma unroll
-        for (int e = 0; e < E; ++e) chunk |= (uint32_t)cp[e] << ((B + 1) * e);
-        pack_store<D, B + 1>(chunk, reinterpret_cast<uint32_t*>(V.payload + vid * V.pay_bytes), lane);
+        for (int e = 0; e < E; ++e) chunk |= ((sbits >> e) & 1u) << (W * e + B);
+        pack_store<D, W>(chunk, reinterpret_cast<uint32_t*>(V.payload + vid * V.pay_bytes), lane);
       }
       __syncthreads();
     }
   } else {
+    // warps take runs of 8 consecutive vectors (whole tokens when H divides 8), the next
+    // vector's load in flight while the current one is encoded
     uint8_t* codes_s = dyn + warp * D;  // [warps][D] (min-max packing)
-    const long long gw = (long long)blockIdx.x * kEncWarps + warp;
+    constexpr int RUN = 8;
     const long long nw = (long long)gridDim.x * kEncWarps;
-    for (long long gv = gw; gv < a.n_vectors; gv += nw) {
-      const __half* src;
-      const long long vid = enc_locate(a, gv, &src);
-      if (vid < 0) continue;  // warp-uniform
-      float x[E];
-      load_vec<D>(src, x, lane);
-      unsigned char* pay = V.payload + vid * V.pay_bytes;
-      unsigned char* hdr = V.header + vid * V.hdr_bytes;
-      if constexpr (KIND == kTurboV) {
-        const float n = stage1_rotate<D>(x, c1);
-        uint32_t chunk = 0;
-#pragma unroll
-        for (int e = 0; e < E; ++e) chunk |= lloyd_index<B>(x[e], bnd) << (B * e);
-        if (lane == 0) *reinterpret_cast<__half*>(hdr) = __float2half_rn(n);
-        pack_store<D, B>(chunk, reinterpret_cast<uint32_t*>(pay), lane);
-      } else if constexpr (KIND == kQ8) {
-        // block of 32 coordinates = 32/E consecutive lanes
-        float amax = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
-#pragma unroll
-        for (int m = 1; m < 32 / E; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, m));
-        const float delta = __fdiv_rn(amax, 127.0f);
-        uint32_t packed[E / 2 > 0 ? E / 2 : 1] = {};
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const float qf = delta > 0.f ? roundf(__fdiv_rn(x[e], delta)) : 0.f;
-          const uint32_t qb = (uint32_t)(uint8_t)(int8_t)(int)qf;
-          packed[e / 4] |= qb << (8 * (e % 4));
-        }
-        if constexpr (E == 2) {
-          reinterpret_cast<uint16_t*>(pay)[lane] = (uint16_t)packed[0];
-        } else if constexpr (E == 4) {
-          reinterpret_cast<uint32_t*>(pay)[lane] = packed[0];
-        } else {
-          reinterpret_cast<uint2*>(pay)[lane] = make_uint2(packed[0], packed[1]);
-        }
-        if ((lane % (32 / E)) == 0)
-          reinterpret_cast<__half*>(hdr)[lane / (32 / E)] = __float2half_rn(delta);
-      } else {  // kMinMax: groups of 64 coordinates = 64/E consecutive lanes
-        float mn = x[0], mx = x[0];
-#pragma unroll
-        for (int e = 1; e < E; ++e) { mn = fminf(mn, x[e]); mx = fmaxf(mx, x[e]); }
-#pragma unroll
-        for (int m = 1; m < 64 / E; m <<= 1) {
-          mn = fminf(mn, __shfl_xor_sync(kFull, mn, m));
-          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, m));
-        }
-        const int b = V.idx_bits;
-        const int qmax = (1 << b) - 1;
-        const float scale = __fdiv_rn(__fsub_rn(mx, mn), (float)qmax);
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          int q = 0;
-          if (scale > 0.f) {
-            const float t = __fadd_rn(__fdiv_rn(__fsub_rn(x[e], mn), scale), 0.5f);
-            q = (int)floorf(t);
-            q = q < 0 ? 0 : (q > qmax ? qmax : q);
-          }
-          codes_s[E * lane + e] = (uint8_t)q;
-        }
-        if ((lane % (64 / E)) == 0)
-          reinterpret_cast<__half2*>(hdr)[lane / (64 / E)] =
-              __halves2half2(__float2half_rn(scale), __float2half_rn(mn));
-        __syncwarp();
-        warp_pack_store<D>(codes_s, V.code_bits, reinterpret_cast<uint32_t*>(pay), lane);
+    long long run = (long long)blockIdx.x * kEncWarps + warp;
+    int i = 0;
+    long long gv = run * RUN;
+    Loc cur{nullptr, -1};
+    RawVec<D> raw;
+    raw.zero();
+    if (gv < a.n_vectors) {
+      cur = locate(a, (uint32_t)gv, tc, lane);
+      if (cur.vid >= 0) raw.load(cur.src, lane);
+    }
+    while (gv < a.n_vectors) {
+      // next vector of this warp
+      long long gn;
+      if (i + 1 < RUN) {
+        gn = gv + 1;
+        ++i;
+      } else {
+        run += nw;
+        gn = run * RUN;
+        i = 0;
       }
-      __syncwarp();
+      Loc nxt{nullptr, -1};
+      RawVec<D> rawn;
+      rawn.zero();
+      if (gn < a.n_vectors) {
+        nxt = locate(a, (uint32_t)gn, tc, lane);
+        if (nxt.vid >= 0) rawn.load(nxt.src, lane);
+      }
+      if (cur.vid >= 0) {  // warp-uniform
+        float x[E];
+        raw.to_float(x);
+        unsigned char* pay = V.payload + cur.vid * V.pay_bytes;
+        unsigned char* hdr = V.header + cur.vid * V.hdr_bytes;
+        if constexpr (KIND == kTurboV) {
+          const float n = stage1_rotate<D>(x, c1);
+          uint32_t chunk = 0;
+#pragma unroll
+          for (int e = 0; e < E; ++e) chunk |= lloyd_index<B>(x[e], bnd) << (B * e);
+          if (lane == 0) *reinterpret_cast<__half*>(hdr) = __float2half_rn(n);
+          pack_store<D, B>(chunk, reinterpret_cast<uint32_t*>(pay), lane);
+        } else if constexpr (KIND == kQ8) {
+          // block of 32 coordinates = 32/E consecutive lanes
+          float amax = 0.f;
+#pragma unroll
+          for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+          for (int m = 1; m < 32 / E; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, m));
+          const float delta = __fdiv_rn(amax, 127.0f);
+          uint32_t packed[E / 2 > 0 ? E / 2 : 1] = {};
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const float qf = delta > 0.f ? roundf(__fdiv_rn(x[e], delta)) : 0.f;
+            const uint32_t qb = (uint32_t)(uint8_t)(int8_t)(int)qf;
+            packed[e / 4] |= qb << (8 * (e % 4));
+          }
+          if constexpr (E == 2) {
+            reinterpret_cast<uint16_t*>(pay)[lane] = (uint16_t)packed[0];
+          } else if constexpr (E == 4) {
+            reinterpret_cast<uint32_t*>(pay)[lane] = packed[0];
+          } else {
+            reinterpret_cast<uint2*>(pay)[lane] = make_uint2(packed[0], packed[1]);
+          }
+          if ((lane % (32 / E)) == 0)
+            reinterpret_cast<__half*>(hdr)[lane / (32 / E)] = __float2half_rn(delta);
+        } else {  // kMinMax: groups of 64 coordinates = 64/E consecutive lanes
+          float mn = x[0], mx = x[0];
+#pragma unroll
+          for (int e = 1; e < E; ++e) { mn = fminf(mn, x[e]); mx = fmaxf(mx, x[e]); }
+#pragma unroll
+          for (int m = 1; m < 64 / E; m <<= 1) {
+            mn = fminf(mn, __shfl_xor_sync(kFull, mn, m));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, m));
+          }
+          const int b = V.idx_bits;
+          const int qmax = (1 << b) - 1;
+          const float scale = __fdiv_rn(__fsub_rn(mx, mn), (float)qmax);
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            int q = 0;
+            if (scale > 0.f) {
+              const float tq = __fadd_rn(__fdiv_rn(__fsub_rn(x[e], mn), scale), 0.5f);
+              q = (int)floorf(tq);
+              q = q < 0 ? 0 : (q > qmax ? qmax : q);
+            }
+            codes_s[E * lane + e] = (uint8_t)q;
+          }
+          if ((lane % (64 / E)) == 0)
+            reinterpret_cast<__half2*>(hdr)[lane / (64 / E)] =
+                __halves2half2(__float2half_rn(scale), __float2half_rn(mn));
+          __syncwarp();
+          warp_pack_store<D>(codes_s, V.code_bits, reinterpret_cast<uint32_t*>(pay), lane);
+          __syncwarp();
+        }
+      }
+      cur = nxt;
+      raw = rawn;
+      gv = gn;
     }
   }
 }
@@ -446,11 +530,11 @@ cudaError_t launch_kind(const EncArgs& a, int sm_count, cudaStream_t s) {
   long long work;
   if (KIND == kTurboK) {
     using Sh = EncShape<D>;
-    smem += (size_t)Sh::NV * Sh::RS * 4 + (size_t)Sh::NV * D + Sh::NV * 8;
+    smem += (size_t)Sh::NV * Sh::RS * 4 + (size_t)Sh::NV * 32 * 4 + (size_t)Sh::NV * (D / 32) * 4 + Sh::NV * 8;
     work = (a.n_vectors + Sh::NV - 1) / Sh::NV;
   } else {
     smem += (size_t)kEncWarps * D;
-    work = (a.n_vectors + kEncWarps - 1) / kEncWarps;
+    work = (a.n_vectors + 8 * kEncWarps - 1) / (8 * kEncWarps);  // runs of 8 vectors per warp
   }
   auto kern = encode_kernel<D, KIND, B>;
   if (smem > 48 * 1024) {
