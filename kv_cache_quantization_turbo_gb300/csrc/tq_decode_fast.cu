@@ -46,10 +46,11 @@
 // Work: a work item is (layer x sequence, KV head, split of the context); each
 // warp takes items from an atomic counter (zeroed by the prologue kernel) and
 // writes one partial per query head and item, so warps never wait for each
-// other.  Memory: the K and V bytes a few tiles ahead are requested into L2
-// with bulk prefetches, so a tile's own register loads (K at its start, V after
-// the K contraction) meet L2 and registers hold one tile only; cache loads carry
-// an evict-first L2 policy so that the partials stay in L2 for the combine.
+// other.  Memory: the K and V bytes of the tiles 4 and 5 ahead are requested
+// into L2 with bulk prefetches every second tile, so a tile's own register loads
+// (K at its start, V after the K contraction) meet L2 and registers hold one
+// tile only; cache loads carry an evict-first L2 policy so that the partials
+// stay in L2 for the combine.
 // One persistent CTA of 16 warps per SM.
 #include <cuda_fp16.h>
 
@@ -275,16 +276,16 @@ struct FastWarp {
            ((reinterpret_cast<uintptr_t>(k.a.k.header) | reinterpret_cast<uintptr_t>(k.a.v.header)) & 15) == 0;
   }
 
-  // Requests the first tiles of a work item into L2 (lane 0, whose addresses are the tile's
-  // own; only tiles wholly inside the page).
-  __device__ __forceinline__ void prefetch_first() {
-    const int n = min(min(ntiles, kPrefetchTiles), (k.a.k.page_size - c.in_page) / 16);
+  // Requests tiles [tile + ahead, tile + ahead + n) into L2, n <= count, clipped to the work
+  // item and to the page (lane 0, whose addresses are the current tile's own).
+  __device__ __forceinline__ void prefetch_tiles(int tile, int ahead, int count) {
+    const int n = min(min(ntiles - tile - ahead, count), (k.a.k.page_size - c.in_page) / 16 - ahead);
     if (lane != 0 || n <= 0 || !c.ok) return;
-    prefetch_l2(c.kp, 16 * n * kKPay);
-    prefetch_l2(c.vp, 16 * n * kVPay);
+    prefetch_l2(c.kp + 16 * ahead * kKPay, 16 * n * kKPay);
+    prefetch_l2(c.vp + 16 * ahead * kVPay, 16 * n * kVPay);
     if (headers_aligned()) {
-      prefetch_l2(c.kh, 16 * n * kKHdr);
-      prefetch_l2(c.vh, 16 * n * kVHdr);
+      prefetch_l2(c.kh + 16 * ahead * kKHdr, 16 * n * kKHdr);
+      prefetch_l2(c.vh + 16 * ahead * kVHdr, 16 * n * kVHdr);
     }
   }
 
@@ -319,15 +320,6 @@ struct FastWarp {
   template <int BUF>
   __device__ __forceinline__ void step(int tile) {
     const int nvalid = tile == ntiles - 1 ? last_valid : 16;
-    if (lane == 0 && tile + kPrefetchTiles < ntiles &&
-        c.in_page + 16 * (kPrefetchTiles + 1) <= k.a.k.page_size) {
-      prefetch_l2(c.kp + 16 * kPrefetchTiles * kKPay, 16 * kKPay);
-      prefetch_l2(c.vp + 16 * kPrefetchTiles * kVPay, 16 * kVPay);
-      if (headers_aligned()) {
-        prefetch_l2(c.kh + 16 * kPrefetchTiles * kKHdr, 16 * kKHdr);
-        prefetch_l2(c.vh + 16 * kPrefetchTiles * kVHdr, 16 * kVHdr);
-      }
-    }
     if (!c.ok) {  // warp-uniform: the tile's page was out of range
       __syncwarp();
       return;
@@ -514,8 +506,9 @@ struct FastWarp {
       c.page_ord = t0 / a.k.page_size;
       c.in_page = t0 - c.page_ord * a.k.page_size;
       set_page();
-      prefetch_first();
+      prefetch_tiles(0, 0, kPrefetchTiles);
       for (int tile = 0; tile < ntiles; tile += 2) {
+        prefetch_tiles(tile, kPrefetchTiles, 2);  // the two tiles that follow the ones already requested
         step<0>(tile);
         if (tile + 1 >= ntiles) break;
         advance();
