@@ -191,7 +191,9 @@ tq_status tq_get_status(tq_context* ctx, uint32_t* flags);
  * not both).  Input element (l, t, h, i) of K is
  *     k[l * in_layer_stride + t * in_token_stride + h * d + i]
  * for l < n_layers, t < n_tokens, h < n_kv_heads of the view, i < d (same for V);
- * strides are in elements and heads are contiguous d-vectors.  Layer l of the
+ * strides are in elements and heads are contiguous d-vectors.  k and v must be
+ * 16-byte aligned and both strides multiples of 8 elements (the inputs are read
+ * with 16-byte loads), else TQ_ERR_INVALID_ARG.  Layer l of the
  * input goes to layer layer_begin + l of the view.  Token t goes to slot
  * slots[t] (device int64 [n_tokens]) when `slots` is non-NULL, else to slot
  * slot_begin + t; a slot outside [0, num_pages * page_size) is skipped and

@@ -376,6 +376,10 @@ tq_status tq_encode_kv(const tq_context* ctx, const tq_cache_view* k_view, const
   const int H = k_view ? kv.H : vv.H;
   if (in_token_stride < (int64_t)H * d || (n_layers > 1 && in_layer_stride < in_token_stride * n_tokens))
     return TQ_ERR_INVALID_ARG;
+  // the kernels read inputs with 16-byte vector loads
+  if ((reinterpret_cast<uintptr_t>(k) & 15) || (reinterpret_cast<uintptr_t>(v) & 15) || (in_token_stride & 7) ||
+      (n_layers > 1 && (in_layer_stride & 7)))
+    return TQ_ERR_INVALID_ARG;
   if (n_layers == 0 || n_tokens == 0) return TQ_OK;
   if ((int64_t)n_layers * n_tokens * H >= (int64_t(1) << 32)) return TQ_ERR_UNSUPPORTED;  // split the call
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

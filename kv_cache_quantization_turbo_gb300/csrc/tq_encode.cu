@@ -9,23 +9,23 @@
 // the pages' baselines.
 //
 // Work decomposition
-//   - one warp per vector for everything but the QJL projection; lane l holds
-//     the E = d/32 consecutive coordinates [E l, E l + E); the sign flips, the
-//     codebook boundaries and the WHT butterfly signs live in registers;
-//   - the Lloyd-Max index is a binary search over the sorted boundaries (the
-//     count of boundaries <= y, ties included as the definition has it);
-//   - codes are packed by warp shuffles: lane l forms the E w-bit codes of its
-//     coordinates as one chunk, and lane j gathers the chunks that overlap
-//     32-bit word j of the little-endian stream;
-//   - turbo K: a CTA encodes a batch of NV = 8192/d vectors: phase A (warps:
-//     stage 1, the residual r into shared memory), phase B (the whole CTA: the
-//     d x d projection S r on mma.sync m16n8k16, f16 inputs split into high and
-//     low parts, r_hi s_hi + r_lo s_hi + r_hi s_lo accumulated in fp32, which
-//     leaves an error near 1e-7 of |r|, far inside the 1e-6 sign band), phase C
-//     (warps: pack codes and store);
+//   - turbo formats: a vector is held by a group of L = d/32 lanes, each lane owning
+//     32 consecutive coordinates, so a warp encodes 32/L vectors at once.  The sign
+//     flips are applied on the fp16 words, five of the WHT stages run inside a lane
+//     and log2(L) across the group (shuffles), 1/(n sqrt(d)) is applied once;
+//   - the Lloyd-Max index is a binary search over the sorted boundaries (the count
+//     of boundaries <= y, ties included as the definition has it), and each lane
+//     packs its 32 codes into its own w words of the stream and stores them;
+//   - turbo K: a CTA encodes a batch of NV = 8192/d vectors: phase A (stage 1, the
+//     residual r into shared memory), phase B (the whole CTA: the d x d projection
+//     S r on mma.sync m16n8k16, f16 inputs split into high and low parts,
+//     r_hi s_hi + r_lo s_hi + r_hi s_lo accumulated in fp32, which leaves an error
+//     near 1e-7 of |r|, far inside the 1e-6 sign band; signs gathered by warp
+//     ballots), phase C (codes = index | sign << b, stored);
+//   - q8_0 and min-max: one warp per vector, lane l holds E = d/32 coordinates;
 //   - vector ids -> (layer, token, head) and slots -> (page, offset) use
 //     multiply-shift division by invariant divisors;
-//   - grids are persistent: min(work, resident CTAs) CTAs loop over batches.
+//   - grids are persistent: min(work, resident CTAs) CTAs loop over the work.
 #include <cuda_fp16.h>
 
 #include "tq_device.cuh"
@@ -163,59 +163,6 @@ __device__ __forceinline__ uint32_t spread4(uint32_t x) {
   return (x | (x << 1)) & 0x55u;
 }
 
-// Per-lane constants of stage 1: sign flips of the lane's coordinates and the
-// butterfly signs of the five shuffle stages (-1 on the upper lane of a pair).
-template <int D>
-struct Stage1Consts {
-  float sgn[D / 32];
-  float bfly[5];
-  __device__ __forceinline__ void init(const int8_t* signs, int lane) {
-    constexpr int E = D / 32;
-#pragma unroll
-    for (int e = 0; e < E; ++e) sgn[e] = (float)signs[E * lane + e];
-#pragma unroll
-    for (int s = 0; s < 5; ++s) bfly[s] = (lane >> s) & 1 ? -1.f : 1.f;
-  }
-};
-
-// Stage 1 for one vector held by a warp: returns n and leaves y = H diag(s) x / n in x
-// (orthonormal H: the butterflies run unscaled and 1/(n sqrt(d)) is applied once).
-template <int D>
-__device__ __forceinline__ float stage1_rotate(float (&x)[D / 32], const Stage1Consts<D>& c) {
-  constexpr int E = D / 32;
-  float ss = 0.f;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    ss = fmaf(x[e], x[e], ss);
-    x[e] *= c.sgn[e];
-  }
-#pragma unroll
-  for (int s = 1; s < E; s <<= 1) {
-#pragma unroll
-    for (int i = 0; i < E; ++i) {
-      if ((i & s) == 0) {
-        const float u = x[i], v = x[i + s];
-        x[i] = u + v;
-        x[i + s] = u - v;
-      }
-    }
-  }
-  ss = warp_sum(ss);
-#pragma unroll
-  for (int st = 0; st < 5; ++st) {
-#pragma unroll
-    for (int i = 0; i < E; ++i) {
-      const float o = __shfl_xor_sync(kFull, x[i], 1 << st);
-      x[i] = fmaf(x[i], c.bfly[st], o);  // lower lane: x + o, upper lane: o - x
-    }
-  }
-  const float n = sqrtf(ss);
-  const float f = n > 0.f ? __fdividef(inv_sqrt_dim<D>(), n) : 0.f;  // ~2 ulp: far inside the code band
-#pragma unroll
-  for (int e = 0; e < E; ++e) x[e] *= f;
-  return n;
-}
-
 // Lloyd-Max index of y: the number of sorted boundaries bnd[k] <= y (b bits, 2^b - 1 boundaries).
 template <int B>
 __device__ __forceinline__ uint32_t lloyd_index(float y, const float (&bnd)[7]) {
@@ -235,25 +182,6 @@ __device__ __forceinline__ uint32_t lloyd_index(float y, const float (&bnd)[7]) 
   }
 }
 
-// Stores the packed stream of one vector: lane l holds the E = D/32 codes of its
-// coordinates as chunk = sum_e code_e << (W e) (bits [C l, C l + C) of the stream,
-// C = E W); lane j < E W writes 32-bit word j.
-template <int D, int W>
-__device__ __forceinline__ void pack_store(uint32_t chunk, uint32_t* dst, int lane) {
-  constexpr int E = D / 32, C = E * W, NW = E * W;
-  constexpr int MAXL = (32 + C - 1) / C + 1;
-  const int lfirst = (32 * lane) / C;
-  uint32_t word = 0;
-#pragma unroll
-  for (int k = 0; k < MAXL; ++k) {
-    const int src = lfirst + k;
-    const uint32_t v = __shfl_sync(kFull, chunk, src & 31);
-    const int sh = C * src - 32 * lane;
-    if (src < 32 && sh < 32) word |= sh >= 0 ? (v << sh) : (v >> -sh);
-  }
-  if (lane < NW) dst[lane] = word;
-}
-
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
 __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -271,88 +199,321 @@ __device__ __forceinline__ void split_pair(float2 v, uint32_t& hi, uint32_t& lo)
   lo = h2u(__floats2half2_rn(v.x - hf.x, v.y - hf.y));
 }
 
-// B = stage-1 index bits (turbo K: the stored code adds the QJL sign as bit B).
-template <int D, int KIND, int B>
-__global__ void __launch_bounds__(kEncThreads, KIND == kTurboK ? 3 : 4) encode_kernel(EncArgs a) {
-  using Sh = EncShape<D>;
-  constexpr int E = Sh::E;
+// q8_0 and per-group min-max: one warp per vector (lane l holds E = d/32 coordinates).
+template <int D, int KIND>
+__global__ void __launch_bounds__(kEncThreads, 4) encode_kernel(EncArgs a) {
+  constexpr int E = D / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint8_t* codes_s = smem + warp * D;  // [warps][D] (min-max packing)
+  const DevView& V = a.view;
+  TokenCache tc;
+  // warps take runs of 8 consecutive vectors (whole tokens when H divides 8), the next
+  // vector's load in flight while the current one is encoded
+  constexpr int RUN = 8;
+  const long long nw = (long long)gridDim.x * kEncWarps;
+  long long run = (long long)blockIdx.x * kEncWarps + warp;
+  int i = 0;
+  long long gv = run * RUN;
+  Loc cur{nullptr, -1};
+  RawVec<D> raw;
+  raw.zero();
+  if (gv < a.n_vectors) {
+    cur = locate(a, (uint32_t)gv, tc, lane);
+    if (cur.vid >= 0) raw.load(cur.src, lane);
+  }
+  while (gv < a.n_vectors) {
+    long long gn;
+    if (i + 1 < RUN) {
+      gn = gv + 1;
+      ++i;
+    } else {
+      run += nw;
+      gn = run * RUN;
+      i = 0;
+    }
+    Loc nxt{nullptr, -1};
+    RawVec<D> rawn;
+    rawn.zero();
+    if (gn < a.n_vectors) {
+      nxt = locate(a, (uint32_t)gn, tc, lane);
+      if (nxt.vid >= 0) rawn.load(nxt.src, lane);
+    }
+    if (cur.vid >= 0) {  // warp-uniform
+      float x[E];
+      raw.to_float(x);
+      unsigned char* pay = V.payload + cur.vid * V.pay_bytes;
+      unsigned char* hdr = V.header + cur.vid * V.hdr_bytes;
+      if constexpr (KIND == kQ8) {
+        // block of 32 coordinates = 32/E consecutive lanes
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+        for (int m = 1; m < 32 / E; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, m));
+        const float delta = __fdiv_rn(amax, 127.0f);
+        uint32_t packed[E / 2 > 0 ? E / 2 : 1] = {};
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float qf = delta > 0.f ? roundf(__fdiv_rn(x[e], delta)) : 0.f;
+          const uint32_t qb = (uint32_t)(uint8_t)(int8_t)(int)qf;
+          packed[e / 4] |= qb << (8 * (e % 4));
+        }
+        if constexpr (E == 2) {
+          reinterpret_cast<uint16_t*>(pay)[lane] = (uint16_t)packed[0];
+        } else if constexpr (E == 4) {
+          reinterpret_cast<uint32_t*>(pay)[lane] = packed[0];
+        } else {
+          reinterpret_cast<uint2*>(pay)[lane] = make_uint2(packed[0], packed[1]);
+        }
+        if ((lane % (32 / E)) == 0)
+          reinterpret_cast<__half*>(hdr)[lane / (32 / E)] = __float2half_rn(delta);
+      } else {  // kMinMax: groups of 64 coordinates = 64/E consecutive lanes
+        float mn = x[0], mx = x[0];
+#pragma unroll
+        for (int e = 1; e < E; ++e) { mn = fminf(mn, x[e]); mx = fmaxf(mx, x[e]); }
+#pragma unroll
+        for (int m = 1; m < 64 / E; m <<= 1) {
+          mn = fminf(mn, __shfl_xor_sync(kFull, mn, m));
+          mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, m));
+        }
+        const int b = V.idx_bits;
+        const int qmax = (1 << b) - 1;
+        const float scale = __fdiv_rn(__fsub_rn(mx, mn), (float)qmax);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          int q = 0;
+          if (scale > 0.f) {
+            const float tq = __fadd_rn(__fdiv_rn(__fsub_rn(x[e], mn), scale), 0.5f);
+            q = (int)floorf(tq);
+            q = q < 0 ? 0 : (q > qmax ? qmax : q);
+          }
+          codes_s[E * lane + e] = (uint8_t)q;
+        }
+        if ((lane % (64 / E)) == 0)
+          reinterpret_cast<__half2*>(hdr)[lane / (64 / E)] =
+              __halves2half2(__float2half_rn(scale), __float2half_rn(mn));
+        __syncwarp();
+        warp_pack_store<D>(codes_s, V.code_bits, reinterpret_cast<uint32_t*>(pay), lane);
+        __syncwarp();
+      }
+    }
+    cur = nxt;
+    raw = rawn;
+    gv = gn;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Turbo formats: a vector is held by a group of L = d/32 lanes, each lane owning 32
+// consecutive coordinates, so a warp encodes 32/L vectors at once.  Five of the WHT
+// stages, the Lloyd-Max indices and the packing of the lane's own code words stay in
+// registers; only log2(L) butterfly stages and the norm need shuffles within the group.
+// ---------------------------------------------------------------------------
+template <int D>
+struct GroupShape {
+  static constexpr int L = D / 32;       // lanes per vector
+  static constexpr int VPW = 32 / L;     // vectors per warp
+  static constexpr int NV = 8192 / D;    // vectors per CTA batch (turbo K) = warps x VPW
+  static constexpr int RS = D + 8;       // row stride of the residual tile (floats)
+  static constexpr int KS = D / 16;      // k steps of the projection
+  static_assert(NV == kEncWarps * VPW, "one group pass per warp and batch");
+};
+
+// fp16 sign masks of the lane's 32 coordinates: word j flips coordinates 2j, 2j+1.
+__device__ __forceinline__ void lane_sign_masks(const int8_t* signs, int sub, uint32_t (&sg)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    sg[j] = (signs[32 * sub + 2 * j] < 0 ? 0x8000u : 0u) | (signs[32 * sub + 2 * j + 1] < 0 ? 0x80000000u : 0u);
+}
+
+// The lane's 32 fp16 coordinates (64 contiguous bytes), loaded ahead of their use.
+struct Raw32 {
+  uint4 q[4];
+  __device__ __forceinline__ void load(const __half* src) {
+    const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) q[k] = p[k];
+  }
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) q[k] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  // signs applied on the fp16 words (exact), then widened to fp32
+  __device__ __forceinline__ void to_float(float (&x)[32], const uint32_t (&sg)[16]) const {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t w[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t u = w[i] ^ sg[4 * k + i];
+        const __half2 h = *reinterpret_cast<const __half2*>(&u);
+        x[8 * k + 2 * i] = __low2float(h);
+        x[8 * k + 2 * i + 1] = __high2float(h);
+      }
+    }
+  }
+};
+
+// Stage 1 of one vector held by a group: x holds diag(s) x on entry (coordinates 32 sub + e);
+// returns n and leaves y = H diag(s) x / n.  The butterflies run unscaled and 1/(n sqrt(d)) is
+// applied once; bfly[s] = -1 on the upper lane of each pair of the cross-lane stage s.
+template <int D>
+__device__ __forceinline__ float group_stage1(float (&x)[32], const float (&bfly)[3]) {
+  constexpr int L = D / 32;
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) ss = fmaf(x[e], x[e], ss);  // |s_i x_i| = |x_i|
+#pragma unroll
+  for (int s = 1; s < 32; s <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if ((i & s) == 0) {
+        const float u = x[i], v = x[i + s];
+        x[i] = u + v;
+        x[i + s] = u - v;
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < L; m <<= 1) ss += __shfl_xor_sync(kFull, ss, m);
+#pragma unroll
+  for (int st = 0; (1 << st) < L; ++st) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float o = __shfl_xor_sync(kFull, x[i], 1 << st);
+      x[i] = fmaf(x[i], bfly[st], o);  // lower lane: x + o, upper lane: o - x
+    }
+  }
+  const float n = sqrtf(ss);
+  const float f = n > 0.f ? __fdividef(inv_sqrt_dim<D>(), n) : 0.f;  // ~2 ulp: far inside the code band
+#pragma unroll
+  for (int e = 0; e < 32; ++e) x[e] *= f;
+  return n;
+}
+
+// ORs the W-bit code c of the lane's coordinate e into its W words (bit W e of the lane's stream).
+template <int W>
+__device__ __forceinline__ void put_code(uint32_t (&w)[W], int e, uint32_t c) {
+  const int bit = W * e, k = bit >> 5, sh = bit & 31;
+  w[k] |= c << sh;
+  if (sh + W > 32) w[k + 1] |= c >> (32 - sh);
+}
+
+// Stores the lane's W words at word W sub of the vector's payload.
+template <int W>
+__device__ __forceinline__ void store_words(uint32_t* dst, const uint32_t (&w)[W]) {
+  if constexpr (W == 4) {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else if constexpr (W == 2) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < W; ++k) dst[k] = w[k];
+  }
+}
+
+// Location of the vector of global id gv (no caching: the lanes of a warp serve different vectors).
+__device__ __forceinline__ Loc locate_one(const EncArgs& a, uint32_t gv, int report) {
+  const uint32_t lt = fdiv(gv, a.div_h);
+  const uint32_t h = gv - lt * (uint32_t)a.view.H;
+  const uint32_t l = fdiv(lt, a.div_t);
+  const uint32_t t = lt - l * (uint32_t)a.n_tokens;
+  Loc r;
+  r.src = a.x + (long long)l * a.layer_stride + (long long)t * a.token_stride + (long long)h * a.view.d;
+  const long long slot = a.slots ? a.slots[t] : a.slot_begin + t;
+  const DevView& V = a.view;
+  const long long cap = V.num_pages * (long long)V.page_size;
+  if (slot < 0 || slot >= cap) {
+    if (report && h == 0) atomicOr(a.tab.status, kFlagSlot);
+    r.vid = -1;
+    return r;
+  }
+  long long page, p;
+  if (a.slot32) {
+    const uint32_t s32 = (uint32_t)slot, pg = fdiv(s32, a.div_p);
+    page = pg;
+    p = s32 - pg * (uint32_t)V.page_size;
+  } else {
+    page = slot / V.page_size;
+    p = slot - page * V.page_size;
+  }
+  r.vid = (((long long)(a.layer_begin + (int)l) * V.num_pages + page) * V.H + h) * V.page_size + p;
+  return r;
+}
+
+// B = stage-1 index bits; QJL: turbo K (code = index | sign << B, plus residual norm).
+template <int D, bool QJL, int B>
+__global__ void __launch_bounds__(kEncThreads, 2) encode_turbo_kernel(EncArgs a) {
+  using Sh = GroupShape<D>;
+  constexpr int L = Sh::L, VPW = Sh::VPW;
+  constexpr int W = QJL ? B + 1 : B;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane % L, vl = lane / L;
 
   extern __shared__ __align__(16) unsigned char smem[];
   float* cb_s = reinterpret_cast<float*>(smem);  // centroids [8]
   unsigned char* dyn = smem + 64;
+  if (threadIdx.x < 8) cb_s[threadIdx.x] = a.tab.centroids[(B - 1) * 8 + threadIdx.x];
 
-  const DevView& V = a.view;
-  Stage1Consts<D> c1;
-  float bnd[7];
-  if (KIND == kTurboK || KIND == kTurboV) {
-    c1.init(a.tab.signs, lane);
+  uint32_t sg[16];
+  lane_sign_masks(a.tab.signs, sub, sg);
+  float bfly[3];
 #pragma unroll
-    for (int k = 0; k < 7; ++k) bnd[k] = k < (1 << B) - 1 ? a.tab.boundaries[(B - 1) * 7 + k] : 0.f;
-    if (threadIdx.x < 8) cb_s[threadIdx.x] = a.tab.centroids[(B - 1) * 8 + threadIdx.x];
-  }
+  for (int s = 0; s < 3; ++s) bfly[s] = (sub >> s) & 1 ? -1.f : 1.f;
+  float bnd[7];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) bnd[k] = k < (1 << B) - 1 ? a.tab.boundaries[(B - 1) * 7 + k] : 0.f;
   __syncthreads();
-  TokenCache tc;
+  const DevView& V = a.view;
 
-  if constexpr (KIND == kTurboK) {
-    constexpr int NV = Sh::NV, RS = Sh::RS, KS = Sh::KS, W = B + 1;
-    constexpr int VPW = NV / kEncWarps;                                    // vectors per warp in phases A, C
-    float* r_s = reinterpret_cast<float*>(dyn);                            // [NV][RS] residual x kRScale
-    uint32_t* chunk_s = reinterpret_cast<uint32_t*>(dyn + NV * RS * 4);    // [NV][32] index chunks
-    uint32_t* sig_s = chunk_s + NV * 32;                                   // [NV][D/32] QJL sign bits
+  if constexpr (QJL) {
+    constexpr int NV = Sh::NV, RS = Sh::RS, KS = Sh::KS;
+    float* r_s = reinterpret_cast<float*>(dyn);                              // [NV][RS] residual x kRScale
+    uint32_t* code_s = reinterpret_cast<uint32_t*>(dyn + NV * RS * 4);      // [NV][L][W] index words
+    uint32_t* sig_s = code_s + NV * L * W;                                  // [NV][D/32] QJL sign bits
     long long* vid_s = reinterpret_cast<long long*>(sig_s + NV * (D / 32));  // [NV]
     const long long n_batches = (a.n_vectors + NV - 1) / NV;
     for (long long bt = blockIdx.x; bt < n_batches; bt += gridDim.x) {
-      const long long base = bt * NV + warp * VPW;
-      // ---- phase A: stage 1 and the residual, one warp per vector (next vector's load in flight) ----
-      Loc cur{nullptr, -1};
-      RawVec<D> raw;
-      raw.zero();
-      if (base < a.n_vectors) {
-        cur = locate(a, (uint32_t)base, tc, lane);
-        if (cur.vid >= 0) raw.load(cur.src, lane);
-      }
-#pragma unroll 1
-      for (int i = 0; i < VPW; ++i) {
-        const int v = warp * VPW + i;
-        Loc nxt{nullptr, -1};
-        RawVec<D> rawn;
-        rawn.zero();
-        if (i + 1 < VPW && base + i + 1 < a.n_vectors) {
-          nxt = locate(a, (uint32_t)(base + i + 1), tc, lane);
-          if (nxt.vid >= 0) rawn.load(nxt.src, lane);
+      const int v = warp * VPW + vl;  // this lane's vector in the batch
+      const long long gv = bt * NV + v;
+      // ---- phase A: stage 1 and the residual ----
+      {
+        Loc loc{nullptr, -1};
+        Raw32 raw;
+        raw.zero();
+        if (gv < a.n_vectors) {
+          loc = locate_one(a, (uint32_t)gv, sub == 0);
+          if (loc.vid >= 0) raw.load(loc.src + 32 * sub);
         }
-        float x[E];
-        raw.to_float(x);
-        const float n = stage1_rotate<D>(x, c1);
+        float x[32];
+        raw.to_float(x, sg);
+        const float n = group_stage1<D>(x, bfly);
         float rr = 0.f;
-        uint32_t chunk = 0;
+        uint32_t w[W] = {};
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
+        for (int e = 0; e < 32; ++e) {
           const uint32_t idx = lloyd_index<B>(x[e], bnd);
           const float r = x[e] - cb_s[idx];
           rr = fmaf(r, r, rr);
           x[e] = r * kRScale;
-          chunk |= idx << (W * e);
+          put_code<W>(w, e, idx);
         }
-        float* rp = r_s + v * RS + E * lane;
-        if constexpr (E == 2) {
-          *reinterpret_cast<float2*>(rp) = make_float2(x[0], x[1]);
-        } else {
-          *reinterpret_cast<float4*>(rp) = make_float4(x[0], x[1], x[2], x[3]);
-          if constexpr (E == 8) *reinterpret_cast<float4*>(rp + 4) = make_float4(x[4], x[5], x[6], x[7]);
+        float4* rp = reinterpret_cast<float4*>(r_s + v * RS + 32 * sub);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) rp[k] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+        uint32_t* cw = code_s + (v * L + sub) * W;
+#pragma unroll
+        for (int k = 0; k < W; ++k) cw[k] = w[k];
+#pragma unroll
+        for (int m = 1; m < L; m <<= 1) rr += __shfl_xor_sync(kFull, rr, m);
+        const float rnorm = n * sqrtf(rr);
+        if (sub == 0) {
+          vid_s[v] = loc.vid;
+          if (loc.vid >= 0)
+            *reinterpret_cast<__half2*>(V.header + loc.vid * V.hdr_bytes) =
+                __halves2half2(__float2half_rn(n), __float2half_rn(rnorm));
         }
-        chunk_s[v * 32 + lane] = chunk;
-        const float rnorm = n * sqrtf(warp_sum(rr));
-        if (lane == 0) {
-          vid_s[v] = cur.vid;
-          if (cur.vid >= 0) {
-            const __half2 hd = __halves2half2(__float2half_rn(n), __float2half_rn(rnorm));
-            *reinterpret_cast<__half2*>(V.header + cur.vid * V.hdr_bytes) = hd;
-          }
-        }
-        cur = nxt;
-        raw = rawn;
       }
       __syncthreads();
       // ---- phase B: sigma_j = [(S r)_j > 0] for the batch on tensor cores ----
@@ -403,140 +564,79 @@ __global__ void __launch_bounds__(kEncThreads, KIND == kTurboK ? 3 : 4) encode_k
         sig_s[(16 * mt + vv) * (D / 32) + 2 * pg + half] = word;
       }
       __syncthreads();
-      // ---- phase C: codes = index | sign << B, pack and store ----
-#pragma unroll 1
-      for (int i = 0; i < VPW; ++i) {
-        const int v = warp * VPW + i;
+      // ---- phase C: codes = index | sign << B, store ----
+      {
         const long long vid = vid_s[v];
-        if (vid < 0) continue;  // warp-uniform
-        const uint32_t sbits = (sig_s[v * (D / 32) + (E * lane) / 32] >> ((E * lane) % 32)) & ((1u << E) - 1u);
-        uint32_t chunk = chunk_s[v * 32 + lane];
+        if (vid >= 0) {
+          uint32_t w[W];
+          const uint32_t* cw = code_s + (v * L + sub) * W;
 #pragma unroll
-        for (int e = 0; e < E; ++e) chunk |= ((sbits >> e) & 1u) << (W * e + B);
-        pack_store<D, W>(chunk, reinterpret_cast<uint32_t*>(V.payload + vid * V.pay_bytes), lane);
+          for (int k = 0; k < W; ++k) w[k] = cw[k];
+          const uint32_t sbits = sig_s[v * (D / 32) + sub];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int bit = W * e + B;
+            w[bit >> 5] |= ((sbits >> e) & 1u) << (bit & 31);
+          }
+          store_words<W>(reinterpret_cast<uint32_t*>(V.payload + vid * V.pay_bytes) + W * sub, w);
+        }
       }
       __syncthreads();
     }
   } else {
-    // warps take runs of 8 consecutive vectors (whole tokens when H divides 8), the next
-    // vector's load in flight while the current one is encoded
-    uint8_t* codes_s = dyn + warp * D;  // [warps][D] (min-max packing)
-    constexpr int RUN = 8;
+    // V: warps take groups of VPW consecutive vectors; the next group's loads are in flight
+    // while the current one is encoded
     const long long nw = (long long)gridDim.x * kEncWarps;
-    long long run = (long long)blockIdx.x * kEncWarps + warp;
-    int i = 0;
-    long long gv = run * RUN;
+    long long grp = (long long)blockIdx.x * kEncWarps + warp;
+    long long gv = grp * VPW + vl;
     Loc cur{nullptr, -1};
-    RawVec<D> raw;
+    Raw32 raw;
     raw.zero();
     if (gv < a.n_vectors) {
-      cur = locate(a, (uint32_t)gv, tc, lane);
-      if (cur.vid >= 0) raw.load(cur.src, lane);
+      cur = locate_one(a, (uint32_t)gv, sub == 0);
+      if (cur.vid >= 0) raw.load(cur.src + 32 * sub);
     }
-    while (gv < a.n_vectors) {
-      // next vector of this warp
-      long long gn;
-      if (i + 1 < RUN) {
-        gn = gv + 1;
-        ++i;
-      } else {
-        run += nw;
-        gn = run * RUN;
-        i = 0;
-      }
+    while (grp * VPW < a.n_vectors) {  // warp-uniform
+      const long long gn = gv + nw * VPW;
       Loc nxt{nullptr, -1};
-      RawVec<D> rawn;
+      Raw32 rawn;
       rawn.zero();
       if (gn < a.n_vectors) {
-        nxt = locate(a, (uint32_t)gn, tc, lane);
-        if (nxt.vid >= 0) rawn.load(nxt.src, lane);
+        nxt = locate_one(a, (uint32_t)gn, sub == 0);
+        if (nxt.vid >= 0) rawn.load(nxt.src + 32 * sub);
       }
-      if (cur.vid >= 0) {  // warp-uniform
-        float x[E];
-        raw.to_float(x);
-        unsigned char* pay = V.payload + cur.vid * V.pay_bytes;
-        unsigned char* hdr = V.header + cur.vid * V.hdr_bytes;
-        if constexpr (KIND == kTurboV) {
-          const float n = stage1_rotate<D>(x, c1);
-          uint32_t chunk = 0;
+      float x[32];
+      raw.to_float(x, sg);
+      const float n = group_stage1<D>(x, bfly);
+      if (cur.vid >= 0) {
+        uint32_t w[W] = {};
 #pragma unroll
-          for (int e = 0; e < E; ++e) chunk |= lloyd_index<B>(x[e], bnd) << (B * e);
-          if (lane == 0) *reinterpret_cast<__half*>(hdr) = __float2half_rn(n);
-          pack_store<D, B>(chunk, reinterpret_cast<uint32_t*>(pay), lane);
-        } else if constexpr (KIND == kQ8) {
-          // block of 32 coordinates = 32/E consecutive lanes
-          float amax = 0.f;
-#pragma unroll
-          for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
-#pragma unroll
-          for (int m = 1; m < 32 / E; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, m));
-          const float delta = __fdiv_rn(amax, 127.0f);
-          uint32_t packed[E / 2 > 0 ? E / 2 : 1] = {};
-#pragma unroll
-          for (int e = 0; e < E; ++e) {
-            const float qf = delta > 0.f ? roundf(__fdiv_rn(x[e], delta)) : 0.f;
-            const uint32_t qb = (uint32_t)(uint8_t)(int8_t)(int)qf;
-            packed[e / 4] |= qb << (8 * (e % 4));
-          }
-          if constexpr (E == 2) {
-            reinterpret_cast<uint16_t*>(pay)[lane] = (uint16_t)packed[0];
-          } else if constexpr (E == 4) {
-            reinterpret_cast<uint32_t*>(pay)[lane] = packed[0];
-          } else {
-            reinterpret_cast<uint2*>(pay)[lane] = make_uint2(packed[0], packed[1]);
-          }
-          if ((lane % (32 / E)) == 0)
-            reinterpret_cast<__half*>(hdr)[lane / (32 / E)] = __float2half_rn(delta);
-        } else {  // kMinMax: groups of 64 coordinates = 64/E consecutive lanes
-          float mn = x[0], mx = x[0];
-#pragma unroll
-          for (int e = 1; e < E; ++e) { mn = fminf(mn, x[e]); mx = fmaxf(mx, x[e]); }
-#pragma unroll
-          for (int m = 1; m < 64 / E; m <<= 1) {
-            mn = fminf(mn, __shfl_xor_sync(kFull, mn, m));
-            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, m));
-          }
-          const int b = V.idx_bits;
-          const int qmax = (1 << b) - 1;
-          const float scale = __fdiv_rn(__fsub_rn(mx, mn), (float)qmax);
-#pragma unroll
-          for (int e = 0; e < E; ++e) {
-            int q = 0;
-            if (scale > 0.f) {
-              const float tq = __fadd_rn(__fdiv_rn(__fsub_rn(x[e], mn), scale), 0.5f);
-              q = (int)floorf(tq);
-              q = q < 0 ? 0 : (q > qmax ? qmax : q);
-            }
-            codes_s[E * lane + e] = (uint8_t)q;
-          }
-          if ((lane % (64 / E)) == 0)
-            reinterpret_cast<__half2*>(hdr)[lane / (64 / E)] =
-                __halves2half2(__float2half_rn(scale), __float2half_rn(mn));
-          __syncwarp();
-          warp_pack_store<D>(codes_s, V.code_bits, reinterpret_cast<uint32_t*>(pay), lane);
-          __syncwarp();
-        }
+        for (int e = 0; e < 32; ++e) put_code<W>(w, e, lloyd_index<B>(x[e], bnd));
+        store_words<W>(reinterpret_cast<uint32_t*>(V.payload + cur.vid * V.pay_bytes) + W * sub, w);
+        if (sub == 0) *reinterpret_cast<__half*>(V.header + cur.vid * V.hdr_bytes) = __float2half_rn(n);
       }
       cur = nxt;
       raw = rawn;
       gv = gn;
+      grp += nw;
     }
   }
 }
 
-template <int D, int KIND, int B>
-cudaError_t launch_kind(const EncArgs& a, int sm_count, cudaStream_t s) {
+template <int D, bool QJL, int B>
+cudaError_t launch_turbo(const EncArgs& a, int sm_count, cudaStream_t s) {
+  using Sh = GroupShape<D>;
+  constexpr int W = QJL ? B + 1 : B;
   size_t smem = 64;
   long long work;
-  if (KIND == kTurboK) {
-    using Sh = EncShape<D>;
-    smem += (size_t)Sh::NV * Sh::RS * 4 + (size_t)Sh::NV * 32 * 4 + (size_t)Sh::NV * (D / 32) * 4 + Sh::NV * 8;
+  if (QJL) {
+    smem += (size_t)Sh::NV * Sh::RS * 4 + (size_t)Sh::NV * Sh::L * W * 4 + (size_t)Sh::NV * (D / 32) * 4 +
+            (size_t)Sh::NV * 8;
     work = (a.n_vectors + Sh::NV - 1) / Sh::NV;
   } else {
-    smem += (size_t)kEncWarps * D;
-    work = (a.n_vectors + 8 * kEncWarps - 1) / (8 * kEncWarps);  // runs of 8 vectors per warp
+    work = (a.n_vectors + kEncWarps * Sh::VPW - 1) / (kEncWarps * Sh::VPW);
   }
-  auto kern = encode_kernel<D, KIND, B>;
+  auto kern = encode_turbo_kernel<D, QJL, B>;
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -550,23 +650,37 @@ cudaError_t launch_kind(const EncArgs& a, int sm_count, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int D, int KIND>
-cudaError_t launch_bits(const EncArgs& a, int sm_count, cudaStream_t s) {
+template <int D, bool QJL>
+cudaError_t launch_turbo_bits(const EncArgs& a, int sm_count, cudaStream_t s) {
   switch (a.view.idx_bits) {
-    case 1: return launch_kind<D, KIND, 1>(a, sm_count, s);
-    case 2: return launch_kind<D, KIND, 2>(a, sm_count, s);
-    case 3: return launch_kind<D, KIND, 3>(a, sm_count, s);
+    case 1: return launch_turbo<D, QJL, 1>(a, sm_count, s);
+    case 2: return launch_turbo<D, QJL, 2>(a, sm_count, s);
+    case 3: return launch_turbo<D, QJL, 3>(a, sm_count, s);
   }
   return cudaErrorInvalidValue;
+}
+
+template <int D, int KIND>
+cudaError_t launch_kind(const EncArgs& a, int sm_count, cudaStream_t s) {
+  const size_t smem = (size_t)kEncWarps * D;
+  const long long work = (a.n_vectors + 8 * kEncWarps - 1) / (8 * kEncWarps);  // runs of 8 vectors per warp
+  auto kern = encode_kernel<D, KIND>;
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kEncThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const long long grid = work < (long long)per_sm * sm_count ? work : (long long)per_sm * sm_count;
+  kern<<<(unsigned)grid, kEncThreads, smem, s>>>(a);
+  return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_dim(const EncArgs& a, int sm_count, cudaStream_t s) {
   const int f = a.view.format;
-  if (f == TQ_FMT_Q8_0) return launch_kind<D, kQ8, 1>(a, sm_count, s);
-  if (f == TQ_FMT_MINMAX) return launch_kind<D, kMinMax, 1>(a, sm_count, s);
-  if (a.view.has_qjl) return launch_bits<D, kTurboK>(a, sm_count, s);
-  return launch_bits<D, kTurboV>(a, sm_count, s);
+  if (f == TQ_FMT_Q8_0) return launch_kind<D, kQ8>(a, sm_count, s);
+  if (f == TQ_FMT_MINMAX) return launch_kind<D, kMinMax>(a, sm_count, s);
+  if (a.view.has_qjl) return launch_turbo_bits<D, true>(a, sm_count, s);
+  return launch_turbo_bits<D, false>(a, sm_count, s);
 }
 
 }  // namespace

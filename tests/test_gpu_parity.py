@@ -353,6 +353,21 @@ def test_decode_flags_bad_block_table_and_long_sequence(ctx128):
     assert flags & 1
 
 
+def test_encode_rejects_misaligned_inputs(ctx128):
+    d, H, T = 128, 2, 16
+    view = tq.alloc_view("turbo4_mse", d, H, page_size=T, num_pages=1)
+    x = torch.zeros((T + 1, H, d), dtype=torch.float16, device="cuda")
+    ok = tq.tq_encode_kv(ctx128.h, None, None, view, x, 0, 1, T, T * H * d, H * d)
+    assert ok == tq.TQ_OK
+    # input pointer not 16-byte aligned
+    assert tq.tq_encode_kv(ctx128.h, None, None, view, x.data_ptr() + 2, 0, 1, T, T * H * d, H * d) == \
+        tq.TQ_ERR_INVALID_ARG
+    # token stride not a multiple of 8 elements
+    assert tq.tq_encode_kv(ctx128.h, None, None, view, x, 0, 1, T - 1, (T - 1) * (H * d + 1), H * d + 1) == \
+        tq.TQ_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+
+
 def test_decode_rejects_bad_arguments(ctx128):
     d = 128
     kview = tq.alloc_view("turbo4", d, 2, page_size=64, num_pages=1)
