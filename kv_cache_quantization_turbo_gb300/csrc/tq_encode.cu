@@ -320,6 +320,21 @@ struct GroupShape {
   static_assert(NV == kEncWarps * VPW, "one group pass per warp and batch");
 };
 
+// Residual tile swizzle: the 16-byte chunk k (coordinates 32 sub + 4k .. + 3) of a row is
+// stored at chunk k ^ f(sub), so that the 8 lanes of a 128-bit store (consecutive lanes
+// covering 2 rows of 4 groups at d = 128) fall on 8 distinct 4-bank groups; the projection's
+// 64-bit loads use the same map and stay conflict-free.
+template <int L>
+__device__ __forceinline__ int chunk_swz(int sub) {
+  return L == 4 ? ((sub & 1) | ((sub & 2) << 1)) : sub;
+}
+// Swizzled position (in floats) of coordinate c in a residual row.
+template <int L>
+__device__ __forceinline__ int r_pos(int c) {
+  const int sub = c >> 5;
+  return (c & ~31) | ((((c >> 2) & 7) ^ chunk_swz<L>(sub)) << 2) | (c & 3);
+}
+
 // fp16 sign masks of the lane's 32 coordinates: word j flips coordinates 2j, 2j+1.
 __device__ __forceinline__ void lane_sign_masks(const int8_t* signs, int sub, uint32_t (&sg)[16]) {
 #pragma unroll
@@ -500,8 +515,9 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_turbo_kernel(EncArgs a)
           put_code<W>(w, e, idx);
         }
         float4* rp = reinterpret_cast<float4*>(r_s + v * RS + 32 * sub);
+        const int swz = chunk_swz<L>(sub);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) rp[k] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+        for (int k = 0; k < 8; ++k) rp[k ^ swz] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
         uint32_t* cw = code_s + (v * L + sub) * W;
 #pragma unroll
         for (int k = 0; k < W; ++k) cw[k] = w[k];
@@ -525,15 +541,16 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_turbo_kernel(EncArgs a)
         float acc[8][4];
 #pragma unroll
         for (int nb = 0; nb < 8; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
-        const float* ra = r_s + (16 * mt + g) * RS + 2 * t;
+        const float* ra = r_s + (16 * mt + g) * RS;
         const uint4* sf = a.tab.S_frag + (size_t)(8 * pg) * KS * 32 + lane;
 #pragma unroll 1
         for (int ks = 0; ks < KS; ++ks) {
           uint32_t ahi[4], alo[4];
-          split_pair(*reinterpret_cast<const float2*>(ra + 16 * ks), ahi[0], alo[0]);
-          split_pair(*reinterpret_cast<const float2*>(ra + 8 * RS + 16 * ks), ahi[1], alo[1]);
-          split_pair(*reinterpret_cast<const float2*>(ra + 16 * ks + 8), ahi[2], alo[2]);
-          split_pair(*reinterpret_cast<const float2*>(ra + 8 * RS + 16 * ks + 8), ahi[3], alo[3]);
+          const int c0 = r_pos<L>(16 * ks + 2 * t), c1 = r_pos<L>(16 * ks + 2 * t + 8);
+          split_pair(*reinterpret_cast<const float2*>(ra + c0), ahi[0], alo[0]);
+          split_pair(*reinterpret_cast<const float2*>(ra + 8 * RS + c0), ahi[1], alo[1]);
+          split_pair(*reinterpret_cast<const float2*>(ra + c1), ahi[2], alo[2]);
+          split_pair(*reinterpret_cast<const float2*>(ra + 8 * RS + c1), ahi[3], alo[3]);
 #pragma unroll
           for (int nb = 0; nb < 8; ++nb) {
             const uint4 b = __ldg(sf + ((size_t)nb * KS + ks) * 32);
@@ -573,10 +590,22 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_turbo_kernel(EncArgs a)
 #pragma unroll
           for (int k = 0; k < W; ++k) w[k] = cw[k];
           const uint32_t sbits = sig_s[v * (D / 32) + sub];
+          if constexpr (W == 4) {
+            // bits 8k..8k+7 of sbits -> bit 3 of each nibble of word k
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int bit = W * e + B;
-            w[bit >> 5] |= ((sbits >> e) & 1u) << (bit & 31);
+            for (int k = 0; k < 4; ++k) {
+              uint32_t b = (sbits >> (8 * k)) & 0xFFu;
+              b = (b | (b << 12)) & 0x000F000Fu;
+              b = (b | (b << 6)) & 0x03030303u;
+              b = (b | (b << 3)) & 0x11111111u;
+              w[k] |= b << 3;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int bit = W * e + B;
+              w[bit >> 5] |= ((sbits >> e) & 1u) << (bit & 31);
+            }
           }
           store_words<W>(reinterpret_cast<uint32_t*>(V.payload + vid * V.pay_bytes) + W * sub, w);
         }
