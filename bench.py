@@ -84,20 +84,24 @@ def measured_peaks():
         return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
-def source_hash(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_hash(paths):
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_src):
+def profiled_traffic(kernel_srcs):
     """Per-launch DRAM bytes of the decode call from the committed ncu summary, or None
-    when the kernel source changed since the counters were taken."""
+    when the kernel sources (attention kernel and its launch plan) changed since the
+    counters were taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "decode_traffic.json")) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if rec.get("source_sha256_16") != source_hash(kernel_src):
+    if rec.get("source_sha256_16") != source_hash(kernel_srcs):
         return None
     return rec.get("traffic_bytes_per_launch")
 
@@ -398,8 +402,8 @@ def main():
                      "frac": round(achieved / hbm, 4), "peak_source": f"{peak_src} hbm_gbs",
                      "kernel": "decode attention call (prologue + split-K attention + combine), one launch set "
                                f"over all {wl.n_layers} layers",
-                     "traffic": profiled_traffic(os.path.join(ROOT, "kv_cache_quantization_turbo_gb300", "csrc",
-                                                              "tq_decode_fast.cu"))},
+                     "traffic": profiled_traffic([os.path.join(ROOT, "kv_cache_quantization_turbo_gb300", "csrc", f)
+                                                  for f in ("tq_decode_fast.cu", "tq_decode.cu")])},
         "e2e": {"value": round(weak_scaling_value(dbytes, world, t_e2e), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 3),
                 "what": "per step: H2D of the 4096-token K/V chunk (all layers) and q, encode, decode, D2H of out;"

@@ -28,10 +28,12 @@ static int next_pow2(long long v) {
 
 DecodePlan plan_decode(int sm_count, int d, int n_layers, int batch, int n_q_heads, int max_ctx) {
   DecodePlan p{};
-  // Split size: aim at ~6 work items per warp of the fast kernel (16 warps per SM,
-  // query heads shared by about 4 per KV head), between 256 and 4096 tokens.
+  // Split size: aim at ~12 work items per warp of the fast kernel (16 warps per SM,
+  // query heads shared by about 4 per KV head), between 256 and 4096 tokens.  Timed on
+  // the 32-layer x 32K bench workload: 512-token splits beat 1024 (item count vs. load
+  // balance) and 256 (per-item overhead and partial traffic).
   const long long work = (long long)max_ctx * n_layers * batch * n_q_heads;
-  const long long per_item = (work + 4LL * 16 * 6 * sm_count - 1) / (4LL * 16 * 6 * sm_count);
+  const long long per_item = (work + 4LL * 16 * 12 * sm_count - 1) / (4LL * 16 * 12 * sm_count);
   int st = next_pow2(per_item);
   st = st < 256 ? 256 : (st > 4096 ? 4096 : st);
   p.split_tokens = st;
