@@ -210,6 +210,13 @@ def decode_bytes(tq, wl):
     return wl.n_layers * wl.n_kv_heads * wl.ctx * per_token_head
 
 
+def encode_bytes(tq, wl):
+    """Algorithmic bytes of one encode call: the fp16 K and V chunk read, the codes and headers written."""
+    vectors = wl.n_layers * wl.encode_chunk * wl.n_kv_heads
+    written = tq.tq_vector_bytes(wl.k_format, wl.head_dim) + tq.tq_vector_bytes(wl.v_format, wl.head_dim)
+    return vectors * (2 * 2 * wl.head_dim + written)
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle leg
 # ---------------------------------------------------------------------------
@@ -404,6 +411,11 @@ def main():
                                f"over all {wl.n_layers} layers",
                      "traffic": profiled_traffic([os.path.join(ROOT, "kv_cache_quantization_turbo_gb300", "csrc", f)
                                                   for f in ("tq_decode_fast.cu", "tq_decode.cu")])},
+        "roofline_encode": {"bound": "hbm", "achieved": round(encode_bytes(tq, wl) / t_enc / 1e9, 2), "peak": hbm,
+                            "unit": "GB/s", "frac": round(encode_bytes(tq, wl) / t_enc / 1e9 / hbm, 4),
+                            "peak_source": f"{peak_src} hbm_gbs", "traffic": None,
+                            "kernel": f"encode call (K and V kernels) of the {wl.encode_chunk}-token chunk over all "
+                                      f"{wl.n_layers} layers: fp16 input read, codes and headers written"},
         "e2e": {"value": round(weak_scaling_value(dbytes, world, t_e2e), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 3),
                 "what": "per step: H2D of the 4096-token K/V chunk (all layers) and q, encode, decode, D2H of out;"
