@@ -53,14 +53,18 @@ using DecodeKernelArgs = DecodeLaunch;
 // ---------------------------------------------------------------------------
 // 1. query prologue
 // ---------------------------------------------------------------------------
+constexpr int kRowsPerBlock = 1;  // query rows (one warp each) per CTA of the prologue and the combine (1 timed fastest)
+
 template <int D>
-__global__ void __launch_bounds__(32) qprep_kernel(DecodeKernelArgs ka) {
+__global__ void __launch_bounds__(32 * kRowsPerBlock) qprep_kernel(DecodeKernelArgs ka) {
   constexpr int E = D / 32;
   const DecodeArgs& a = ka.a;
-  const int lane = threadIdx.x;
-  const long long row = blockIdx.x;  // (layer, batch, q head)
+  const int lane = threadIdx.x & 31, wq = threadIdx.x >> 5;
+  const long long row = (long long)blockIdx.x * kRowsPerBlock + wq;  // (layer, batch, q head)
+  const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
   if (row == 0 && lane == 0) *ka.counter = 0u;  // work counter of the attention kernel that follows
-  __shared__ float q_s[D];
+  if (row >= rows) return;  // warp-uniform
+  __shared__ float q_s[kRowsPerBlock][D];
   float x[E];
   if (a.q_is_fp16) {
     const __half* q = static_cast<const __half*>(a.q) + row * D;
@@ -83,15 +87,16 @@ __global__ void __launch_bounds__(32) qprep_kernel(DecodeKernelArgs ka) {
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     x[e] *= a.softmax_scale;
-    q_s[E * lane + e] = x[e];
+    q_s[wq][E * lane + e] = x[e];
     dst[E * lane + e] = x[e];
   }
   __syncwarp();
   float sq[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) sq[e] = 0.f;
+#pragma unroll 8
   for (int i = 0; i < D; ++i) {
-    const float qi = q_s[i];
+    const float qi = q_s[wq][i];
 #pragma unroll
     for (int e = 0; e < E; ++e) sq[e] = fmaf(__ldg(ka.tab.S_T + i * D + E * lane + e), qi, sq[e]);
   }
@@ -292,27 +297,44 @@ __global__ void __launch_bounds__(32) attend_generic_kernel(DecodeKernelArgs ka)
 // 3. combine
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(32) combine_kernel(DecodeKernelArgs ka) {
+__global__ void __launch_bounds__(32 * kRowsPerBlock) combine_kernel(DecodeKernelArgs ka) {
   constexpr int E = D / 32;
   const DecodeArgs& a = ka.a;
-  const int lane = threadIdx.x;
-  const long long row = blockIdx.x;
-  const float* part = ka.partial + row * ka.n_splits * (D + 4);
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+  const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
+  if (row >= rows) return;  // warp-uniform
+  const int ns = ka.n_splits;
+  const float* part = ka.partial + row * ns * (D + 4);
+  // split maxima, lane-parallel
   float M = -INFINITY;
-  for (int s = 0; s < ka.n_splits; ++s) M = fmaxf(M, part[s * (D + 4)]);
+  for (int s = lane; s < ns; s += 32) M = fmaxf(M, part[s * (D + 4)]);
+  M = warp_max(M);
   float x[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) x[e] = 0.f;
   float L = 0.f;
   if (M != -INFINITY) {
-    for (int s = 0; s < ka.n_splits; ++s) {
-      const float ms = part[s * (D + 4)];
-      if (ms == -INFINITY) continue;
-      const float w = expf(ms - M);
-      L = fmaf(part[s * (D + 4) + 1], w, L);
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+      // weight of split s0 + lane (empty splits: m = -inf, weight 0)
+      float w = 0.f;
+      if (s0 + lane < ns) {
+        const float ms = part[(s0 + lane) * (D + 4)];
+        if (ms != -INFINITY) {
+          w = expf(ms - M);
+          L = fmaf(part[(s0 + lane) * (D + 4) + 1], w, L);
+        }
+      }
+      const int n = ns - s0 < 32 ? ns - s0 : 32;
+#pragma unroll 4
+      for (int j = 0; j < n; ++j) {
+        const float wj = __shfl_sync(kFull, w, j);
+        const float* p = part + (s0 + j) * (D + 4) + 4 + E * lane;
 #pragma unroll
-      for (int e = 0; e < E; ++e) x[e] = fmaf(part[s * (D + 4) + 4 + E * lane + e], w, x[e]);
+        for (int e = 0; e < E; ++e) x[e] = fmaf(p[e], wj, x[e]);
+      }
     }
+    L = warp_sum(L);
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
@@ -330,12 +352,13 @@ __global__ void __launch_bounds__(32) combine_kernel(DecodeKernelArgs ka) {
 template <int D>
 cudaError_t launch_decode_dim(const DecodeKernelArgs& ka, int sm_count, cudaStream_t s) {
   const DecodeArgs& a = ka.a;
-  const unsigned rows = (unsigned)((long long)a.n_layers * a.batch * a.n_q_heads);
-  qprep_kernel<D><<<rows, 32, 0, s>>>(ka);
+  const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
+  const unsigned blocks = (unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock);
+  qprep_kernel<D><<<blocks, 32 * kRowsPerBlock, 0, s>>>(ka);
   if (attend_fast_supported(ka)) {
     const cudaError_t e = launch_attend_fast(ka, sm_count, s);
     if (e != cudaSuccess) return e;
-    combine_kernel<D><<<rows, 32, 0, s>>>(ka);
+    combine_kernel<D><<<blocks, 32 * kRowsPerBlock, 0, s>>>(ka);
     return cudaGetLastError();
   }
   dim3 grid(ka.n_splits, a.k.H, a.n_layers * a.batch);
@@ -346,7 +369,7 @@ cudaError_t launch_decode_dim(const DecodeKernelArgs& ka, int sm_count, cudaStre
     if (e != cudaSuccess) return e;
   }
   attend_generic_kernel<D><<<grid, 32, smem, s>>>(ka);
-  combine_kernel<D><<<rows, 32, 0, s>>>(ka);
+  combine_kernel<D><<<blocks, 32 * kRowsPerBlock, 0, s>>>(ka);
   return cudaGetLastError();
 }
 
