@@ -107,7 +107,7 @@ def profiled_traffic(kernel_srcs):
 
 
 class ClockSampler:
-    """nvidia-smi clocks sampled every 200 ms while the timed region runs."""
+    """nvidia-smi clocks sampled every 200 ms around the timed region (see the call site)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -154,7 +154,8 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows),
+                "window": "1 s of untimed steps of the same workload, then the timed region"}
 
 
 # ---------------------------------------------------------------------------
@@ -331,6 +332,13 @@ def main():
     barrier()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     with ClockSampler(local_rank) as clocks:
+        # untimed steps for ~1 s, so that the clock record (200 ms samples) spans a steady load
+        # that ends where the timed region starts
+        t_soak = time.perf_counter()
+        while time.perf_counter() - t_soak < 1.0:
+            encode_step(tq, w, w["k_chunk"], w["v_chunk"], stream)
+            decode_step(tq, w, w["q"], w["out"], stream)
+            torch.cuda.synchronize(dev)
         barrier()
         t_wall = time.perf_counter()
         for s in range(args.steps):
