@@ -179,8 +179,9 @@ tq_status tq_context_get_tables(const tq_context* ctx, int8_t* signs, float* qjl
  * Reads and clears the context's device status word (synchronises the device).
  * *flags (host, may be NULL) receives the bits: 1 = a sequence length above
  * max_ctx or the view's capacity was clamped, 2 = a block-table entry out of
- * [0, num_pages) was skipped, 4 = a slot id out of range was skipped.
- * Returns TQ_ERR_INVALID_ARG if any bit was set, else TQ_OK.
+ * [0, num_pages) was skipped, 4 = a slot id out of range was skipped, 8 = a
+ * bounded wait for the tensor cores ran out (the results of that call are not
+ * valid).  Returns TQ_ERR_INVALID_ARG if any bit was set, else TQ_OK.
  */
 tq_status tq_get_status(tq_context* ctx, uint32_t* flags);
 

@@ -29,6 +29,7 @@
 #include <cuda_fp16.h>
 
 #include "tq_device.cuh"
+#include "tq_tc.cuh"
 
 namespace tq {
 namespace {
@@ -652,6 +653,215 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_turbo_kernel(EncArgs a)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Turbo K at d = 128 on the fifth-generation tensor cores.  A persistent CTA of 16 warps
+// encodes batches of 128 vectors: phase A (groups of 4 lanes per vector: stage 1, index
+// chunks, residual r 2^14 split into fp16 high and low parts, written into shared memory in
+// the core-matrix layout of an MMA operand); phase B (one thread issues
+// D[128 vectors x 128 projections] = r_lo S_hi^T + r_hi S_lo^T + r_hi S_hi^T as 24
+// tcgen05.mma of M 128, N 128, K 16 into tensor memory, S's split resident in shared memory
+// for the CTA's lifetime; every warp then reads 32 projections of one vector per lane and
+// packs their signs); phase C (codes = index | sign << b, stored).
+// ---------------------------------------------------------------------------
+namespace ktc {
+constexpr int D = 128, NV = 128, L = 4, VPW = 8, WARPS = 16, THREADS = 32 * WARPS;
+constexpr int kOp = D * 128 * 2;  // bytes of one 128 x 128 f16 operand
+// byte offset of element (row, k) in a 128 x 128 K-major operand: core matrix (row / 8, k / 8)
+// at (row / 8 * 16 + k / 8) * 128, row % 8 at 16 (row % 8); lbo (along K) = 128, sbo (rows) = 2048
+__host__ __device__ constexpr int core_off(int row, int k) {
+  return ((row >> 3) * (D / 8) + (k >> 3)) * 128 + (row & 7) * 16 + (k & 7) * 2;
+}
+constexpr uint32_t kLbo = 128, kSbo = 128 * (D / 8);
+}  // namespace ktc
+
+template <int B>
+__global__ void __launch_bounds__(ktc::THREADS, 1) encode_k_tc_kernel(EncArgs a) {
+  using namespace ktc;
+  constexpr int W = B + 1;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane % L, vl = lane / L;
+
+  extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char* s_hi = smem;
+  unsigned char* s_lo = smem + kOp;
+  unsigned char* r_hi = smem + 2 * kOp;
+  unsigned char* r_lo = smem + 3 * kOp;
+  uint32_t* code_s = reinterpret_cast<uint32_t*>(smem + 4 * kOp);  // [NV][L][W] index words
+  uint32_t* sig_s = code_s + NV * L * W;                             // [NV][4] QJL sign words
+  long long* vid_s = reinterpret_cast<long long*>(sig_s + NV * 4);   // [NV]
+  float* cb_s = reinterpret_cast<float*>(vid_s + NV);                 // [8]
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(cb_s + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mbar + 1);
+
+  if (warp == 0) tc::tmem_alloc(tmem_slot, 128);
+  if (threadIdx.x == 0) tc::mbar_init(mbar, 1);
+  if (threadIdx.x < 8) cb_s[threadIdx.x] = a.tab.centroids[(B - 1) * 8 + threadIdx.x];
+  // S (row j = projection j) split into fp16 high and low parts, operand layout
+  for (int i = threadIdx.x; i < D * D; i += THREADS) {
+    const int j = i / D, c = i % D;
+    const float v = a.tab.S[i];
+    const __half h = __float2half_rn(v);
+    *reinterpret_cast<__half*>(s_hi + core_off(j, c)) = h;
+    *reinterpret_cast<__half*>(s_lo + core_off(j, c)) = __float2half_rn(v - __half2float(h));
+  }
+  uint32_t sg[16];
+  lane_sign_masks(a.tab.signs, sub, sg);
+  float bfly[3];
+#pragma unroll
+  for (int s = 0; s < 3; ++s) bfly[s] = (sub >> s) & 1 ? -1.f : 1.f;
+  float bnd[7];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) bnd[k] = k < (1 << B) - 1 ? a.tab.boundaries[(B - 1) * 7 + k] : 0.f;
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const DevView& V = a.view;
+  constexpr uint32_t idesc = tc::idesc_f16_f32(128, 128);
+  uint32_t parity = 0;
+  bool timed_out = false;
+
+  const long long n_batches = (a.n_vectors + NV - 1) / NV;
+  for (long long bt = blockIdx.x; bt < n_batches; bt += gridDim.x) {
+    const int v = warp * VPW + vl;  // this lane's vector in the batch
+    const long long gv = bt * NV + v;
+    // ---- phase A ----
+    {
+      Loc loc{nullptr, -1};
+      Raw32 raw;
+      raw.zero();
+      if (gv < a.n_vectors) {
+        loc = locate_one(a, (uint32_t)gv, sub == 0);
+        if (loc.vid >= 0) raw.load(loc.src + 32 * sub);
+      }
+      float x[32];
+      raw.to_float(x, sg);
+      const float n = group_stage1<D>(x, bfly);
+      float rr = 0.f;
+      uint32_t w[W] = {};
+      uint32_t hi[16], lo[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const uint32_t i0 = lloyd_index<B>(x[e], bnd), i1 = lloyd_index<B>(x[e + 1], bnd);
+        const float r0 = x[e] - cb_s[i0], r1 = x[e + 1] - cb_s[i1];
+        rr = fmaf(r0, r0, rr);
+        rr = fmaf(r1, r1, rr);
+        put_code<W>(w, e, i0);
+        put_code<W>(w, e + 1, i1);
+        split_pair(make_float2(r0 * kRScale, r1 * kRScale), hi[e / 2], lo[e / 2]);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int off = core_off(v, 32 * sub + 8 * j);
+        *reinterpret_cast<uint4*>(r_hi + off) = make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
+        *reinterpret_cast<uint4*>(r_lo + off) = make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
+      }
+      uint32_t* cw = code_s + (v * L + sub) * W;
+#pragma unroll
+      for (int k = 0; k < W; ++k) cw[k] = w[k];
+#pragma unroll
+      for (int m = 1; m < L; m <<= 1) rr += __shfl_xor_sync(kFull, rr, m);
+      const float rnorm = n * sqrtf(rr);
+      if (sub == 0) {
+        vid_s[v] = loc.vid;
+        if (loc.vid >= 0)
+          *reinterpret_cast<__half2*>(V.header + loc.vid * V.hdr_bytes) =
+              __halves2half2(__float2half_rn(n), __float2half_rn(rnorm));
+      }
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    // ---- phase B: the projection on the tensor cores, signs from tensor memory ----
+    if (threadIdx.x == 0) {
+      const uint32_t ah = tc::smem_addr(r_hi), al = tc::smem_addr(r_lo);
+      const uint32_t bh = tc::smem_addr(s_hi), bl = tc::smem_addr(s_lo);
+#pragma unroll 1
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t koff = ks * 2 * 128;  // two core matrices along K per step
+        tc::mma_f16(tmem, tc::desc_kmajor(al + koff, kLbo, kSbo), tc::desc_kmajor(bh + koff, kLbo, kSbo), idesc,
+                    ks > 0);
+        tc::mma_f16(tmem, tc::desc_kmajor(ah + koff, kLbo, kSbo), tc::desc_kmajor(bl + koff, kLbo, kSbo), idesc,
+                    true);
+        tc::mma_f16(tmem, tc::desc_kmajor(ah + koff, kLbo, kSbo), tc::desc_kmajor(bh + koff, kLbo, kSbo), idesc,
+                    true);
+      }
+      tc::commit(mbar);
+    }
+    const bool ok = tc::mbar_wait(mbar, parity);
+    if (__syncthreads_or(!ok)) {  // the wait ran out: flag it and leave
+      if (threadIdx.x == 0) atomicOr(a.tab.status, kFlagTimeout);
+      timed_out = true;
+      break;
+    }
+    parity ^= 1u;
+    tc::fence_after_sync();
+    {
+      // warp: tensor-memory lanes 32 (warp % 4) .. + 31 (vectors), columns 32 (warp / 4) .. + 31
+      const int q = warp & 3, cbk = warp >> 2;
+      uint32_t pv[32];
+      tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * cbk, pv);
+      uint32_t word = 0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) word |= (__uint_as_float(pv[j]) > 0.f ? 1u : 0u) << j;
+      sig_s[(32 * q + lane) * 4 + cbk] = word;
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    // ---- phase C: codes = index | sign << B, store ----
+    {
+      const long long vid = vid_s[v];
+      if (vid >= 0) {
+        uint32_t w[W];
+        const uint32_t* cw = code_s + (v * L + sub) * W;
+#pragma unroll
+        for (int k = 0; k < W; ++k) w[k] = cw[k];
+        const uint32_t sbits = sig_s[v * 4 + sub];
+        if constexpr (W == 4) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint32_t b = (sbits >> (8 * k)) & 0xFFu;
+            b = (b | (b << 12)) & 0x000F000Fu;
+            b = (b | (b << 6)) & 0x03030303u;
+            b = (b | (b << 3)) & 0x11111111u;
+            w[k] |= b << 3;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int bit = W * e + B;
+            w[bit >> 5] |= ((sbits >> e) & 1u) << (bit & 31);
+          }
+        }
+        store_words<W>(reinterpret_cast<uint32_t*>(V.payload + vid * V.pay_bytes) + W * sub, w);
+      }
+    }
+    __syncthreads();
+  }
+  if (timed_out) tc::mbar_wait(mbar, parity);  // give the MMAs in flight one more bounded wait
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, 128);
+}
+
+template <int B>
+cudaError_t launch_k_tc(const EncArgs& a, int sm_count, cudaStream_t s) {
+  using namespace ktc;
+  constexpr int W = B + 1;
+  const size_t smem = 4 * (size_t)kOp + (size_t)NV * L * W * 4 + (size_t)NV * 4 * 4 + NV * 8 + 8 * 4 + 16;
+  auto kern = encode_k_tc_kernel<B>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const long long work = (a.n_vectors + NV - 1) / NV;
+  const long long grid = work < sm_count ? work : sm_count;  // one CTA per SM (shared memory)
+  kern<<<(unsigned)grid, THREADS, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <int D, bool QJL, int B>
 cudaError_t launch_turbo(const EncArgs& a, int sm_count, cudaStream_t s) {
   using Sh = GroupShape<D>;
@@ -681,6 +891,14 @@ cudaError_t launch_turbo(const EncArgs& a, int sm_count, cudaStream_t s) {
 
 template <int D, bool QJL>
 cudaError_t launch_turbo_bits(const EncArgs& a, int sm_count, cudaStream_t s) {
+  if constexpr (QJL && D == 128) {
+    switch (a.view.idx_bits) {
+      case 1: return launch_k_tc<1>(a, sm_count, s);
+      case 2: return launch_k_tc<2>(a, sm_count, s);
+      case 3: return launch_k_tc<3>(a, sm_count, s);
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (a.view.idx_bits) {
     case 1: return launch_turbo<D, QJL, 1>(a, sm_count, s);
     case 2: return launch_turbo<D, QJL, 2>(a, sm_count, s);

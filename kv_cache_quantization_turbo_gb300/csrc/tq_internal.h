@@ -13,7 +13,7 @@
 namespace tq {
 
 // Status-word bits written by kernels (documented in tq_get_status).
-enum : uint32_t { kFlagSeqLen = 1u, kFlagBlockTable = 2u, kFlagSlot = 4u };
+enum : uint32_t { kFlagSeqLen = 1u, kFlagBlockTable = 2u, kFlagSlot = 4u, kFlagTimeout = 8u };
 
 // Highest supported head_dim and codebook sizes.
 constexpr int kMaxDim = 256;
