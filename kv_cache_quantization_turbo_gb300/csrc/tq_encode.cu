@@ -26,6 +26,8 @@
 //   - vector ids -> (layer, token, head) and slots -> (page, offset) use
 //     multiply-shift division by invariant divisors;
 //   - grids are persistent: min(work, resident CTAs) CTAs loop over the work.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include "tq_device.cuh"
@@ -655,211 +657,457 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_turbo_kernel(EncArgs a)
 
 
 // ---------------------------------------------------------------------------
-// Turbo K at d = 128 on the fifth-generation tensor cores.  A persistent CTA of 16 warps
-// encodes batches of 128 vectors: phase A (groups of 4 lanes per vector: stage 1, index
-// chunks, residual r 2^14 split into fp16 high and low parts, written into shared memory in
-// the core-matrix layout of an MMA operand); phase B (one thread issues
-// D[128 vectors x 128 projections] = r_lo S_hi^T + r_hi S_lo^T + r_hi S_hi^T as 24
-// tcgen05.mma of M 128, N 128, K 16 into tensor memory, S's split resident in shared memory
-// for the CTA's lifetime; every warp then reads 32 projections of one vector per lane and
-// packs their signs); phase C (codes = index | sign << b, stored).
+// Turbo K and V at d = 128 on the fifth-generation tensor cores.  One CTA per SM: 16 SIMT warps
+// and one issuer warp.  A batch is the H TB vectors (TB = floor(128 / H)) of TB consecutive
+// tokens of one layer, all heads; row r of a batch is token r / H, head r % H.
+//   - the issuer loads batches ahead by TMA (a 4-D tensor map over (d, head, token, layer); one
+//     box per 64-coordinate half, written with the 128-byte swizzle, which is the K-major
+//     operand layout the tensor core reads); tokens past the end read as zero;
+//   - the rotation Y = X (H D)^T runs as tcgen05.mma (M 128) into tensor memory, using the
+//     Sylvester split of H_128 into H_64 blocks: y_top = H64 D_a a + H64 D_b b,
+//     y_bot = H64 D_a a - H64 D_b b, with a, b the halves of x; the blocks are +-1 (exact in
+//     fp16) and x is fp16, so only the fp32 accumulation rounds;
+//   - turbo K: the QJL projection P = R S^T of R = 2^14 r split into fp16 high and low parts
+//     (R_lo S_hi + R_hi S_lo + R_hi S_hi); R_hi is written over the consumed input tile;
+//   - the issuer runs one batch ahead: the rotation of batch j + 1 and the projection of batch
+//     j overlap the SIMT work of batch j, and the sign bits of batch j are merged into its
+//     words during batch j + 1;
+//   - SIMT warp w reads tensor-memory lanes 32 (w % 4) .. + 31 (one row per thread) and
+//     columns 32 (w / 4) .. + 31, so a thread finishes 32 coordinates of one vector: norm
+//     (partial sums exchanged in shared memory), Lloyd-Max index, residual, sign bits, words.
+// Every wait is bounded; a wait that runs out stops the CTA at the next barrier and sets the
+// timeout status bit.
 // ---------------------------------------------------------------------------
-namespace ktc {
-constexpr int D = 128, NV = 128, L = 4, VPW = 8, WARPS = 16, THREADS = 32 * WARPS;
-constexpr int kOp = D * 128 * 2;  // bytes of one 128 x 128 f16 operand
-// byte offset of element (row, k) in a 128 x 128 K-major operand: core matrix (row / 8, k / 8)
-// at (row / 8 * 16 + k / 8) * 128, row % 8 at 16 (row % 8); lbo (along K) = 128, sbo (rows) = 2048
-__host__ __device__ constexpr int core_off(int row, int k) {
-  return ((row >> 3) * (D / 8) + (k >> 3)) * 128 + (row & 7) * 16 + (k & 7) * 2;
+namespace etc {
+constexpr int D = 128, NV = 128, SIMT_WARPS = 16, THREADS = 32 * (SIMT_WARPS + 1);
+constexpr int kOp = D * NV * 2;  // one 128 x 128 f16 operand
+constexpr int kG = 64 * 64 * 2;  // one 64 x 64 f16 block of the rotation
+// Every operand tile is K-major with the 128-byte swizzle, one 64-column half after the other:
+// half k/64 at 128 R (R rows), row r at 128 r, 16-byte chunk (k % 64) / 8 at chunk position
+// ((k % 64) / 8) ^ (r % 8).  The tensor copy writes the input tiles in this layout.
+template <int R>
+__host__ __device__ constexpr int swz(int row, int k) {
+  return (k >> 6) * (128 * R) + row * 128 + ((((k >> 3) & 7) ^ (row & 7)) << 4) + (k & 7) * 2;
 }
-constexpr uint32_t kLbo = 128, kSbo = 128 * (D / 8);
-}  // namespace ktc
+// K step ks (16 columns) of a tile with R rows: start of its descriptor
+template <int R>
+__host__ __device__ constexpr uint32_t kstep(int ks) {
+  return (uint32_t)((ks >> 2) * (128 * R) + (ks & 3) * 32);
+}
 
-template <int B>
-__global__ void __launch_bounds__(ktc::THREADS, 1) encode_k_tc_kernel(EncArgs a) {
-  using namespace ktc;
-  constexpr int W = B + 1;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int sub = lane % L, vl = lane / L;
+template <bool QJL>
+struct Smem {  // byte offsets in dynamic shared memory
+  static constexpr int NX = QJL ? 3 : 4;            // input tiles in flight
+  static constexpr int g = 0;                        // H64 D_a, H64 D_b, -H64 D_b
+  static constexpr int s_hi = 3 * kG;                // S high part (QJL)
+  static constexpr int s_lo = s_hi + (QJL ? kOp : 0);
+  static constexpr int x0 = s_lo + (QJL ? kOp : 0);  // NX input tiles (batch j in tile j % NX)
+  static constexpr int r_lo = x0 + NX * kOp;          // R low part (QJL)
+  static constexpr int ss = r_lo + (QJL ? kOp : 0);   // float [2][4][NV]: partial sums of y^2
+  static constexpr int rr = ss + 2 * 4 * NV * 4;      // float [2][4][NV]: partial sums of (2^14 r)^2
+  static constexpr int cb = rr + (QJL ? 2 * 4 * NV * 4 : 0);  // float [8]: centroids x 2^14
+  static constexpr int bar = cb + 8 * 4;  // mbarriers: full[NX], y[2], p[2], yfree[2], rready, pfree[2]
+  static constexpr int n_bar = NX + 9;
+  static constexpr int slot = bar + n_bar * 8;  // tensor-memory address, abort flag
+  static constexpr int total = slot + 16;
+};
 
-  extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char* s_hi = smem;
-  unsigned char* s_lo = smem + kOp;
-  unsigned char* r_hi = smem + 2 * kOp;
-  unsigned char* r_lo = smem + 3 * kOp;
-  uint32_t* code_s = reinterpret_cast<uint32_t*>(smem + 4 * kOp);  // [NV][L][W] index words
-  uint32_t* sig_s = code_s + NV * L * W;                             // [NV][4] QJL sign words
-  long long* vid_s = reinterpret_cast<long long*>(sig_s + NV * 4);   // [NV]
-  float* cb_s = reinterpret_cast<float*>(vid_s + NV);                 // [8]
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(cb_s + 8);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mbar + 1);
+struct TcShape {
+  int H, TB, rows;      // heads, tokens per batch, rows = H TB
+  uint32_t n_tb;        // token blocks per layer
+  FastDiv div_tb;
+  long long n_batches;  // n_layers n_tb
+  uint32_t tx_bytes;    // bytes one batch's copies deliver
+};
 
-  if (warp == 0) tc::tmem_alloc(tmem_slot, 128);
-  if (threadIdx.x == 0) tc::mbar_init(mbar, 1);
-  if (threadIdx.x < 8) cb_s[threadIdx.x] = a.tab.centroids[(B - 1) * 8 + threadIdx.x];
-  // S (row j = projection j) split into fp16 high and low parts, operand layout
-  for (int i = threadIdx.x; i < D * D; i += THREADS) {
-    const int j = i / D, c = i % D;
-    const float v = a.tab.S[i];
-    const __half h = __float2half_rn(v);
-    *reinterpret_cast<__half*>(s_hi + core_off(j, c)) = h;
-    *reinterpret_cast<__half*>(s_lo + core_off(j, c)) = __float2half_rn(v - __half2float(h));
+// Destination id of vector (layer l of the input, token t, head h), or -1 for a slot out of range.
+__device__ __forceinline__ long long vid_at(const EncArgs& a, int l, int t, int h, bool report) {
+  const long long slot = a.slots ? a.slots[t] : a.slot_begin + t;
+  const DevView& V = a.view;
+  const long long cap = V.num_pages * (long long)V.page_size;
+  if (slot < 0 || slot >= cap) {
+    if (report && h == 0) atomicOr(a.tab.status, kFlagSlot);
+    return -1;
   }
-  uint32_t sg[16];
-  lane_sign_masks(a.tab.signs, sub, sg);
-  float bfly[3];
+  long long page, p;
+  if (a.slot32) {
+    const uint32_t s32 = (uint32_t)slot, pg = fdiv(s32, a.div_p);
+    page = pg;
+    p = s32 - pg * (uint32_t)V.page_size;
+  } else {
+    page = slot / V.page_size;
+    p = slot - page * V.page_size;
+  }
+  return (((long long)(a.layer_begin + l) * V.num_pages + page) * V.H + h) * V.page_size + p;
+}
+
+// Merges the QJL sign bits (bit e of sbits: projection 32 c + e, c = the thread's column group)
+// into the thread's W words: the code of coordinate e is index | sign << B at bit W e.
+template <int W, int B>
+__device__ __forceinline__ void merge_signs(uint32_t (&w)[W], uint32_t sbits) {
+  if constexpr (W == 4) {
 #pragma unroll
-  for (int s = 0; s < 3; ++s) bfly[s] = (sub >> s) & 1 ? -1.f : 1.f;
-  float bnd[7];
+    for (int k = 0; k < 4; ++k) {  // bits 8k .. 8k + 7 -> bit 3 of each nibble of word k
+      uint32_t b = (sbits >> (8 * k)) & 0xFFu;
+      b = (b | (b << 12)) & 0x000F000Fu;
+      b = (b | (b << 6)) & 0x03030303u;
+      b = (b | (b << 3)) & 0x11111111u;
+      w[k] |= b << 3;
+    }
+  } else {
 #pragma unroll
-  for (int k = 0; k < 7; ++k) bnd[k] = k < (1 << B) - 1 ? a.tab.boundaries[(B - 1) * 7 + k] : 0.f;
+    for (int e = 0; e < 32; ++e) {
+      const int bit = W * e + B;
+      w[bit >> 5] |= ((sbits >> e) & 1u) << (bit & 31);
+    }
+  }
+}
+}  // namespace etc
+
+template <bool QJL, int B>
+__global__ void __launch_bounds__(etc::THREADS, 1)
+    encode_tc_kernel(const __grid_constant__ EncArgs a, const __grid_constant__ CUtensorMap tmap,
+                     const etc::TcShape sh) {
+  using namespace etc;
+  using L = Smem<QJL>;
+  constexpr int NX = L::NX;
+  constexpr int W = QJL ? B + 1 : B;
+  constexpr int kSimt = 32 * SIMT_WARPS;
+  constexpr uint32_t kCols = QJL ? 512 : 256;  // Y[2] at columns [0, 256), P[2] at [256, 512)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool issuer = warp == SIMT_WARPS;
+  const int q = warp & 3, cg = (warp >> 2) & 3;  // tensor-memory lane quarter, column group
+  const int v = 32 * q + lane;                   // this thread's row of the batch
+  const int tt = v / sh.H, h = v - tt * sh.H;
+
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  // operand tiles and tensor-copy destinations on a 1024-byte boundary (1 KB extra is allocated)
+  unsigned char* smem = smem_raw + ((1024u - (tc::smem_addr(smem_raw) & 1023u)) & 1023u);
+  float* ss_s = reinterpret_cast<float*>(smem + L::ss);
+  float* rr_s = reinterpret_cast<float*>(smem + L::rr);
+  float* cb_s = reinterpret_cast<float*>(smem + L::cb);
+  uint64_t* full_x = reinterpret_cast<uint64_t*>(smem + L::bar);  // tile landed (TMA)
+  uint64_t* bar_y = full_x + NX;    // rotation of a batch done
+  uint64_t* bar_p = bar_y + 2;      // projection of a batch done
+  uint64_t* yfree = bar_p + 2;      // Y of a batch read by all 16 SIMT warps
+  uint64_t* rready = yfree + 2;     // R of a batch stored by all 16 SIMT warps
+  uint64_t* pfree = rready + 1;     // P of a batch read by all 16 SIMT warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::slot);
+  const uint32_t sbase = tc::smem_addr(smem);
+
+  if (issuer) {
+    tc::tmem_alloc(tmem_slot, kCols);
+    if (lane == 0) {
+      for (int i = 0; i < NX + 4; ++i) tc::mbar_init(full_x + i, 1);
+      for (int i = NX + 4; i < L::n_bar; ++i) tc::mbar_init(full_x + i, SIMT_WARPS);
+    }
+  }
+  if (threadIdx.x < 8) cb_s[threadIdx.x] = a.tab.centroids[(B - 1) * 8 + threadIdx.x] * kRScale;
+  for (int i = threadIdx.x; i < 64 * 64; i += THREADS) {
+    const int n = i >> 6, k = i & 63;
+    const float hv = (__popc(n & k) & 1) ? -1.f : 1.f;
+    const float ga = a.tab.signs[k] < 0 ? -hv : hv, gb = a.tab.signs[64 + k] < 0 ? -hv : hv;
+    *reinterpret_cast<__half*>(smem + L::g + swz<64>(n, k)) = __float2half_rn(ga);
+    *reinterpret_cast<__half*>(smem + L::g + kG + swz<64>(n, k)) = __float2half_rn(gb);
+    *reinterpret_cast<__half*>(smem + L::g + 2 * kG + swz<64>(n, k)) = __float2half_rn(-gb);
+  }
+  if constexpr (QJL) {
+    for (int i = threadIdx.x; i < D * D; i += THREADS) {
+      const int n = i / D, k = i % D;
+      const float sv = a.tab.S[i];
+      const __half hh = __float2half_rn(sv);
+      *reinterpret_cast<__half*>(smem + L::s_hi + swz<128>(n, k)) = hh;
+      *reinterpret_cast<__half*>(smem + L::s_lo + swz<128>(n, k)) = __float2half_rn(sv - __half2float(hh));
+    }
+  }
   tc::fence_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const DevView& V = a.view;
-  constexpr uint32_t idesc = tc::idesc_f16_f32(128, 128);
-  uint32_t parity = 0;
-  bool timed_out = false;
+  const long long nj = (sh.n_batches - blockIdx.x + gridDim.x - 1) / gridDim.x;  // batches of this CTA
+  bool failed = false;
 
-  const long long n_batches = (a.n_vectors + NV - 1) / NV;
-  for (long long bt = blockIdx.x; bt < n_batches; bt += gridDim.x) {
-    const int v = warp * VPW + vl;  // this lane's vector in the batch
-    const long long gv = bt * NV + v;
-    // ---- phase A ----
-    {
-      Loc loc{nullptr, -1};
-      Raw32 raw;
-      raw.zero();
-      if (gv < a.n_vectors) {
-        loc = locate_one(a, (uint32_t)gv, sub == 0);
-        if (loc.vid >= 0) raw.load(loc.src + 32 * sub);
-      }
-      float x[32];
-      raw.to_float(x, sg);
-      const float n = group_stage1<D>(x, bfly);
-      float rr = 0.f;
-      uint32_t w[W] = {};
-      uint32_t hi[16], lo[16];
+  if (issuer) {
+    if (lane == 0) {
+      // ---- issuer: tensor copies and MMAs, driven by the barriers ----
+      long long next_tma = 0, mma1_done = 0, mma2_done = 0;  // counts issued
+      auto issue_tma = [&](long long jj) {
+        const uint32_t bt = (uint32_t)(blockIdx.x + jj * gridDim.x);
+        const uint32_t l = fdiv(bt, sh.div_tb), tb = bt - l * sh.n_tb;
+        uint64_t* fb = full_x + (int)(jj % NX);
+        tc::mbar_arrive_expect_tx(fb, sh.tx_bytes);
+        const uint32_t dst = sbase + L::x0 + (uint32_t)(jj % NX) * kOp;
+        tc::tma_load_4d(dst, &tmap, 0, 0, (int)(tb * sh.TB), (int)l, fb);
+        tc::tma_load_4d(dst + 128 * NV, &tmap, 64, 0, (int)(tb * sh.TB), (int)l, fb);
+        next_tma = jj + 1;
+      };
+      // descriptors: the 14-bit start field (address / 16) of a base descriptor plus an offset
+      const uint64_t dg = tc::desc_sw128(sbase + L::g);
+      const uint64_t dsh = tc::desc_sw128(sbase + L::s_hi), dsl = tc::desc_sw128(sbase + L::s_lo);
+      const uint64_t drl = tc::desc_sw128(sbase + L::r_lo);
+      auto issue_mma1 = [&](long long jj) {
+        const uint64_t dx = tc::desc_sw128(sbase + L::x0 + (uint32_t)(jj % NX) * kOp);
+        const uint32_t d0 = tmem + (uint32_t)(jj & 1) * 128;
+        constexpr uint32_t id64 = tc::idesc_f16_f32(128, 64);
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const uint32_t i0 = lloyd_index<B>(x[e], bnd), i1 = lloyd_index<B>(x[e + 1], bnd);
-        const float r0 = x[e] - cb_s[i0], r1 = x[e + 1] - cb_s[i1];
-        rr = fmaf(r0, r0, rr);
-        rr = fmaf(r1, r1, rr);
-        put_code<W>(w, e, i0);
-        put_code<W>(w, e + 1, i1);
-        split_pair(make_float2(r0 * kRScale, r1 * kRScale), hi[e / 2], lo[e / 2]);
-      }
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t da = dx + (kstep<NV>(ks) >> 4), db = dx + (kstep<NV>(4 + ks) >> 4);
+          const uint64_t go = kstep<64>(ks) >> 4;
+          tc::mma_f16(d0, da, dg + go, id64, ks > 0);
+          tc::mma_f16(d0, db, dg + (kG >> 4) + go, id64, true);
+          tc::mma_f16(d0 + 64, da, dg + go, id64, ks > 0);
+          tc::mma_f16(d0 + 64, db, dg + (2 * kG >> 4) + go, id64, true);
+        }
+        tc::commit(bar_y + (jj & 1));
+        mma1_done = jj + 1;
+      };
+      auto issue_mma2 = [&](long long jj) {
+        const uint64_t dh = tc::desc_sw128(sbase + L::x0 + (uint32_t)(jj % NX) * kOp);  // R_hi
+        const uint32_t dp = tmem + 256 + (uint32_t)(jj & 1) * 128;
+        constexpr uint32_t id128 = tc::idesc_f16_f32(128, 128);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int off = core_off(v, 32 * sub + 8 * j);
-        *reinterpret_cast<uint4*>(r_hi + off) = make_uint4(hi[4 * j], hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
-        *reinterpret_cast<uint4*>(r_lo + off) = make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
-      }
-      uint32_t* cw = code_s + (v * L + sub) * W;
-#pragma unroll
-      for (int k = 0; k < W; ++k) cw[k] = w[k];
-#pragma unroll
-      for (int m = 1; m < L; m <<= 1) rr += __shfl_xor_sync(kFull, rr, m);
-      const float rnorm = n * sqrtf(rr);
-      if (sub == 0) {
-        vid_s[v] = loc.vid;
-        if (loc.vid >= 0)
-          *reinterpret_cast<__half2*>(V.header + loc.vid * V.hdr_bytes) =
-              __halves2half2(__float2half_rn(n), __float2half_rn(rnorm));
-      }
-    }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    // ---- phase B: the projection on the tensor cores, signs from tensor memory ----
-    if (threadIdx.x == 0) {
-      const uint32_t ah = tc::smem_addr(r_hi), al = tc::smem_addr(r_lo);
-      const uint32_t bh = tc::smem_addr(s_hi), bl = tc::smem_addr(s_lo);
-#pragma unroll 1
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t koff = ks * 2 * 128;  // two core matrices along K per step
-        tc::mma_f16(tmem, tc::desc_kmajor(al + koff, kLbo, kSbo), tc::desc_kmajor(bh + koff, kLbo, kSbo), idesc,
-                    ks > 0);
-        tc::mma_f16(tmem, tc::desc_kmajor(ah + koff, kLbo, kSbo), tc::desc_kmajor(bl + koff, kLbo, kSbo), idesc,
-                    true);
-        tc::mma_f16(tmem, tc::desc_kmajor(ah + koff, kLbo, kSbo), tc::desc_kmajor(bh + koff, kLbo, kSbo), idesc,
-                    true);
-      }
-      tc::commit(mbar);
-    }
-    const bool ok = tc::mbar_wait(mbar, parity);
-    if (__syncthreads_or(!ok)) {  // the wait ran out: flag it and leave
-      if (threadIdx.x == 0) atomicOr(a.tab.status, kFlagTimeout);
-      timed_out = true;
-      break;
-    }
-    parity ^= 1u;
-    tc::fence_after_sync();
-    {
-      // warp: tensor-memory lanes 32 (warp % 4) .. + 31 (vectors), columns 32 (warp / 4) .. + 31
-      const int q = warp & 3, cbk = warp >> 2;
-      uint32_t pv[32];
-      tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * cbk, pv);
-      uint32_t word = 0;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) word |= (__uint_as_float(pv[j]) > 0.f ? 1u : 0u) << j;
-      sig_s[(32 * q + lane) * 4 + cbk] = word;
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    // ---- phase C: codes = index | sign << B, store ----
-    {
-      const long long vid = vid_s[v];
-      if (vid >= 0) {
-        uint32_t w[W];
-        const uint32_t* cw = code_s + (v * L + sub) * W;
-#pragma unroll
-        for (int k = 0; k < W; ++k) w[k] = cw[k];
-        const uint32_t sbits = sig_s[v * 4 + sub];
-        if constexpr (W == 4) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint32_t b = (sbits >> (8 * k)) & 0xFFu;
-            b = (b | (b << 12)) & 0x000F000Fu;
-            b = (b | (b << 6)) & 0x03030303u;
-            b = (b | (b << 3)) & 0x11111111u;
-            w[k] |= b << 3;
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t ka = kstep<NV>(ks) >> 4, kb = kstep<D>(ks) >> 4;
+          tc::mma_f16(dp, drl + ka, dsh + kb, id128, ks > 0);
+          tc::mma_f16(dp, dh + ka, dsl + kb, id128, true);
+          tc::mma_f16(dp, dh + ka, dsh + kb, id128, true);
+        }
+        tc::commit(bar_p + (jj & 1));
+        mma2_done = jj + 1;
+      };
+      bool ok = true;
+      for (long long jj = 0; jj < NX && jj < nj; ++jj) issue_tma(jj);
+      for (long long j = 0; ok && j <= nj; ++j) {
+        // rotation of batch j: its tile landed, and Y[j & 1] (batch j - 2) was read
+        if (j < nj) {
+          ok = tc::mbar_wait(full_x + (int)(j % NX), (uint32_t)(j / NX) & 1u);
+          if (ok && j >= 2) ok = tc::mbar_wait(yfree + (j & 1), (uint32_t)((j - 2) >> 1) & 1u);
+          if (!ok) break;
+          tc::fence_after_sync();
+          issue_mma1(j);
+        }
+        if (j == 0) continue;
+        const long long jp = j - 1;
+        if constexpr (QJL) {
+          // projection of batch jp: its R is stored, and P[jp & 1] (batch jp - 2) was read
+          ok = tc::mbar_wait(rready, (uint32_t)jp & 1u);
+          if (ok && jp >= 2) ok = tc::mbar_wait(pfree + (jp & 1), (uint32_t)((jp - 2) >> 1) & 1u);
+          if (!ok) break;
+          tc::fence_after_sync();
+          issue_mma2(jp);
+          // tile jp % NX (R_hi of batch jp) is free once its projection completed
+          if (jp + NX < nj) {
+            ok = tc::mbar_wait(bar_p + (jp & 1), (uint32_t)(jp >> 1) & 1u);
+            if (ok) issue_tma(jp + NX);
           }
         } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int bit = W * e + B;
-            w[bit >> 5] |= ((sbits >> e) & 1u) << (bit & 31);
+          // tile jp % NX is free once the rotation of batch jp completed
+          if (jp + NX < nj) {
+            ok = tc::mbar_wait(bar_y + (jp & 1), (uint32_t)(jp >> 1) & 1u);
+            if (ok) issue_tma(jp + NX);
           }
         }
-        store_words<W>(reinterpret_cast<uint32_t*>(V.payload + vid * V.pay_bytes) + W * sub, w);
+      }
+      if (!ok) {
+        failed = true;
+        // bounded waits for whatever is still in flight
+        for (long long jj = mma1_done; jj < next_tma; ++jj)
+          tc::mbar_wait(full_x + (int)(jj % NX), (uint32_t)(jj / NX) & 1u);
+        if (mma1_done > 0) tc::mbar_wait(bar_y + ((mma1_done - 1) & 1), (uint32_t)((mma1_done - 1) >> 1) & 1u);
+        if (QJL && mma2_done > 0) tc::mbar_wait(bar_p + ((mma2_done - 1) & 1), (uint32_t)((mma2_done - 1) >> 1) & 1u);
       }
     }
-    __syncthreads();
+  } else {
+    // ---- SIMT warps ----
+    float bnd[7];
+#pragma unroll
+    for (int k = 0; k < 7; ++k) bnd[k] = k < (1 << B) - 1 ? a.tab.boundaries[(B - 1) * 7 + k] : 0.f;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    uint32_t w_prev[W] = {};
+    long long vid_prev = -1;
+    float n_prev = 0.f;
+    bool ok = true;
+    for (long long j = 0; j < nj; ++j) {
+      const int yb = (int)(j & 1);
+      // (a) Y of batch j: partial sum of squares of this thread's 32 coordinates
+      ok = tc::mbar_wait(bar_y + yb, (uint32_t)(j >> 1) & 1u) && ok;
+      tc::fence_after_sync();
+      uint32_t t[32];
+      tc::tmem_ld32(tmem + lane_base + yb * 128 + 32 * cg, t);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(yfree + yb);
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) ss = fmaf(__uint_as_float(t[e]), __uint_as_float(t[e]), ss);
+      ss_s[(yb * 4 + cg) * NV + v] = ss;
+      if (tc::bar_sync_or(1, kSimt, !ok)) {
+        failed = true;
+        break;
+      }
+      // (b) norm, destination
+      const uint32_t bt = (uint32_t)(blockIdx.x + j * gridDim.x);
+      const uint32_t l = fdiv(bt, sh.div_tb), tb = bt - l * sh.n_tb;
+      const int tok = (int)(tb * sh.TB) + tt;
+      long long vid = -1;
+      if (v < sh.rows && tok < a.n_tokens) vid = vid_at(a, (int)l, tok, h, cg == 0);
+      const float* sp = ss_s + yb * 4 * NV + v;
+      const float n = sqrtf((sp[0] + sp[NV] + sp[2 * NV] + sp[3 * NV]) * (1.f / D));  // |x| = |H D x| / sqrt(d)
+      const float f = n > 0.f ? __fdividef(inv_sqrt_dim<D>(), n) : 0.f;
+      uint32_t w[W] = {};
+      if constexpr (QJL) {
+        // header of batch j - 1 (its residual partial sums were stored before the barrier)
+        if (j > 0 && cg == 0 && vid_prev >= 0) {
+          const float* rp = rr_s + (1 - yb) * 4 * NV + v;
+          const float rs = (rp[0] + rp[NV] + rp[2 * NV] + rp[3 * NV]) * (1.f / (kRScale * kRScale));
+          *reinterpret_cast<__half2*>(V.header + vid_prev * V.hdr_bytes) =
+              __halves2half2(__float2half_rn(n_prev), __float2half_rn(n_prev * sqrtf(rs)));
+        }
+        // (c) index and residual; R_lo is free once the projection of batch j - 1 completed
+        if (j > 0) {
+          ok = tc::mbar_wait(bar_p + (1 - yb), (uint32_t)((j - 1) >> 1) & 1u) && ok;
+          tc::fence_after_sync();
+        }
+        unsigned char* rh = smem + L::x0 + (int)(j % NX) * kOp;  // the rotation consumed X: R_hi goes there
+        float rr = 0.f;
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e2 = 0; e2 < 8; e2 += 2) {
+            const int e = 8 * c8 + e2;
+            const float u0 = __uint_as_float(t[e]) * f, u1 = __uint_as_float(t[e + 1]) * f;
+            const uint32_t i0 = lloyd_index<B>(u0, bnd), i1 = lloyd_index<B>(u1, bnd);
+            const float r0 = fmaf(u0, kRScale, -cb_s[i0]), r1 = fmaf(u1, kRScale, -cb_s[i1]);  // 2^14 (u - c)
+            rr = fmaf(r0, r0, rr);
+            rr = fmaf(r1, r1, rr);
+            put_code<W>(w, e, i0);
+            put_code<W>(w, e + 1, i1);
+            split_pair(make_float2(r0, r1), hi[e2 / 2], lo[e2 / 2]);
+          }
+          const int off = swz<NV>(v, 32 * cg + 8 * c8);
+          *reinterpret_cast<uint4*>(rh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(smem + L::r_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        rr_s[(yb * 4 + cg) * NV + v] = rr;
+        tc::fence_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(rready);
+        // (e) sign bits of batch j - 1: its projection completed (waited above)
+        if (j > 0) {
+          uint32_t tp[32];
+          tc::tmem_ld32(tmem + lane_base + 256 + (1 - yb) * 128 + 32 * cg, tp);
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(pfree + (1 - yb));
+          uint32_t sbits = 0;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sbits |= (__uint_as_float(tp[e]) > 0.f ? 1u : 0u) << e;
+          merge_signs<W, B>(w_prev, sbits);
+          if (vid_prev >= 0)
+            store_words<W>(reinterpret_cast<uint32_t*>(V.payload + vid_prev * V.pay_bytes) + W * cg, w_prev);
+        }
+#pragma unroll
+        for (int k = 0; k < W; ++k) w_prev[k] = w[k];
+        vid_prev = vid;
+        n_prev = n;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) put_code<W>(w, e, lloyd_index<B>(__uint_as_float(t[e]) * f, bnd));
+        if (vid >= 0) {
+          if (cg == 0) *reinterpret_cast<__half*>(V.header + vid * V.hdr_bytes) = __float2half_rn(n);
+          store_words<W>(reinterpret_cast<uint32_t*>(V.payload + vid * V.pay_bytes) + W * cg, w);
+        }
+      }
+    }
+    if constexpr (QJL) {
+      // the last batch: its header and sign bits
+      if (!failed && tc::bar_sync_or(1, kSimt, !ok)) failed = true;
+      if (!failed) {
+        const long long jl = nj - 1;
+        const int lb = (int)(jl & 1);
+        if (cg == 0 && vid_prev >= 0) {
+          const float* rp = rr_s + lb * 4 * NV + v;
+          const float rs = (rp[0] + rp[NV] + rp[2 * NV] + rp[3 * NV]) * (1.f / (kRScale * kRScale));
+          *reinterpret_cast<__half2*>(V.header + vid_prev * V.hdr_bytes) =
+              __halves2half2(__float2half_rn(n_prev), __float2half_rn(n_prev * sqrtf(rs)));
+        }
+        if (tc::mbar_wait(bar_p + lb, (uint32_t)(jl >> 1) & 1u)) {
+          tc::fence_after_sync();
+          uint32_t tp[32];
+          tc::tmem_ld32(tmem + lane_base + 256 + lb * 128 + 32 * cg, tp);
+          uint32_t sbits = 0;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sbits |= (__uint_as_float(tp[e]) > 0.f ? 1u : 0u) << e;
+          merge_signs<W, B>(w_prev, sbits);
+          if (vid_prev >= 0)
+            store_words<W>(reinterpret_cast<uint32_t*>(V.payload + vid_prev * V.pay_bytes) + W * cg, w_prev);
+        } else {
+          failed = true;
+        }
+      }
+    }
   }
-  if (timed_out) tc::mbar_wait(mbar, parity);  // give the MMAs in flight one more bounded wait
+  if (failed) atomicOr(a.tab.status, kFlagTimeout);
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 128);
+  if (issuer) tc::tmem_dealloc(tmem, kCols);
 }
 
-template <int B>
-cudaError_t launch_k_tc(const EncArgs& a, int sm_count, cudaStream_t s) {
-  using namespace ktc;
-  constexpr int W = B + 1;
-  const size_t smem = 4 * (size_t)kOp + (size_t)NV * L * W * 4 + (size_t)NV * 4 * 4 + NV * 8 + 8 * 4 + 16;
-  auto kern = encode_k_tc_kernel<B>;
+// cuTensorMapEncodeTiled from the driver (no link-time dependency on it); null if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// Launches the tensor-core encoder; returns false (nothing launched) where its tensor map cannot
+// describe the input, and the caller takes the register path.
+template <bool QJL, int B>
+bool launch_tc(const EncArgs& a, int sm_count, cudaStream_t s, cudaError_t* err) {
+  using namespace etc;
+  const int H = a.view.H;
+  const auto encode = tensor_map_encoder();
+  if (!encode || H > NV || a.n_tokens <= 0) return false;
+  TcShape sh{};
+  sh.H = H;
+  sh.TB = NV / H;
+  sh.rows = sh.H * sh.TB;
+  sh.n_tb = (uint32_t)((a.n_tokens + sh.TB - 1) / sh.TB);
+  sh.div_tb = make_fastdiv(sh.n_tb);
+  sh.n_batches = (long long)a.n_layers * sh.n_tb;
+  sh.tx_bytes = (uint32_t)(D / 8) * 8u * (uint32_t)sh.rows * 2u;
+  if (sh.n_batches >= (1ll << 31)) return false;
+  CUtensorMap tmap;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)a.n_tokens, (cuuint64_t)a.n_layers};
+  const long long ts = a.token_stride * 2, ls = a.n_layers > 1 ? a.layer_stride * 2 : ts * a.n_tokens;
+  if (ts <= 0 || ls <= 0) return false;
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)ts, (cuuint64_t)ls};
+  const cuuint32_t box[4] = {64, (cuuint32_t)H, (cuuint32_t)sh.TB, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<__half*>(a.x), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  constexpr size_t smem = Smem<QJL>::total + 1024;
+  static_assert(smem <= 227 * 1024, "shared memory");
+  auto kern = encode_tc_kernel<QJL, B>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  const long long work = (a.n_vectors + NV - 1) / NV;
-  const long long grid = work < sm_count ? work : sm_count;  // one CTA per SM (shared memory)
-  kern<<<(unsigned)grid, THREADS, smem, s>>>(a);
-  return cudaGetLastError();
+  if (e == cudaSuccess) {
+    const long long grid = sh.n_batches < sm_count ? sh.n_batches : sm_count;  // one CTA per SM
+    kern<<<(unsigned)grid, THREADS, smem, s>>>(a, tmap, sh);
+    e = cudaGetLastError();
+  }
+  *err = e;
+  return true;
 }
 
 template <int D, bool QJL, int B>
@@ -891,13 +1139,15 @@ cudaError_t launch_turbo(const EncArgs& a, int sm_count, cudaStream_t s) {
 
 template <int D, bool QJL>
 cudaError_t launch_turbo_bits(const EncArgs& a, int sm_count, cudaStream_t s) {
-  if constexpr (QJL && D == 128) {
+  if constexpr (D == 128) {
+    cudaError_t e = cudaSuccess;
+    bool done = false;
     switch (a.view.idx_bits) {
-      case 1: return launch_k_tc<1>(a, sm_count, s);
-      case 2: return launch_k_tc<2>(a, sm_count, s);
-      case 3: return launch_k_tc<3>(a, sm_count, s);
+      case 1: done = launch_tc<QJL, 1>(a, sm_count, s, &e); break;
+      case 2: done = launch_tc<QJL, 2>(a, sm_count, s, &e); break;
+      case 3: done = launch_tc<QJL, 3>(a, sm_count, s, &e); break;
     }
-    return cudaErrorInvalidValue;
+    if (done) return e;
   }
   switch (a.view.idx_bits) {
     case 1: return launch_turbo<D, QJL, 1>(a, sm_count, s);

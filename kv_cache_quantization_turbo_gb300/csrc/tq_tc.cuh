@@ -19,6 +19,15 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t addr, uint32_t lbo, uin
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
 
+// Shared-memory matrix descriptor, K-major operand with the 128-byte swizzle: rows of 64 f16
+// (128 bytes) at 128-byte stride, 16-byte chunk c of row r stored at chunk c ^ (r % 8), 8-row
+// atoms of 1024 bytes (sbo); the atom must sit on a 1024-byte boundary.  A K step of 16 elements
+// inside the atom advances the start address by 32 bytes.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+
 // Instruction descriptor of kind::f16: f16 A and B (K-major), f32 accumulator, M x N.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
   return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
@@ -59,17 +68,54 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
 }
 
-// Waits until the phase with the given parity has completed; false if it did not within the bound.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int max_tries = 1 << 22) {
+// Waits until the phase with the given parity has completed; false if it did not within the
+// bound.  Each try suspends the thread for at most 1 us (the suspend-time hint), so the whole
+// wait ends within about a second.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int max_tries = 1 << 20) {
   uint32_t done = 0;
   for (int it = 0; it < max_tries && !done; ++it) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
         : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(1000u)
         : "memory");
   }
   return done != 0;
+}
+
+// One arrival on the mbarrier that also expects tx_bytes of asynchronous copies.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t tx_bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(tx_bytes)
+               : "memory");
+}
+
+// Tiled 4-D tensor copy global -> shared (box of the tensor map at coordinates c0..c3); completion
+// is counted in bytes on the mbarrier.  Coordinates outside the tensor read as zero.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// One plain arrival on the mbarrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Named barrier `id` over `count` threads (a multiple of 32) that also ORs a predicate.
+__device__ __forceinline__ bool bar_sync_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 // 32 consecutive 32-bit columns of this warp's 32 tensor-memory lanes (lane i of the warp reads
