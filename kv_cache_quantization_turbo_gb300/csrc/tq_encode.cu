@@ -658,28 +658,35 @@ __global__ void __launch_bounds__(kEncThreads, 2) encode_turbo_kernel(EncArgs a)
 
 // ---------------------------------------------------------------------------
 // Turbo K and V at d = 128 on the fifth-generation tensor cores.  One CTA per SM: 16 SIMT warps
-// and one issuer warp.  A batch is the H TB vectors (TB = floor(128 / H)) of TB consecutive
-// tokens of one layer, all heads; row r of a batch is token r / H, head r % H.
-//   - the issuer loads batches ahead by TMA (a 4-D tensor map over (d, head, token, layer); one
+// and issuer warps (A: tensor copies and rotations; B, turbo K only: projections).  A batch is
+// the H TB vectors (TB = floor(128 / H)) of TB consecutive tokens of one layer, all heads; row r
+// of a batch is token r / H, head r % H.
+//   - issuer A loads batches ahead by TMA (a 4-D tensor map over (d, head, token, layer); one
 //     box per 64-coordinate half, written with the 128-byte swizzle, which is the K-major
 //     operand layout the tensor core reads); tokens past the end read as zero;
-//   - the rotation Y = X (H D)^T runs as tcgen05.mma (M 128) into tensor memory, using the
-//     Sylvester split of H_128 into H_64 blocks: y_top = H64 D_a a + H64 D_b b,
-//     y_bot = H64 D_a a - H64 D_b b, with a, b the halves of x; the blocks are +-1 (exact in
-//     fp16) and x is fp16, so only the fp32 accumulation rounds;
+//   - the rotation Y = X (H D)^T runs as tcgen05.mma (M 128) into tensor memory.  H D has
+//     entries +-1 (exact in fp16) and x is fp16, so only the fp32 accumulation rounds.  V keeps
+//     H D whole (8 MMAs of N 128); turbo K, short of shared memory, uses the Sylvester split of
+//     H_128 into H_64 blocks: y_top = H64 D_a a + H64 D_b b, y_bot = H64 D_a a - H64 D_b b, with
+//     a, b the halves of x (16 MMAs of N 64);
 //   - turbo K: the QJL projection P = R S^T of R = 2^14 r split into fp16 high and low parts
 //     (R_lo S_hi + R_hi S_lo + R_hi S_hi); R_hi is written over the consumed input tile;
-//   - the issuer runs one batch ahead: the rotation of batch j + 1 and the projection of batch
-//     j overlap the SIMT work of batch j, and the sign bits of batch j are merged into its
-//     words during batch j + 1;
+//   - the issuers run ahead of the SIMT warps: the rotation of batch j + 1 and the projection of
+//     batch j overlap the SIMT work of batch j, and the sign bits of batch j are merged into its
+//     words during batch j + 1.  SIMT warps report per warp on mbarriers (Y read, R stored,
+//     P read) and meet each other on a named barrier, so the issuers never stop them;
 //   - SIMT warp w reads tensor-memory lanes 32 (w % 4) .. + 31 (one row per thread) and
 //     columns 32 (w / 4) .. + 31, so a thread finishes 32 coordinates of one vector: norm
 //     (partial sums exchanged in shared memory), Lloyd-Max index, residual, sign bits, words.
-// Every wait is bounded; a wait that runs out stops the CTA at the next barrier and sets the
-// timeout status bit.
+// Every wait is bounded; a wait that runs out stops the CTA and sets the timeout status bit.
 // ---------------------------------------------------------------------------
 namespace etc {
-constexpr int D = 128, NV = 128, SIMT_WARPS = 16, THREADS = 32 * (SIMT_WARPS + 1);
+constexpr int D = 128, NV = 128, SIMT_WARPS = 16;
+// issuer warps: A (tensor copies, rotation), and for turbo K B (projection) on another SM
+// sub-partition: an MMA or copy instruction waits long for an issue slot next to warps that keep
+// the FMA pipe saturated, so the projection's 24 MMAs get a scheduler of their own
+template <bool QJL>
+constexpr int kThreads = 32 * (SIMT_WARPS + (QJL ? 2 : 1));
 constexpr int kOp = D * NV * 2;  // one 128 x 128 f16 operand
 constexpr int kG = 64 * 64 * 2;  // one 64 x 64 f16 block of the rotation
 // Every operand tile is K-major with the 128-byte swizzle, one 64-column half after the other:
@@ -698,8 +705,8 @@ __host__ __device__ constexpr uint32_t kstep(int ks) {
 template <bool QJL>
 struct Smem {  // byte offsets in dynamic shared memory
   static constexpr int NX = QJL ? 3 : 4;            // input tiles in flight
-  static constexpr int g = 0;                        // H64 D_a, H64 D_b, -H64 D_b
-  static constexpr int s_hi = 3 * kG;                // S high part (QJL)
+  static constexpr int g = 0;                        // K: H64 D_a, H64 D_b, -H64 D_b; V: H D (128 x 128)
+  static constexpr int s_hi = QJL ? 3 * kG : kOp;    // S high part (QJL)
   static constexpr int s_lo = s_hi + (QJL ? kOp : 0);
   static constexpr int x0 = s_lo + (QJL ? kOp : 0);  // NX input tiles (batch j in tile j % NX)
   static constexpr int r_lo = x0 + NX * kOp;          // R low part (QJL)
@@ -762,10 +769,49 @@ __device__ __forceinline__ void merge_signs(uint32_t (&w)[W], uint32_t sbits) {
     }
   }
 }
+
+// Lloyd-Max index on the FMA pipe.  With C_k = -prev(b_k) 2^100 (prev: the next float below;
+// C_k = 1 for b_k = 0), sat(u 2^100 + C_k) is 1 for u >= b_k and 0 below, exactly, whenever
+// u - prev(b_k) is 0 or at least 2^-100 in magnitude.  Nonzero rotated coordinates are sums of
+// fp16 values scaled by 1 / (n sqrt(d)), at least 2^-24 / (65504 sqrt(d)) in magnitude, so
+// this holds for every boundary that is 0 or at least 2^-60 in magnitude (checked per call).
+// The index is the sum of the steps: the count of boundaries <= u, ties included.
+template <int B>
+__device__ __forceinline__ bool step_constants(const float (&bnd)[7], float (&cst)[7]) {
+  bool ok = true;
+#pragma unroll
+  for (int k = 0; k < 7; ++k) {
+    const float b = bnd[k];
+    if (k >= (1 << B) - 1) {
+      cst[k] = 0.f;
+    } else if (b == 0.f) {
+      cst[k] = 1.f;
+    } else {
+      ok = ok && fabsf(b) >= 0x1p-60f;
+      cst[k] = -nextafterf(b, -INFINITY) * 0x1p100f;
+    }
+  }
+  return ok;
+}
+// index of y (a rotated coordinate before the 1 / (n sqrt(d)) scale; F = 2^100 / (n sqrt(d))) as a float
+template <int B>
+__device__ __forceinline__ float step_index(float y, float F, const float (&cst)[7]) {
+  float idx = __saturatef(fmaf(y, F, cst[0]));
+#pragma unroll
+  for (int k = 1; k < (1 << B) - 1; ++k) idx += __saturatef(fmaf(y, F, cst[k]));
+  return idx;
+}
+// ORs an nb-bit chunk into the thread's W words at bit offset off (compile-time after unrolling).
+template <int W>
+__device__ __forceinline__ void or_bits(uint32_t (&w)[W], int off, int nb, uint32_t v) {
+  const int k = off >> 5, sh = off & 31;
+  w[k] |= v << sh;
+  if (sh + nb > 32) w[k + 1] |= v >> (32 - sh);
+}
 }  // namespace etc
 
 template <bool QJL, int B>
-__global__ void __launch_bounds__(etc::THREADS, 1)
+__global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
     encode_tc_kernel(const __grid_constant__ EncArgs a, const __grid_constant__ CUtensorMap tmap,
                      const etc::TcShape sh) {
   using namespace etc;
@@ -775,7 +821,8 @@ __global__ void __launch_bounds__(etc::THREADS, 1)
   constexpr int kSimt = 32 * SIMT_WARPS;
   constexpr uint32_t kCols = QJL ? 512 : 256;  // Y[2] at columns [0, 256), P[2] at [256, 512)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool issuer = warp == SIMT_WARPS;
+  constexpr int THREADS = kThreads<QJL>;
+  const bool issuer = warp >= SIMT_WARPS;  // warp SIMT_WARPS: issuer A; SIMT_WARPS + 1: issuer B
   const int q = warp & 3, cg = (warp >> 2) & 3;  // tensor-memory lane quarter, column group
   const int v = 32 * q + lane;                   // this thread's row of the batch
   const int tt = v / sh.H, h = v - tt * sh.H;
@@ -795,7 +842,7 @@ __global__ void __launch_bounds__(etc::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::slot);
   const uint32_t sbase = tc::smem_addr(smem);
 
-  if (issuer) {
+  if (warp == SIMT_WARPS) {
     tc::tmem_alloc(tmem_slot, kCols);
     if (lane == 0) {
       for (int i = 0; i < NX + 4; ++i) tc::mbar_init(full_x + i, 1);
@@ -803,13 +850,21 @@ __global__ void __launch_bounds__(etc::THREADS, 1)
     }
   }
   if (threadIdx.x < 8) cb_s[threadIdx.x] = a.tab.centroids[(B - 1) * 8 + threadIdx.x] * kRScale;
-  for (int i = threadIdx.x; i < 64 * 64; i += THREADS) {
-    const int n = i >> 6, k = i & 63;
-    const float hv = (__popc(n & k) & 1) ? -1.f : 1.f;
-    const float ga = a.tab.signs[k] < 0 ? -hv : hv, gb = a.tab.signs[64 + k] < 0 ? -hv : hv;
-    *reinterpret_cast<__half*>(smem + L::g + swz<64>(n, k)) = __float2half_rn(ga);
-    *reinterpret_cast<__half*>(smem + L::g + kG + swz<64>(n, k)) = __float2half_rn(gb);
-    *reinterpret_cast<__half*>(smem + L::g + 2 * kG + swz<64>(n, k)) = __float2half_rn(-gb);
+  if constexpr (QJL) {
+    for (int i = threadIdx.x; i < 64 * 64; i += THREADS) {
+      const int n = i >> 6, k = i & 63;
+      const float hv = (__popc(n & k) & 1) ? -1.f : 1.f;
+      const float ga = a.tab.signs[k] < 0 ? -hv : hv, gb = a.tab.signs[64 + k] < 0 ? -hv : hv;
+      *reinterpret_cast<__half*>(smem + L::g + swz<64>(n, k)) = __float2half_rn(ga);
+      *reinterpret_cast<__half*>(smem + L::g + kG + swz<64>(n, k)) = __float2half_rn(gb);
+      *reinterpret_cast<__half*>(smem + L::g + 2 * kG + swz<64>(n, k)) = __float2half_rn(-gb);
+    }
+  } else {
+    for (int i = threadIdx.x; i < D * D; i += THREADS) {  // (H D)[n][k] = (-1)^popcount(n & k) s_k
+      const int n = i / D, k = i % D;
+      const float hv = (__popc(n & k) & 1) ? -1.f : 1.f;
+      *reinterpret_cast<__half*>(smem + L::g + swz<D>(n, k)) = __float2half_rn(a.tab.signs[k] < 0 ? -hv : hv);
+    }
   }
   if constexpr (QJL) {
     for (int i = threadIdx.x; i < D * D; i += THREADS) {
@@ -831,7 +886,7 @@ __global__ void __launch_bounds__(etc::THREADS, 1)
 
   if (issuer) {
     if (lane == 0) {
-      // ---- issuer: tensor copies and MMAs, driven by the barriers ----
+      // ---- issuers: tensor copies and MMAs, driven by the barriers ----
       long long next_tma = 0, mma1_done = 0, mma2_done = 0;  // counts issued
       auto issue_tma = [&](long long jj) {
         const uint32_t bt = (uint32_t)(blockIdx.x + jj * gridDim.x);
@@ -845,26 +900,33 @@ __global__ void __launch_bounds__(etc::THREADS, 1)
       };
       // descriptors: the 14-bit start field (address / 16) of a base descriptor plus an offset
       const uint64_t dg = tc::desc_sw128(sbase + L::g);
-      const uint64_t dsh = tc::desc_sw128(sbase + L::s_hi), dsl = tc::desc_sw128(sbase + L::s_lo);
-      const uint64_t drl = tc::desc_sw128(sbase + L::r_lo);
       auto issue_mma1 = [&](long long jj) {
         const uint64_t dx = tc::desc_sw128(sbase + L::x0 + (uint32_t)(jj % NX) * kOp);
         const uint32_t d0 = tmem + (uint32_t)(jj & 1) * 128;
-        constexpr uint32_t id64 = tc::idesc_f16_f32(128, 64);
+        if constexpr (QJL) {
+          constexpr uint32_t id64 = tc::idesc_f16_f32(128, 64);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t da = dx + (kstep<NV>(ks) >> 4), db = dx + (kstep<NV>(4 + ks) >> 4);
-          const uint64_t go = kstep<64>(ks) >> 4;
-          tc::mma_f16(d0, da, dg + go, id64, ks > 0);
-          tc::mma_f16(d0, db, dg + (kG >> 4) + go, id64, true);
-          tc::mma_f16(d0 + 64, da, dg + go, id64, ks > 0);
-          tc::mma_f16(d0 + 64, db, dg + (2 * kG >> 4) + go, id64, true);
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t da = dx + (kstep<NV>(ks) >> 4), db = dx + (kstep<NV>(4 + ks) >> 4);
+            const uint64_t go = kstep<64>(ks) >> 4;
+            tc::mma_f16(d0, da, dg + go, id64, ks > 0);
+            tc::mma_f16(d0, db, dg + (kG >> 4) + go, id64, true);
+            tc::mma_f16(d0 + 64, da, dg + go, id64, ks > 0);
+            tc::mma_f16(d0 + 64, db, dg + (2 * kG >> 4) + go, id64, true);
+          }
+        } else {
+          constexpr uint32_t id128 = tc::idesc_f16_f32(128, 128);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            tc::mma_f16(d0, dx + (kstep<NV>(ks) >> 4), dg + (kstep<D>(ks) >> 4), id128, ks > 0);
         }
         tc::commit(bar_y + (jj & 1));
         mma1_done = jj + 1;
       };
       auto issue_mma2 = [&](long long jj) {
         const uint64_t dh = tc::desc_sw128(sbase + L::x0 + (uint32_t)(jj % NX) * kOp);  // R_hi
+        const uint64_t drl = tc::desc_sw128(sbase + L::r_lo);
+        const uint64_t dsh = tc::desc_sw128(sbase + L::s_hi), dsl = tc::desc_sw128(sbase + L::s_lo);
         const uint32_t dp = tmem + 256 + (uint32_t)(jj & 1) * 128;
         constexpr uint32_t id128 = tc::idesc_f16_f32(128, 128);
 #pragma unroll
@@ -878,45 +940,43 @@ __global__ void __launch_bounds__(etc::THREADS, 1)
         mma2_done = jj + 1;
       };
       bool ok = true;
-      for (long long jj = 0; jj < NX && jj < nj; ++jj) issue_tma(jj);
-      for (long long j = 0; ok && j <= nj; ++j) {
-        // rotation of batch j: its tile landed, and Y[j & 1] (batch j - 2) was read
-        if (j < nj) {
-          ok = tc::mbar_wait(full_x + (int)(j % NX), (uint32_t)(j / NX) & 1u);
-          if (ok && j >= 2) ok = tc::mbar_wait(yfree + (j & 1), (uint32_t)((j - 2) >> 1) & 1u);
-          if (!ok) break;
-          tc::fence_after_sync();
-          issue_mma1(j);
+      if (warp == SIMT_WARPS) {
+        // issuer A: tiles and rotations
+        for (long long jj = 0; jj < NX && jj < nj; ++jj) issue_tma(jj);
+        for (long long j = 0; ok && j <= nj; ++j) {
+          // rotation of batch j: its tile landed, and Y[j & 1] (batch j - 2) was read
+          if (j < nj) {
+            ok = tc::mbar_wait(full_x + (int)(j % NX), (uint32_t)(j / NX) & 1u);
+            if (ok && j >= 2) ok = tc::mbar_wait(yfree + (j & 1), (uint32_t)((j - 2) >> 1) & 1u);
+            if (!ok) break;
+            tc::fence_after_sync();
+            issue_mma1(j);
+          }
+          // tile (j - 1) % NX is free once batch j - 1's last MMA (K: projection, V: rotation) completed
+          const long long jp = j - 1;
+          if (jp >= 0 && jp + NX < nj) {
+            ok = QJL ? tc::mbar_wait(bar_p + (jp & 1), (uint32_t)(jp >> 1) & 1u)
+                     : tc::mbar_wait(bar_y + (jp & 1), (uint32_t)(jp >> 1) & 1u);
+            if (ok) issue_tma(jp + NX);
+          }
         }
-        if (j == 0) continue;
-        const long long jp = j - 1;
-        if constexpr (QJL) {
-          // projection of batch jp: its R is stored, and P[jp & 1] (batch jp - 2) was read
+      } else {
+        // issuer B (turbo K): projections, once R of the batch is stored and P[jp & 1] (batch jp - 2) was read
+        for (long long jp = 0; ok && jp < nj; ++jp) {
           ok = tc::mbar_wait(rready, (uint32_t)jp & 1u);
           if (ok && jp >= 2) ok = tc::mbar_wait(pfree + (jp & 1), (uint32_t)((jp - 2) >> 1) & 1u);
           if (!ok) break;
           tc::fence_after_sync();
           issue_mma2(jp);
-          // tile jp % NX (R_hi of batch jp) is free once its projection completed
-          if (jp + NX < nj) {
-            ok = tc::mbar_wait(bar_p + (jp & 1), (uint32_t)(jp >> 1) & 1u);
-            if (ok) issue_tma(jp + NX);
-          }
-        } else {
-          // tile jp % NX is free once the rotation of batch jp completed
-          if (jp + NX < nj) {
-            ok = tc::mbar_wait(bar_y + (jp & 1), (uint32_t)(jp >> 1) & 1u);
-            if (ok) issue_tma(jp + NX);
-          }
         }
       }
       if (!ok) {
         failed = true;
-        // bounded waits for whatever is still in flight
+        // bounded waits for whatever this issuer still has in flight
         for (long long jj = mma1_done; jj < next_tma; ++jj)
           tc::mbar_wait(full_x + (int)(jj % NX), (uint32_t)(jj / NX) & 1u);
         if (mma1_done > 0) tc::mbar_wait(bar_y + ((mma1_done - 1) & 1), (uint32_t)((mma1_done - 1) >> 1) & 1u);
-        if (QJL && mma2_done > 0) tc::mbar_wait(bar_p + ((mma2_done - 1) & 1), (uint32_t)((mma2_done - 1) >> 1) & 1u);
+        if (mma2_done > 0) tc::mbar_wait(bar_p + ((mma2_done - 1) & 1), (uint32_t)((mma2_done - 1) >> 1) & 1u);
       }
     }
   } else {
@@ -924,6 +984,9 @@ __global__ void __launch_bounds__(etc::THREADS, 1)
     float bnd[7];
 #pragma unroll
     for (int k = 0; k < 7; ++k) bnd[k] = k < (1 << B) - 1 ? a.tab.boundaries[(B - 1) * 7 + k] : 0.f;
+    float cst[7];
+    const bool fma_idx = step_constants<B>(bnd, cst);  // the same on every thread
+    constexpr int CPC = 8 * W <= 24 ? 8 : 4;           // codes per float-accumulated chunk
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     uint32_t w_prev[W] = {};
     long long vid_prev = -1;
@@ -972,20 +1035,42 @@ __global__ void __launch_bounds__(etc::THREADS, 1)
         }
         unsigned char* rh = smem + L::x0 + (int)(j % NX) * kOp;  // the rotation consumed X: R_hi goes there
         float rr = 0.f;
+        const float F = f * 0x1p100f, FR = f * kRScale;
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {
           uint32_t hi[4], lo[4];
+          if (fma_idx) {
+            float acc[8 / CPC] = {};
 #pragma unroll
-          for (int e2 = 0; e2 < 8; e2 += 2) {
-            const int e = 8 * c8 + e2;
-            const float u0 = __uint_as_float(t[e]) * f, u1 = __uint_as_float(t[e + 1]) * f;
-            const uint32_t i0 = lloyd_index<B>(u0, bnd), i1 = lloyd_index<B>(u1, bnd);
-            const float r0 = fmaf(u0, kRScale, -cb_s[i0]), r1 = fmaf(u1, kRScale, -cb_s[i1]);  // 2^14 (u - c)
-            rr = fmaf(r0, r0, rr);
-            rr = fmaf(r1, r1, rr);
-            put_code<W>(w, e, i0);
-            put_code<W>(w, e + 1, i1);
-            split_pair(make_float2(r0, r1), hi[e2 / 2], lo[e2 / 2]);
+            for (int e2 = 0; e2 < 8; e2 += 2) {
+              float r2[2];
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int ec = e2 + hh;
+                const float yv = __uint_as_float(t[8 * c8 + ec]);
+                const float idx = step_index<B>(yv, F, cst);
+                const uint32_t ii = __float_as_uint(idx + 0x1p23f) & 7u;  // the integer index
+                r2[hh] = fmaf(yv, FR, -cb_s[ii]);                            // 2^14 (u - c)
+                rr = fmaf(r2[hh], r2[hh], rr);
+                acc[ec / CPC] = fmaf(idx, (float)(1u << (W * (ec % CPC))), acc[ec / CPC]);
+              }
+              split_pair(make_float2(r2[0], r2[1]), hi[e2 / 2], lo[e2 / 2]);
+            }
+#pragma unroll
+            for (int c = 0; c < 8 / CPC; ++c) or_bits<W>(w, W * (8 * c8 + CPC * c), W * CPC, (uint32_t)acc[c]);
+          } else {
+#pragma unroll
+            for (int e2 = 0; e2 < 8; e2 += 2) {
+              const int e = 8 * c8 + e2;
+              const float u0 = __uint_as_float(t[e]) * f, u1 = __uint_as_float(t[e + 1]) * f;
+              const uint32_t i0 = lloyd_index<B>(u0, bnd), i1 = lloyd_index<B>(u1, bnd);
+              const float r0 = fmaf(u0, kRScale, -cb_s[i0]), r1 = fmaf(u1, kRScale, -cb_s[i1]);  // 2^14 (u - c)
+              rr = fmaf(r0, r0, rr);
+              rr = fmaf(r1, r1, rr);
+              put_code<W>(w, e, i0);
+              put_code<W>(w, e + 1, i1);
+              split_pair(make_float2(r0, r1), hi[e2 / 2], lo[e2 / 2]);
+            }
           }
           const int off = swz<NV>(v, 32 * cg + 8 * c8);
           *reinterpret_cast<uint4*>(rh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -1014,8 +1099,20 @@ __global__ void __launch_bounds__(etc::THREADS, 1)
         vid_prev = vid;
         n_prev = n;
       } else {
+        if (fma_idx) {
+          const float F = f * 0x1p100f;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) put_code<W>(w, e, lloyd_index<B>(__uint_as_float(t[e]) * f, bnd));
+          for (int c = 0; c < 32 / CPC; ++c) {
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < CPC; ++e)
+              acc = fmaf(step_index<B>(__uint_as_float(t[CPC * c + e]), F, cst), (float)(1u << (W * e)), acc);
+            or_bits<W>(w, W * CPC * c, W * CPC, (uint32_t)acc);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) put_code<W>(w, e, lloyd_index<B>(__uint_as_float(t[e]) * f, bnd));
+        }
         if (vid >= 0) {
           if (cg == 0) *reinterpret_cast<__half*>(V.header + vid * V.hdr_bytes) = __float2half_rn(n);
           store_words<W>(reinterpret_cast<uint32_t*>(V.payload + vid * V.pay_bytes) + W * cg, w);
@@ -1053,7 +1150,7 @@ __global__ void __launch_bounds__(etc::THREADS, 1)
   if (failed) atomicOr(a.tab.status, kFlagTimeout);
   tc::fence_before_sync();
   __syncthreads();
-  if (issuer) tc::tmem_dealloc(tmem, kCols);
+  if (warp == SIMT_WARPS) tc::tmem_dealloc(tmem, kCols);
 }
 
 // cuTensorMapEncodeTiled from the driver (no link-time dependency on it); null if unavailable.
@@ -1103,7 +1200,7 @@ bool launch_tc(const EncArgs& a, int sm_count, cudaStream_t s, cudaError_t* err)
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess) {
     const long long grid = sh.n_batches < sm_count ? sh.n_batches : sm_count;  // one CTA per SM
-    kern<<<(unsigned)grid, THREADS, smem, s>>>(a, tmap, sh);
+    kern<<<(unsigned)grid, kThreads<QJL>, smem, s>>>(a, tmap, sh);
     e = cudaGetLastError();
   }
   *err = e;
