@@ -92,12 +92,12 @@ def source_hash(paths):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_srcs):
-    """Per-launch DRAM bytes of the decode call from the committed ncu summary, or None
-    when the kernel sources (attention kernel and its launch plan) changed since the
-    counters were taken."""
+def profiled_traffic(kernel_srcs, record="decode_traffic.json"):
+    """DRAM bytes per call from a committed ncu summary under profiles/ (decode call:
+    decode_traffic.json; encode call: encode_traffic.json), or None when the kernel
+    sources changed since the counters were taken."""
     try:
-        with open(os.path.join(ROOT, "profiles", "decode_traffic.json")) as f:
+        with open(os.path.join(ROOT, "profiles", record)) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
@@ -421,7 +421,10 @@ def main():
                                                   for f in ("tq_decode_fast.cu", "tq_decode.cu")])},
         "roofline_encode": {"bound": "hbm", "achieved": round(encode_bytes(tq, wl) / t_enc / 1e9, 2), "peak": hbm,
                             "unit": "GB/s", "frac": round(encode_bytes(tq, wl) / t_enc / 1e9 / hbm, 4),
-                            "peak_source": f"{peak_src} hbm_gbs", "traffic": None,
+                            "peak_source": f"{peak_src} hbm_gbs",
+                            "traffic": profiled_traffic([os.path.join(ROOT, "kv_cache_quantization_turbo_gb300", "csrc", f)
+                                                         for f in ("tq_encode.cu", "tq_tc.cuh")],
+                                                        "encode_traffic.json"),
                             "kernel": f"encode call (K and V kernels) of the {wl.encode_chunk}-token chunk over all "
                                       f"{wl.n_layers} layers: fp16 input read, codes and headers written"},
         "e2e": {"value": round(weak_scaling_value(dbytes, world, t_e2e), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
