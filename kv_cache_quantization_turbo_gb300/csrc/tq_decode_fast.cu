@@ -5,15 +5,17 @@
 // split), combined afterwards.
 //
 // Per warp, tiles of 16 tokens:
-//   * scores on mma.sync m16n8k16 (f16 in, f32 accumulate), one product per
-//     group of 8 tokens: rows 0-7 hold the codebook part c[idx] of the 8
-//     tokens, rows 8-15 their QJL part (2 sigma - 1); column 2j holds q' and
-//     column 2j + 1 holds S q' of one query head, so the (row < 8, column 2j)
-//     and (row >= 8, column 2j + 1) entries are the two inner products the
-//     score needs (the other two are not used).  Both parts of two coordinates
-//     come from one 8-byte lookup, indexed by one payload byte (index + sign
-//     nibbles), in a 256-entry table in shared memory; two lookups fill one
-//     A fragment as it stands.  The table is replicated per lane (entry stride
+//   * scores on mma.sync m16n8k16 (f16 in, f32 accumulate), two products per
+//     tile and k step, rows = the 16 tokens: one of the codebook parts c[idx]
+//     against q', one of the QJL parts (2 sigma - 1) against S q'.  Both parts
+//     of two coordinates of one token come from one 8-byte lookup, indexed by
+//     one payload byte (index + sign nibbles), in a 256-entry table in shared
+//     memory: its first word goes to the codebook product's A fragment, its
+//     second to the QJL product's.  The contraction index is permuted so that
+//     thread t's k slots are coordinates of its own 32-coordinate block of
+//     tokens g and g + 8 (the query fragments follow the same permutation), so
+//     four lookups fill the two A fragments as they stand and every output of
+//     both products is used.  The table is replicated per lane (entry stride
 //     256 B, lane offset 8 B) so the 32 lookups of a warp never collide, and
 //     it starts on a 64 KB boundary of the shared window, so one prmt of the
 //     payload word with (table base | lane << 3) is the whole address.
@@ -31,13 +33,13 @@
 //     fragment layout of a contraction over tokens.  The k slots of that
 //     contraction hold the tokens in the order 0, 8, 1, 9, ..., so each thread
 //     stores its two tokens' weights of one column as one 32-bit word.
-// Query heads: each score product runs over two blocks of 8 columns on the
-// same A fragments.  With up to 4 query heads per KV head, the blocks hold the
-// high and the low fp16 parts of q' and S q' (about 21 significant bits), and
-// in the V product column 2t holds head t's weights as the high part and
-// column 2t + 1 as the low part; thread (g, t) owns head t.  With 5 to 8
-// heads, the blocks hold heads 0-3 and 4-7 in plain fp16, columns 2t and
-// 2t + 1 of the V product are heads t and t + 4, and thread (g, t) owns both.
+// Query heads: the 8 columns of a score product.  With up to 4 query heads per
+// KV head, column 2h holds the high and column 2h + 1 the low fp16 part of
+// head h's q' (or S q'), about 21 significant bits, and in the V product column
+// 2t holds head t's weights as the high part and column 2t + 1 as the low part;
+// thread (g, t) owns head t.  With 5 to 8 heads, columns 2h and 2h + 1 hold
+// heads h and h + 4 in plain fp16 (score and V products alike), and thread
+// (g, t) owns both.
 //
 // The fp16 tables hold lambda * centroid, lambda chosen on the host so that
 // every entry is within ~2e-5 of its fp32 value; 1/lambda goes into the query
@@ -66,7 +68,11 @@ constexpr int kFThreads = kFWarps * 32;
 constexpr uint32_t kLutKBytes = 256 * 256;        // 256 entries x 32 lanes x 8 B
 constexpr uint32_t kLutVBytes = 64 * 128;         // 64 entries x 32 lanes x 4 B
 constexpr uint32_t kPsBytes = kFWarps * 2 * 256;  // per warp two P' tiles [8 cols][16 tokens] f16
-constexpr int kFSmem = 2 * 65536;                 // room to put the K table on a 64 KB boundary
+constexpr int kQfBytes = 32 * 32 * 4;             // per warp: the query fragments, 32 words x 32 lanes
+// The K table on a 64 KB boundary, the V table and the P' tiles next to it all end below 128 KB
+// (the table starts below 64 KB, and the other two fit on one side of it); the query fragments
+// of the warps follow at 128 KB.
+constexpr int kFSmem = 2 * 65536 + kFWarps * kQfBytes;
 constexpr int kPrefetchTiles = 4;                 // L2 prefetch distance
 
 constexpr float kLog2e = 1.4426950408889634074f;
@@ -104,6 +110,11 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
+}
+
+// Query fragments of a work item (written once per item by the lane that reads them).
+__device__ __forceinline__ void sts64(uint32_t addr, uint32_t x, uint32_t y) {
+  asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(addr), "r"(x), "r"(y) : "memory");
 }
 
 // P' tile accesses (ordered by __syncwarp, hence volatile).
@@ -175,12 +186,11 @@ struct Cursor {
   bool ok;                                 // page in range
 };
 
-// HILO (up to 4 query heads per KV head): the two column blocks of the score product hold the
-// high and the low fp16 parts of the same heads, and so do the P' columns; otherwise (5 to 8
-// heads) they hold heads t and t + 4 in plain fp16.
+// HILO (up to 4 query heads per KV head): columns 2h and 2h + 1 of the score products and of
+// P' hold the high and the low fp16 parts of head h; otherwise (5 to 8 heads) heads h and h + 4
+// in plain fp16.
 template <bool HILO>
 struct FastWarp {
-  static constexpr int NCB = 2;            // column blocks of the score product
   static constexpr int NH = HILO ? 1 : 2;  // query heads per thread: t (and t + 4)
 
   const DecodeLaunch& k;
@@ -193,7 +203,8 @@ struct FastWarp {
   // per work item
   int layer, b, kvh, ntiles, last_valid;
   Cursor c;
-  uint32_t bf[NCB][8][2];  // B fragments: column g = q' (g even) or S q' (g odd) of head g/2 (+ 4cb)
+  uint32_t qf;  // shared address of this lane's query fragments: step ch at qf + 256 ch (codebook
+                // product), qf + 2048 + 256 ch (QJL product), 8 bytes each
   float oacc[8][4];
   float m[NH], l[NH];      // per head slot: head t + 4 * slot
 
@@ -232,18 +243,19 @@ struct FastWarp {
     }
   }
 
-  __device__ __forceinline__ void load_k(KTile& K, int nvalid) {
+  // K of a tile whose lane addresses are kp, kh (this lane's rows g, g + 8)
+  __device__ __forceinline__ void load_k(KTile& K, const unsigned char* kp, const unsigned char* kh, int nvalid) {
     if (nvalid == 16) {
-      K.a = ld_stream_v4(c.kp, pol);
-      K.b = ld_stream_v4(c.kp + 8 * kKPay, pol);
-      K.ha = ld_stream_u32(c.kh, pol);
-      K.hb = ld_stream_u32(c.kh + 8 * kKHdr, pol);
+      K.a = ld_stream_v4(kp, pol);
+      K.b = ld_stream_v4(kp + 8 * kKPay, pol);
+      K.ha = ld_stream_u32(kh, pol);
+      K.hb = ld_stream_u32(kh + 8 * kKHdr, pol);
     } else {  // ragged last tile: rows at or beyond nvalid re-read row nvalid - 1 (their scores are masked)
       const int da = min(g, nvalid - 1) - g, db = min(g + 8, nvalid - 1) - g;
-      K.a = ld_stream_v4(c.kp + da * kKPay, pol);
-      K.b = ld_stream_v4(c.kp + db * kKPay, pol);
-      K.ha = ld_stream_u32(c.kh + da * kKHdr, pol);
-      K.hb = ld_stream_u32(c.kh + db * kKHdr, pol);
+      K.a = ld_stream_v4(kp + da * kKPay, pol);
+      K.b = ld_stream_v4(kp + db * kKPay, pol);
+      K.ha = ld_stream_u32(kh + da * kKHdr, pol);
+      K.hb = ld_stream_u32(kh + db * kKHdr, pol);
     }
   }
 
@@ -325,15 +337,10 @@ struct FastWarp {
       return;
     }
     KTile kc;
-    load_k(kc, nvalid);
+    load_k(kc, c.kp, c.kh, nvalid);
 
-    // ---- K: rows 0-7 = codebook part, rows 8-15 = QJL part of 8 tokens (tokens 0-7 in c0,
-    // 8-15 in c1); column 2j = q', 2j + 1 = S q' of one head ----
-    float c0[NCB][4], c1[NCB][4];
-#pragma unroll
-    for (int cb = 0; cb < NCB; ++cb)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) c0[cb][e] = c1[cb][e] = 0.f;
+    // ---- K: rows = tokens g / g + 8 of the thread; cc = codebook part . q', cs = QJL part . S q' ----
+    float cc[4] = {0.f, 0.f, 0.f, 0.f}, cs[4] = {0.f, 0.f, 0.f, 0.f};
     const uint32_t wa[4] = {kc.a.x, kc.a.y, kc.a.z, kc.a.w};
     const uint32_t wb[4] = {kc.b.x, kc.b.y, kc.b.z, kc.b.w};
 #pragma unroll
@@ -347,26 +354,24 @@ struct FastWarp {
         ea0 = lds64(lutk_addr<0>(xa, ylk)); ea1 = lds64(lutk_addr<1>(xa, ylk));
         eb0 = lds64(lutk_addr<0>(xb, ylk)); eb1 = lds64(lutk_addr<1>(xb, ylk));
       }
-#pragma unroll
-      for (int cb = 0; cb < NCB; ++cb) {
-        mma_16816(c0[cb], ea0.x, ea0.y, ea1.x, ea1.y, bf[cb][ch][0], bf[cb][ch][1]);
-        mma_16816(c1[cb], eb0.x, eb0.y, eb1.x, eb1.y, bf[cb][ch][0], bf[cb][ch][1]);
-      }
+      const uint2 fq = lds64(qf + 256 * ch), fs = lds64(qf + 2048 + 256 * ch);
+      mma_16816(cc, ea0.x, eb0.x, ea1.x, eb1.x, fq.x, fq.y);
+      mma_16816(cs, ea0.y, eb0.y, ea1.y, eb1.y, fs.x, fs.y);
     }
     VTile vc;
     load_v(vc, nvalid);
-    // thread (g, t): c[0] = codebook part . q' and c[3] = QJL part . S q' of the block's head t,
-    // token g (c0) / g + 8 (c1); with HILO the two blocks are the two parts of one head
+    // thread (g, t): entries 0, 1 = token g, columns 2t, 2t + 1; entries 2, 3 = token g + 8.
+    // HILO: the two columns are the two parts of head t; otherwise heads t and t + 4.
     const float2 hA = __half22float2(u32_as_h2(kc.ha)), hB = __half22float2(u32_as_h2(kc.hb));
     float s[NH][2];
     if (HILO) {
-      s[0][0] = fmaf(hA.x, c0[0][0] + c0[1][0], hA.y * (c0[0][3] + c0[1][3]));
-      s[0][1] = fmaf(hB.x, c1[0][0] + c1[1][0], hB.y * (c1[0][3] + c1[1][3]));
+      s[0][0] = fmaf(hA.x, cc[0] + cc[1], hA.y * (cs[0] + cs[1]));
+      s[0][1] = fmaf(hB.x, cc[2] + cc[3], hB.y * (cs[2] + cs[3]));
     } else {
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
-        s[h][0] = fmaf(hA.x, c0[h][0], hA.y * c0[h][3]);
-        s[h][1] = fmaf(hB.x, c1[h][0], hB.y * c1[h][3]);
+        s[h][0] = fmaf(hA.x, cc[h], hA.y * cs[h]);
+        s[h][1] = fmaf(hB.x, cc[2 + h], hB.y * cs[2 + h]);
       }
     }
     if (nvalid < 16) {
@@ -474,23 +479,25 @@ struct FastWarp {
     const int t1 = min(t0 + k.split_tokens, len);
     const long long row0 = (long long)lb * Hq + (long long)kvh * G;
 
-    // ---- B fragments: column g = q' (g even) or S q' (g odd) of head g/2 (HILO: block cb holds
-    // the high / low fp16 part) or of head g/2 + 4cb; log2 e / lambda or log2 e sqrt(pi/2) / d
-    // folded in ----
-#pragma unroll
-    for (int cb = 0; cb < NCB; ++cb) {
-      const int head = HILO ? (g >> 1) : 4 * cb + (g >> 1);
-      const bool lo = HILO && cb == 1;
-      const bool qjl = g & 1;
+    // ---- B fragments, column g: HILO: head g/2, the high (g even) or low (g odd) fp16 part;
+    // otherwise head g/2 + 4 (g & 1).  Codebook product: q' with log2 e / lambda folded in; QJL
+    // product: S q' with log2 e sqrt(pi/2) / d.  k slots 2t, 2t + 1 (+8) of step ch = coordinates
+    // 32t + 4ch + {0, 1} ({2, 3}), as the A fragments have them ----
+    {
+      const int head = HILO ? (g >> 1) : (g >> 1) + 4 * (g & 1);
+      const bool lo = HILO && (g & 1);
       const bool valid = head < G;
-      const float* qp = k.qprep + (row0 + (valid ? head : 0)) * 2 * kFD + (qjl ? kFD : 0) + 32 * t;
-      const float f = !valid ? 0.f : (qjl ? kLog2e * kSqrtHalfPi / (float)kFD : kLog2e / k.tab.f16_scale[2]);
+      const float* qp = k.qprep + (row0 + (valid ? head : 0)) * 2 * kFD + 32 * t;
+      const float fq = valid ? kLog2e / k.tab.f16_scale[2] : 0.f;
+      const float fs = valid ? kLog2e * kSqrtHalfPi / (float)kFD : 0.f;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
         const float4 v = *reinterpret_cast<const float4*>(qp + 4 * ch);
-        bf[cb][ch][0] = pack_part(v.x * f, v.y * f, lo);
-        bf[cb][ch][1] = pack_part(v.z * f, v.w * f, lo);
+        const float4 u = *reinterpret_cast<const float4*>(qp + kFD + 4 * ch);
+        sts64(qf + 256 * ch, pack_part(v.x * fq, v.y * fq, lo), pack_part(v.z * fq, v.w * fq, lo));
+        sts64(qf + 2048 + 256 * ch, pack_part(u.x * fs, u.y * fs, lo), pack_part(u.z * fs, u.w * fs, lo));
       }
+      __syncwarp();  // the lanes' own fragments only, but keep the stores ahead of the first read
     }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
@@ -605,6 +612,7 @@ __global__ void __launch_bounds__(kFThreads, 1) attend_fast_kernel(DecodeLaunch 
   w.psw1 = ps + 4 * ps_word(2 * w.t + 1, w.g);
   w.psr = ps + 4 * ps_word(w.g, w.t);
   w.vsh = (w.g & 1) ? 16u : 0u;
+  w.qf = sbase + 2 * 65536 + warp * (uint32_t)kQfBytes + lane * 8;
   asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(w.pol));
 
   const DecodeArgs& a = k.a;
