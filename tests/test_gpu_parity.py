@@ -80,6 +80,28 @@ def test_encode_scattered_slots_multi_layer(ctx128, fmt):
     assert not pay0.any() and not hdr0.any()  # untouched layer
 
 
+@pytest.mark.parametrize("H", [3, 6, 12])
+def test_encode_tensor_core_partial_batches_and_strides(ctx128, H):
+    """d = 128 (the tensor-core encoder): head counts that do not divide 128, so a batch holds
+    H * floor(128 / H) < 128 rows, a ragged token count, two layers, and K and V read in place from
+    one interleaved [layer][token][K | V][head][d] buffer (token stride 2 H d, layer stride 2 T H d)."""
+    d, T, L = 128, 173, 2
+    kv = torch.stack([torch.stack([W.kv_tensor(T, H, d, seed=40 + 10 * l + j, device="cuda", outliers_per_head=2)
+                                   for j in (0, 1)], dim=1) for l in range(L)])  # [L, T, 2, H, d]
+    assert kv.is_contiguous()
+    for fmt, j in (("turbo4", 0), ("turbo3_mse", 1)):
+        is_k = j == 0
+        view = tq.alloc_view(fmt, d, H, page_size=T, num_pages=1, n_layers=L)
+        x = kv[:, :, j]  # a strided view of the interleaved buffer
+        args = (view, x, None, None) if is_k else (None, None, view, x)
+        st = tq.tq_encode_kv(ctx128.h, *args, 0, L, T, T * 2 * H * d, 2 * H * d, None, 0, None)
+        assert st == tq.TQ_OK, tq.tq_status_string(st)
+        for l in range(L):
+            pay, hdr = C.read_vectors(view, layer=l)
+            enc = O.turbo_encode(x[l].cpu().numpy(), fmt, ctx128.signs, ctx128.S)
+            C.check_turbo_codes(fmt, d, pay[0].transpose(1, 0, 2), hdr[0].transpose(1, 0, 2), enc)
+
+
 def test_encode_zero_and_single_vectors(ctx128):
     """Zero vectors (every rotated coordinate exactly 0: the tie rule decides, identically on
     both sides), a basis vector, and the all-ones vector, whose rotated coordinates are
