@@ -53,7 +53,7 @@ using DecodeKernelArgs = DecodeLaunch;
 // ---------------------------------------------------------------------------
 // 1. query prologue
 // ---------------------------------------------------------------------------
-constexpr int kRowsPerBlock = 1;  // query rows (one warp each) per CTA of the prologue and the combine (1 timed fastest)
+constexpr int kRowsPerBlock = 1;  // query rows (one warp each) per CTA of the prologue (1 timed fastest)
 
 template <int D>
 __global__ void __launch_bounds__(32 * kRowsPerBlock) qprep_kernel(DecodeKernelArgs ka) {
@@ -296,17 +296,23 @@ __global__ void __launch_bounds__(32) attend_generic_kernel(DecodeKernelArgs ka)
 // ---------------------------------------------------------------------------
 // 3. combine
 // ---------------------------------------------------------------------------
+// One CTA of kCombineWarps warps per query row: warp w merges the splits w, w + kCombineWarps, ...
+// (several splits' partials in flight per warp), the warps' sums meet in shared memory, and warp 0
+// finishes the row.
+constexpr int kCombineWarps = 4;
 template <int D>
-__global__ void __launch_bounds__(32 * kRowsPerBlock) combine_kernel(DecodeKernelArgs ka) {
+__global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(DecodeKernelArgs ka) {
   constexpr int E = D / 32;
+  __shared__ float xs[kCombineWarps][D];
+  __shared__ float ls[kCombineWarps];
   const DecodeArgs& a = ka.a;
-  const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const long long row = blockIdx.x;
   const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
-  if (row >= rows) return;  // warp-uniform
+  if (row >= rows) return;  // block-uniform
   const int ns = ka.n_splits;
   const float* part = ka.partial + row * ns * (D + 4);
-  // split maxima, lane-parallel
+  // split maxima, lane-parallel (every warp)
   float M = -INFINITY;
   for (int s = lane; s < ns; s += 32) M = fmaxf(M, part[s * (D + 4)]);
   M = warp_max(M);
@@ -315,26 +321,30 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) combine_kernel(DecodeKerne
   for (int e = 0; e < E; ++e) x[e] = 0.f;
   float L = 0.f;
   if (M != -INFINITY) {
-    for (int s0 = 0; s0 < ns; s0 += 32) {
-      // weight of split s0 + lane (empty splits: m = -inf, weight 0)
-      float w = 0.f;
-      if (s0 + lane < ns) {
-        const float ms = part[(s0 + lane) * (D + 4)];
-        if (ms != -INFINITY) {
-          w = expf(ms - M);
-          L = fmaf(part[(s0 + lane) * (D + 4) + 1], w, L);
-        }
-      }
-      const int n = ns - s0 < 32 ? ns - s0 : 32;
 #pragma unroll 4
-      for (int j = 0; j < n; ++j) {
-        const float wj = __shfl_sync(kFull, w, j);
-        const float* p = part + (s0 + j) * (D + 4) + 4 + E * lane;
-#pragma unroll
-        for (int e = 0; e < E; ++e) x[e] = fmaf(p[e], wj, x[e]);
+    for (int s = w; s < ns; s += kCombineWarps) {
+      const float* p = part + s * (D + 4);
+      const float ms = p[0];  // empty splits: m = -inf, weight 0
+      float wj = 0.f;
+      if (ms != -INFINITY) {
+        wj = expf(ms - M);
+        L = fmaf(p[1], wj, L);
       }
+#pragma unroll
+      for (int e = 0; e < E; ++e) x[e] = fmaf(p[4 + E * lane + e], wj, x[e]);
     }
-    L = warp_sum(L);
+  }
+  if (lane == 0) ls[w] = L;
+#pragma unroll
+  for (int e = 0; e < E; ++e) xs[w][E * lane + e] = x[e];
+  __syncthreads();
+  if (w != 0) return;
+  L = ls[0];
+#pragma unroll
+  for (int q = 1; q < kCombineWarps; ++q) {
+    L += ls[q];
+#pragma unroll
+    for (int e = 0; e < E; ++e) x[e] += xs[q][E * lane + e];
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
@@ -358,7 +368,7 @@ cudaError_t launch_decode_dim(const DecodeKernelArgs& ka, int sm_count, cudaStre
   if (attend_fast_supported(ka)) {
     const cudaError_t e = launch_attend_fast(ka, sm_count, s);
     if (e != cudaSuccess) return e;
-    combine_kernel<D><<<blocks, 32 * kRowsPerBlock, 0, s>>>(ka);
+    combine_kernel<D><<<(unsigned)rows, 32 * kCombineWarps, 0, s>>>(ka);
     return cudaGetLastError();
   }
   dim3 grid(ka.n_splits, a.k.H, a.n_layers * a.batch);
@@ -369,7 +379,7 @@ cudaError_t launch_decode_dim(const DecodeKernelArgs& ka, int sm_count, cudaStre
     if (e != cudaSuccess) return e;
   }
   attend_generic_kernel<D><<<grid, 32, smem, s>>>(ka);
-  combine_kernel<D><<<blocks, 32 * kRowsPerBlock, 0, s>>>(ka);
+  combine_kernel<D><<<(unsigned)rows, 32 * kCombineWarps, 0, s>>>(ka);
   return cudaGetLastError();
 }
 
