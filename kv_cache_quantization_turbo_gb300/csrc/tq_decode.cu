@@ -53,55 +53,57 @@ using DecodeKernelArgs = DecodeLaunch;
 // ---------------------------------------------------------------------------
 // 1. query prologue
 // ---------------------------------------------------------------------------
-constexpr int kRowsPerBlock = 1;  // query rows (one warp each) per CTA of the prologue (1 timed fastest)
-
+// One CTA of D threads per query row: warp 0 rotates q (signs, WHT, softmax scale) into shared
+// memory, then thread j forms (S q')_j = sum_i S_T[i][j] q'_i with four partial sums (coalesced rows
+// of S_T, several products in flight).
 template <int D>
-__global__ void __launch_bounds__(32 * kRowsPerBlock) qprep_kernel(DecodeKernelArgs ka) {
+__global__ void __launch_bounds__(D) qprep_kernel(DecodeKernelArgs ka) {
   constexpr int E = D / 32;
   const DecodeArgs& a = ka.a;
-  const int lane = threadIdx.x & 31, wq = threadIdx.x >> 5;
-  const long long row = (long long)blockIdx.x * kRowsPerBlock + wq;  // (layer, batch, q head)
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const long long row = blockIdx.x;  // (layer, batch, q head)
   const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
-  if (row == 0 && lane == 0) *ka.counter = 0u;  // work counter of the attention kernel that follows
-  if (row >= rows) return;  // warp-uniform
-  __shared__ float q_s[kRowsPerBlock][D];
-  float x[E];
-  if (a.q_is_fp16) {
-    const __half* q = static_cast<const __half*>(a.q) + row * D;
-#pragma unroll
-    for (int e = 0; e < E; ++e) x[e] = __half2float(q[E * lane + e]);
-  } else {
-    const float* q = static_cast<const float*>(a.q) + row * D;
-#pragma unroll
-    for (int e = 0; e < E; ++e) x[e] = q[E * lane + e];
-  }
+  if (row == 0 && threadIdx.x == 0) *ka.counter = 0u;  // work counter of the attention kernel that follows
+  if (row >= rows) return;  // block-uniform
+  __shared__ float q_s[D];
   float* dst = ka.qprep + row * 2 * D;
-  if (a.k.format == TQ_FMT_Q8_0) {
+  const bool q8 = a.k.format == TQ_FMT_Q8_0;  // q8_0 K scores the unrotated q, and needs no S q
+  if (w == 0) {
+    float x[E];
+    if (a.q_is_fp16) {
+      const __half* q = static_cast<const __half*>(a.q) + row * D;
 #pragma unroll
-    for (int e = 0; e < E; ++e) dst[E * lane + e] = x[e] * a.softmax_scale;
-    return;
+      for (int e = 0; e < E; ++e) x[e] = __half2float(q[E * lane + e]);
+    } else {
+      const float* q = static_cast<const float*>(a.q) + row * D;
+#pragma unroll
+      for (int e = 0; e < E; ++e) x[e] = q[E * lane + e];
+    }
+    if (!q8) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) x[e] *= (float)ka.tab.signs[E * lane + e];
+      warp_wht<D>(x, lane);
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      x[e] *= a.softmax_scale;
+      q_s[E * lane + e] = x[e];
+      dst[E * lane + e] = x[e];
+    }
   }
-#pragma unroll
-  for (int e = 0; e < E; ++e) x[e] *= (float)ka.tab.signs[E * lane + e];
-  warp_wht<D>(x, lane);
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    x[e] *= a.softmax_scale;
-    q_s[wq][E * lane + e] = x[e];
-    dst[E * lane + e] = x[e];
+  if (q8) return;  // block-uniform
+  __syncthreads();
+  const int j = threadIdx.x;
+  const float* st = ka.tab.S_T + j;
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll 4
+  for (int i = 0; i < D; i += 4) {
+    s0 = fmaf(__ldg(st + (i + 0) * D), q_s[i + 0], s0);
+    s1 = fmaf(__ldg(st + (i + 1) * D), q_s[i + 1], s1);
+    s2 = fmaf(__ldg(st + (i + 2) * D), q_s[i + 2], s2);
+    s3 = fmaf(__ldg(st + (i + 3) * D), q_s[i + 3], s3);
   }
-  __syncwarp();
-  float sq[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) sq[e] = 0.f;
-#pragma unroll 8
-  for (int i = 0; i < D; ++i) {
-    const float qi = q_s[wq][i];
-#pragma unroll
-    for (int e = 0; e < E; ++e) sq[e] = fmaf(__ldg(ka.tab.S_T + i * D + E * lane + e), qi, sq[e]);
-  }
-#pragma unroll
-  for (int e = 0; e < E; ++e) dst[D + E * lane + e] = sq[e];
+  dst[D + j] = (s0 + s1) + (s2 + s3);
 }
 
 // ---------------------------------------------------------------------------
@@ -363,8 +365,7 @@ template <int D>
 cudaError_t launch_decode_dim(const DecodeKernelArgs& ka, int sm_count, cudaStream_t s) {
   const DecodeArgs& a = ka.a;
   const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
-  const unsigned blocks = (unsigned)((rows + kRowsPerBlock - 1) / kRowsPerBlock);
-  qprep_kernel<D><<<blocks, 32 * kRowsPerBlock, 0, s>>>(ka);
+  qprep_kernel<D><<<(unsigned)rows, D, 0, s>>>(ka);
   if (attend_fast_supported(ka)) {
     const cudaError_t e = launch_attend_fast(ka, sm_count, s);
     if (e != cudaSuccess) return e;
