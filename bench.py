@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target seconds of timed oracle work")
     p.add_argument("--layers", type=int, default=0,
                    help="use only this many layers (small cases for profiler captures; 0 = all)")
+    p.add_argument("--workload", default=WORKLOAD, choices=["llama3-8b-32k-turbo4", "llama-70b-128k-turbo4"],
+                   help="contiguous batch-1 turbo4 workloads; the default is the benchmark's")
     return p.parse_args()
 
 
@@ -168,6 +170,8 @@ def build_workload(tq, W, torch, dev, layers=0):
     wl = W.WORKLOADS[WORKLOAD]
     if layers:
         wl = dataclasses.replace(wl, n_layers=layers)
+    if not wl.encode_chunk:  # decode-only recipes: the step still encodes a 4096-token chunk per layer
+        wl = dataclasses.replace(wl, encode_chunk=4096)
     L, H, d, T, Hq, chunk = wl.n_layers, wl.n_kv_heads, wl.head_dim, wl.ctx, wl.n_q_heads, wl.encode_chunk
     signs, S = W.wht_signs(wl.wht_seed, d), W.qjl_matrix(wl.qjl_seed, d)
     ctx = tq.tq_context_create(d, wl.wht_seed, wl.qjl_seed, signs, S)
@@ -300,7 +304,9 @@ def run_reference(args, rank):
 # ---------------------------------------------------------------------------
 
 def main():
+    global WORKLOAD
     args = parse()
+    WORKLOAD = args.workload
     rank, local_rank, world = dist_env()
     if args.impl == "reference":
         run_reference(args, rank)
