@@ -365,6 +365,7 @@ def main():
     # step i + 1 are copied on a second stream while step i encodes and decodes (two device buffer
     # sets).  The timed region holds exactly K input copies, K encode + decode steps and K result
     # reads: it starts before the first copy and ends after the last read.
+    out_ref = w["out"].cpu()  # the result of the last device-timed step
     k_host = w["k_chunk"].cpu().pin_memory()
     v_host = w["v_chunk"].cpu().pin_memory()
     q_host = w["q"].cpu().pin_memory()
@@ -411,6 +412,9 @@ def main():
     e1 = torch.cuda.Event(enable_timing=True)
     e1.record(stream)
     barrier()
+    # the pipelined steps reproduce the device-resident result bit for bit (same inputs; every split
+    # is owned by one warp and the combine merges in a fixed order)
+    assert torch.equal(out_host, out_ref), "end-to-end output differs from the device-timed output"
     t_e2e = e0.elapsed_time(e1) / e2e_steps / 1e3
     t_e2e = reduce_max([t_e2e], dev)[0]
     ok, flags = tq.tq_get_status(w["ctx"])
