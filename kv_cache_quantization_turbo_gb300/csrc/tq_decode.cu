@@ -361,13 +361,51 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(DecodeKerne
   for (int e = 0; e < E; ++e) dst[E * lane + e] = x[e];
 }
 
+// K and V code widths for the tensor-core kernels (q8_0 = 0; turbo K = index bits + 1; turbo-MSE
+// V = index bits), or -1 for a format they do not take.
+int mma_k_width(const DevView& v) {
+  if (v.format == TQ_FMT_Q8_0) return 0;
+  return format_is_turbo(v.format) && v.has_qjl ? v.code_bits : -1;
+}
+int mma_v_width(const DevView& v) {
+  if (v.format == TQ_FMT_Q8_0) return 0;
+  return format_is_turbo(v.format) && !v.has_qjl ? v.code_bits : -1;
+}
+
+// The format-parameterised tensor-core kernel takes this launch: up to 8 query heads per KV head,
+// pages of a multiple of 16 tokens (or a contiguous cache), an instantiated pair of code widths.
+bool attend_mma_supported(const DecodeKernelArgs& ka, int d) {
+  const DecodeArgs& a = ka.a;
+  if (ka.G < 1 || ka.G > 8 || ka.split_tokens % 16 != 0) return false;
+  if (a.block_table != nullptr && a.k.page_size % 16 != 0) return false;
+  const int wk = mma_k_width(a.k), wv = mma_v_width(a.v);
+  if (wk < 0 || wv < 0) return false;
+  switch (d) {
+    case 64: return mma_has_d64(wk, wv);
+    case 128: return mma_has_d128(wk, wv);
+    case 256: return mma_has_d256(wk, wv);
+  }
+  return false;
+}
+
+cudaError_t launch_attend_mma(const DecodeKernelArgs& ka, int d, int sm_count, cudaStream_t s) {
+  const int wk = mma_k_width(ka.a.k), wv = mma_v_width(ka.a.v);
+  switch (d) {
+    case 64: return mma_launch_d64(ka, wk, wv, sm_count, s);
+    case 128: return mma_launch_d128(ka, wk, wv, sm_count, s);
+    case 256: return mma_launch_d256(ka, wk, wv, sm_count, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
 template <int D>
 cudaError_t launch_decode_dim(const DecodeKernelArgs& ka, int sm_count, cudaStream_t s) {
   const DecodeArgs& a = ka.a;
   const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
   qprep_kernel<D><<<(unsigned)rows, D, 0, s>>>(ka);
-  if (attend_fast_supported(ka)) {
-    const cudaError_t e = launch_attend_fast(ka, sm_count, s);
+  if (attend_fast_supported(ka) || attend_mma_supported(ka, D)) {
+    const cudaError_t e =
+        attend_fast_supported(ka) ? launch_attend_fast(ka, sm_count, s) : launch_attend_mma(ka, D, sm_count, s);
     if (e != cudaSuccess) return e;
     combine_kernel<D><<<(unsigned)rows, 32 * kCombineWarps, 0, s>>>(ka);
     return cudaGetLastError();

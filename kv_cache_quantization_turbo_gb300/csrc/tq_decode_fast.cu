@@ -1,6 +1,8 @@
 // Split-K decode attention on tensor cores for turbo4 K (3-bit index + QJL
 // sign per coordinate, stored as nibbles) and turbo4_mse V (3-bit index),
-// head_dim 128, up to 8 query heads per KV head.  Same contract as the
+// head_dim 128, up to 4 query heads per KV head (5 to 8 take the
+// format-parameterised kernel of tq_decode_mma.cuh, whose two products per part
+// keep the query columns split into high and low parts).  Same contract as the
 // generic kernel in tq_decode.cu: one partial (m, l, acc) per (query row,
 // split), combined afterwards.
 //
@@ -33,13 +35,10 @@
 //     fragment layout of a contraction over tokens.  The k slots of that
 //     contraction hold the tokens in the order 0, 8, 1, 9, ..., so each thread
 //     stores its two tokens' weights of one column as one 32-bit word.
-// Query heads: the 8 columns of a score product.  With up to 4 query heads per
-// KV head, column 2h holds the high and column 2h + 1 the low fp16 part of
-// head h's q' (or S q'), about 21 significant bits, and in the V product column
-// 2t holds head t's weights as the high part and column 2t + 1 as the low part;
-// thread (g, t) owns head t.  With 5 to 8 heads, columns 2h and 2h + 1 hold
-// heads h and h + 4 in plain fp16 (score and V products alike), and thread
-// (g, t) owns both.
+// Query heads: the 8 columns of a score product.  Column 2h holds the high and
+// column 2h + 1 the low fp16 part of head h's q' (or S q'), about 21
+// significant bits, and in the V product column 2t holds head t's weights as
+// the high part and column 2t + 1 as the low part; thread (g, t) owns head t.
 //
 // The fp16 tables hold lambda * centroid, lambda chosen on the host so that
 // every entry is within ~2e-5 of its fp32 value; 1/lambda goes into the query
@@ -57,9 +56,12 @@
 #include <cuda_fp16.h>
 
 #include "tq_device.cuh"
+#include "tq_warp_mma.cuh"
 
 namespace tq {
 namespace {
+
+using namespace wm;
 
 constexpr int kFD = 128;
 constexpr int kFWarps = 16;
@@ -75,80 +77,8 @@ constexpr int kQfBytes = 32 * 32 * 4;             // per warp: the query fragmen
 constexpr int kFSmem = 2 * 65536 + kFWarps * kQfBytes;
 constexpr int kPrefetchTiles = 4;                 // L2 prefetch distance
 
-constexpr float kLog2e = 1.4426950408889634074f;
-constexpr float kLn2 = 0.6931471805599453094f;
-constexpr float kLazyMax = 8.0f;
-
 // Bytes per token of the two formats (d = 128).
 constexpr int kKPay = 64, kKHdr = 4, kVPay = 48, kVHdr = 2;
-
-__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
-__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
-
-__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                          uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// 2^x for x <= 8 (scores never pass the reference by more); -inf -> 0
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Table reads (the tables do not change after the prologue of the kernel).
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-  uint2 v;
-  asm("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
-// Query fragments of a work item (written once per item by the lane that reads them).
-__device__ __forceinline__ void sts64(uint32_t addr, uint32_t x, uint32_t y) {
-  asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(addr), "r"(x), "r"(y) : "memory");
-}
-
-// P' tile accesses (ordered by __syncwarp, hence volatile).
-__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint2 lds64_v(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
-  return v;
-}
-
-// Streaming cache loads: no L1 allocation, evict-first in L2.
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p, uint64_t pol) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p), "l"(pol));
-  return v;
-}
-__device__ __forceinline__ uint32_t ld_stream_u32(const void* p, uint64_t pol) {
-  uint32_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(pol));
-  return v;
-}
-__device__ __forceinline__ uint32_t ld_stream_u16(const void* p, uint64_t pol) {
-  unsigned short v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u16 %0, [%1], %2;" : "=h"(v) : "l"(p), "l"(pol));
-  return v;
-}
-// Bulk request of [p, p + bytes) into L2; p and bytes are multiples of 16.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 
 // Address of the K table entry for byte kk of word x: table base | x.byte[kk] << 8 | lane << 3.
 template <int KK>
@@ -161,13 +91,6 @@ template <int S>
 __device__ __forceinline__ uint32_t lutv_addr(uint32_t w, uint32_t ylv) {
   const uint32_t x = S >= 7 ? (w >> (S - 7)) : (w << (7 - S));
   return (x & 0x1F80u) | ylv;
-}
-
-// P' word (column col, token pair k2 = tokens k2 and k2 + 8) in a warp's P' tile:
-// the reader's two words (k2 = t, t + 4) are adjacent, and both the writers'
-// and the reader's accesses fall on distinct banks.
-__device__ __forceinline__ int ps_word(int col, int k2) {
-  return (col * 8 + (k2 & 3) * 2 + (k2 >> 2)) ^ ((col & 4) << 1);
 }
 
 struct KTile {
@@ -186,12 +109,9 @@ struct Cursor {
   bool ok;                                 // page in range
 };
 
-// HILO (up to 4 query heads per KV head): columns 2h and 2h + 1 of the score products and of
-// P' hold the high and the low fp16 parts of head h; otherwise (5 to 8 heads) heads h and h + 4
-// in plain fp16.
-template <bool HILO>
+// Columns 2h and 2h + 1 of the score products and of P' hold the high and the low fp16 parts of
+// query head h (up to 4 heads per KV head); thread (g, t) owns head t.
 struct FastWarp {
-  static constexpr int NH = HILO ? 1 : 2;  // query heads per thread: t (and t + 4)
 
   const DecodeLaunch& k;
   int lane, g, t;
@@ -206,7 +126,7 @@ struct FastWarp {
   uint32_t qf;  // shared address of this lane's query fragments: step ch at qf + 256 ch (codebook
                 // product), qf + 2048 + 256 ch (QJL product), 8 bytes each
   float oacc[8][4];
-  float m[NH], l[NH];      // per head slot: head t + 4 * slot
+  float m, l;  // running reference and sum of head t
 
   __device__ __forceinline__ FastWarp(const DecodeLaunch& k_) : k(k_) {}
 
@@ -302,30 +222,19 @@ struct FastWarp {
   }
 
   // Raises the reference of every head whose new scores pass it by 2^8 (warp-uniform decision).
-  __device__ __forceinline__ void raise_reference(float (&mx)[NH]) {
-    bool need = false;
+  __device__ __forceinline__ void raise_reference(float mx) {
+    if (!__any_sync(kFull, mx > m + kLazyMax)) return;
 #pragma unroll
-    for (int h = 0; h < NH; ++h) need |= mx[h] > m[h] + kLazyMax;
-    if (!__any_sync(kFull, need)) return;
+    for (int o = 4; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    const float mn = fmaxf(m, mx);
+    const float al = ex2(m - mn);
+    l *= al;
 #pragma unroll
-    for (int h = 0; h < NH; ++h) {
+    for (int mt = 0; mt < 8; ++mt) {
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], o));
-      const float mn = fmaxf(m[h], mx[h]);
-      const float al = ex2(m[h] - mn);
-      l[h] *= al;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        if (HILO) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) oacc[mt][e] *= al;
-        } else {
-          oacc[mt][h] *= al;
-          oacc[mt][2 + h] *= al;
-        }
-      }
-      m[h] = mn;
+      for (int e = 0; e < 4; ++e) oacc[mt][e] *= al;
     }
+    m = mn;
   }
 
   // One tile at the cursor (the caller advances the cursor afterwards).
@@ -360,53 +269,26 @@ struct FastWarp {
     }
     VTile vc;
     load_v(vc, nvalid);
-    // thread (g, t): entries 0, 1 = token g, columns 2t, 2t + 1; entries 2, 3 = token g + 8.
-    // HILO: the two columns are the two parts of head t; otherwise heads t and t + 4.
+    // thread (g, t): entries 0, 1 = token g, columns 2t, 2t + 1 (the two parts of head t);
+    // entries 2, 3 = token g + 8.
     const float2 hA = __half22float2(u32_as_h2(kc.ha)), hB = __half22float2(u32_as_h2(kc.hb));
-    float s[NH][2];
-    if (HILO) {
-      s[0][0] = fmaf(hA.x, cc[0] + cc[1], hA.y * (cs[0] + cs[1]));
-      s[0][1] = fmaf(hB.x, cc[2] + cc[3], hB.y * (cs[2] + cs[3]));
-    } else {
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        s[h][0] = fmaf(hA.x, cc[h], hA.y * cs[h]);
-        s[h][1] = fmaf(hB.x, cc[2 + h], hB.y * cs[2 + h]);
-      }
-    }
+    float s0 = fmaf(hA.x, cc[0] + cc[1], hA.y * (cs[0] + cs[1]));
+    float s1 = fmaf(hB.x, cc[2] + cc[3], hB.y * (cs[2] + cs[3]));
     if (nvalid < 16) {
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        if (g >= nvalid) s[h][0] = -INFINITY;
-        if (g + 8 >= nvalid) s[h][1] = -INFINITY;
-      }
+      if (g >= nvalid) s0 = -INFINITY;
+      if (g + 8 >= nvalid) s1 = -INFINITY;
     }
 
     // ---- online softmax with a lazily raised reference (base 2) ----
-    {
-      float mx[NH];
-#pragma unroll
-      for (int h = 0; h < NH; ++h) mx[h] = fmaxf(s[h][0], s[h][1]);
-      raise_reference(mx);
-    }
-    float p[NH][2];
-#pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      p[h][0] = ex2(s[h][0] - m[h]);
-      p[h][1] = ex2(s[h][1] - m[h]);
-      l[h] += p[h][0] + p[h][1];
-    }
+    raise_reference(fmaxf(s0, s1));
+    float p0 = ex2(s0 - m), p1 = ex2(s1 - m);
+    l += p0 + p1;
     // ---- Sparse V: weights below the threshold are dropped; an all-dropped tile skips V ----
     if (k.a.skip_threshold > 0.f) {
       const float tau = k.a.skip_threshold;
-      bool any = false;
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        p[h][0] = p[h][0] >= tau ? p[h][0] : 0.f;
-        p[h][1] = p[h][1] >= tau ? p[h][1] : 0.f;
-        any |= (p[h][0] + p[h][1]) > 0.f;
-      }
-      if (!__any_sync(kFull, any)) {
+      p0 = p0 >= tau ? p0 : 0.f;
+      p1 = p1 >= tau ? p1 : 0.f;
+      if (!__any_sync(kFull, (p0 + p1) > 0.f)) {
         __syncwarp();
         return;
       }
@@ -415,15 +297,12 @@ struct FastWarp {
     // ---- P' = weight * V norm, one word per (column, token pair g / g + 8) ----
     const float2 nv = __half22float2(u32_as_h2(vc.nv));
     constexpr uint32_t kBuf = 256 * BUF;
-    if (HILO) {
-      const float w0 = p[0][0] * nv.x, w1 = p[0][1] * nv.y;
+    {
+      const float w0 = p0 * nv.x, w1 = p1 * nv.y;
       const __half2 hi = __floats2half2_rn(w0, w1);
       const float2 hf = __half22float2(hi);
       sts32(psw0 + kBuf, h2_as_u32(hi));
       sts32(psw1 + kBuf, h2_as_u32(__floats2half2_rn(w0 - hf.x, w1 - hf.y)));
-    } else {
-      sts32(psw0 + kBuf, h2_as_u32(__floats2half2_rn(p[0][0] * nv.x, p[0][1] * nv.y)));
-      sts32(psw1 + kBuf, h2_as_u32(__floats2half2_rn(p[NH - 1][0] * nv.x, p[NH - 1][1] * nv.y)));
     }
     __syncwarp();
     const uint2 bp = lds64_v(psr + kBuf);
@@ -479,13 +358,13 @@ struct FastWarp {
     const int t1 = min(t0 + k.split_tokens, len);
     const long long row0 = (long long)lb * Hq + (long long)kvh * G;
 
-    // ---- B fragments, column g: HILO: head g/2, the high (g even) or low (g odd) fp16 part;
-    // otherwise head g/2 + 4 (g & 1).  Codebook product: q' with log2 e / lambda folded in; QJL
+    // ---- B fragments, column g: head g/2, the high (g even) or low (g odd) fp16 part.
+    // Codebook product: q' with log2 e / lambda folded in; QJL
     // product: S q' with log2 e sqrt(pi/2) / d.  k slots 2t, 2t + 1 (+8) of step ch = coordinates
     // 32t + 4ch + {0, 1} ({2, 3}), as the A fragments have them ----
     {
-      const int head = HILO ? (g >> 1) : (g >> 1) + 4 * (g & 1);
-      const bool lo = HILO && (g & 1);
+      const int head = g >> 1;
+      const bool lo = g & 1;
       const bool valid = head < G;
       const float* qp = k.qprep + (row0 + (valid ? head : 0)) * 2 * kFD + 32 * t;
       const float fq = valid ? kLog2e / k.tab.f16_scale[2] : 0.f;
@@ -501,11 +380,8 @@ struct FastWarp {
     }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
-#pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.f;
-    }
+    m = -INFINITY;
+    l = 0.f;
 
     ntiles = t1 > t0 ? (t1 - t0 + 15) / 16 : 0;
     last_valid = t1 - t0 - 16 * (ntiles - 1);
@@ -525,35 +401,24 @@ struct FastWarp {
       }
     }
 
-    // ---- partial of this work item: (m, l, acc) per query head ----
+    // ---- partial of this work item: (m, l, acc) of head t ----
 #pragma unroll
-    for (int h = 0; h < NH; ++h) {
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) l[h] += __shfl_xor_sync(kFull, l[h], o);
-    }
-    const float inv_lam = 1.0f / k.tab.f16_scale[2];
-#pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      const int head = t + 4 * h;
-      if (head >= G) continue;
+    for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(kFull, l, o);
+    if (t < G) {
+      const float inv_lam = 1.0f / k.tab.f16_scale[2];
       float v[16];
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        if (HILO) {
-          v[2 * mt] = (oacc[mt][0] + oacc[mt][1]) * inv_lam;
-          v[2 * mt + 1] = (oacc[mt][2] + oacc[mt][3]) * inv_lam;
-        } else {
-          v[2 * mt] = oacc[mt][h] * inv_lam;
-          v[2 * mt + 1] = oacc[mt][2 + h] * inv_lam;
-        }
+        v[2 * mt] = (oacc[mt][0] + oacc[mt][1]) * inv_lam;
+        v[2 * mt + 1] = (oacc[mt][2] + oacc[mt][3]) * inv_lam;
       }
-      float* dst = k.partial + ((row0 + head) * k.n_splits + split) * (kFD + 4);
+      float* dst = k.partial + ((row0 + t) * k.n_splits + split) * (kFD + 4);
       float4* dv = reinterpret_cast<float4*>(dst + 4 + 16 * g);
 #pragma unroll
       for (int q = 0; q < 4; ++q) dv[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       if (g == 0) {
-        dst[0] = m[h] == -INFINITY ? -INFINITY : m[h] * kLn2;
-        dst[1] = l[h];
+        dst[0] = m == -INFINITY ? -INFINITY : m * kLn2;
+        dst[1] = l;
       }
     }
   }
@@ -567,7 +432,6 @@ struct FastWarp {
   }
 };
 
-template <bool HILO>
 __global__ void __launch_bounds__(kFThreads, 1) attend_fast_kernel(DecodeLaunch k) {
   extern __shared__ __align__(16) unsigned char sm[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -601,7 +465,7 @@ __global__ void __launch_bounds__(kFThreads, 1) attend_fast_kernel(DecodeLaunch 
   }
   __syncthreads();
 
-  FastWarp<HILO> w(k);
+  FastWarp w(k);
   w.lane = lane;
   w.g = lane >> 2;
   w.t = lane & 3;
@@ -632,7 +496,7 @@ __global__ void __launch_bounds__(kFThreads, 1) attend_fast_kernel(DecodeLaunch 
 bool attend_fast_supported(const DecodeLaunch& k) {
   const DecodeArgs& a = k.a;
   return a.k.d == kFD && a.k.format == TQ_FMT_TURBO4 && a.v.format == TQ_FMT_TURBO4_MSE && k.G >= 1 &&
-         k.G <= 8 && (a.block_table == nullptr || a.k.page_size % 16 == 0) && k.split_tokens % 16 == 0;
+         k.G <= 4 && (a.block_table == nullptr || a.k.page_size % 16 == 0) && k.split_tokens % 16 == 0;
 }
 
 cudaError_t launch_attend_fast(const DecodeLaunch& k, int sm_count, cudaStream_t s) {
@@ -641,15 +505,9 @@ cudaError_t launch_attend_fast(const DecodeLaunch& k, int sm_count, cudaStream_t
   long long grid = sm_count;  // one persistent CTA per SM
   if (items < grid * kFWarps) grid = (items + kFWarps - 1) / kFWarps;
   if (grid < 1) grid = 1;
-  if (k.G <= 4) {
-    cudaError_t e = cudaFuncSetAttribute(attend_fast_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
-    if (e != cudaSuccess) return e;
-    attend_fast_kernel<true><<<(unsigned)grid, kFThreads, kFSmem, s>>>(k);
-  } else {
-    cudaError_t e = cudaFuncSetAttribute(attend_fast_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
-    if (e != cudaSuccess) return e;
-    attend_fast_kernel<false><<<(unsigned)grid, kFThreads, kFSmem, s>>>(k);
-  }
+  const cudaError_t e = cudaFuncSetAttribute(attend_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
+  if (e != cudaSuccess) return e;
+  attend_fast_kernel<<<(unsigned)grid, kFThreads, kFSmem, s>>>(k);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,726 @@
+// Split-K decode attention on tensor cores, parameterised by the cache formats: turbo K with
+// W-bit codes (W - 1 index bits + the QJL sign bit; turbo2/3/4), turbo-MSE V with W-bit indices
+// (turbo2/3/4_mse), and q8_0 K or V, at head_dim 64, 128 or 256.  The turbo4 K + turbo4_mse V
+// pair at head_dim 128 with up to 4 query heads per KV head keeps its hand-specialised kernel
+// (tq_decode_fast.cu); this template takes everything else, with the same contract (one partial
+// (m, l, acc) per query row and split, combined afterwards), the same work items, 16-token tiles,
+// base-2 online softmax with a lazily raised reference, Sparse V skip and L2 prefetch.  What the
+// formats change is how a tile's codes reach the tensor-core fragments.
+//
+// Score products (mma.sync m16n8k16, rows = the 16 tokens of a tile, columns 2h / 2h + 1 = the
+// high / low fp16 part of query head h, about 21 significant bits of q'; with 5 to 8 query heads
+// per KV head a second product of each kind takes heads 4 .. 7).  Thread (g, t) holds rows g,
+// g + 8, the scores of heads t (and t + 4), and per k step the four k slots 2t, 2t + 1, 2t + 8,
+// 2t + 9:
+//   * turbo K: thread t owns the coordinates [t d/4, (t+1) d/4) of its tokens, a contiguous run
+//     of d W / 4 payload bits; step ch takes coordinates 4ch .. 4ch + 3 of the run.  The 2W bits
+//     of two coordinates index a table of 8-byte entries (replicated per lane, entry stride
+//     256 B): the f16 pair lambda c[idx] for the codebook product (against q') and the pair of
+//     +-1 for the QJL product (against S q').  score = n (c . q') + rnorm sqrt(pi/2)/d (sign . Sq').
+//   * q8_0 K: step ch covers 16 coordinates of the 32-block ch / 2, thread t holding bytes
+//     8t + 4 (ch & 1) .. + 3 of the block; signed bytes become exact f16 pairs, the block's two
+//     steps accumulate into fresh registers, and the block's fp16 scale multiplies that sum in
+//     fp32.  score = sum over blocks of delta_b (int8_b . q'_b).
+// V product: O^T[d x 8 columns] += V~^T[d x 16 token slots] . P'[16 slots x 8 columns], thread
+// (g, t) holding rows g, g + 8 of m tile mt = coordinates g d/8 + 2mt, + 1, and token slots
+// t, t + 8 (fragment registers 0, 1) and t + 4, t + 12 (registers 2, 3):
+//   * turbo-MSE V: the 2W bits of two coordinates index a table of f16 pairs lambda c[idx]
+//     (entry stride 128 B); the V norm goes into P' = weight * norm;
+//   * q8_0 V: the signed bytes of two tokens at one coordinate become an f16 pair, multiplied by
+//     the two tokens' block scales (f16); P' = weight.
+// P' columns: up to 4 heads, 2t / 2t + 1 = high / low fp16 part of head t's P'; 5 to 8 heads,
+// heads t and t + 4 in plain fp16 (a relative rounding of 2^-12 per weight; the query side needs
+// the split, since a score's rounding error grows with the score).
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "tq_device.cuh"
+#include "tq_warp_mma.cuh"
+
+namespace tq {
+namespace mmad {
+
+using namespace wm;
+
+constexpr int kPrefetchTiles = 4;  // L2 prefetch distance in tiles
+
+// Most 32-bit words that cover bits [s, s + n) for the starts s = i n, i < count.
+constexpr int cover_words(int n, int count) {
+  int m = 0;
+  for (int i = 0; i < count; ++i) {
+    const int w = ((i * n) % 32 + n + 31) / 32;
+    m = w > m ? w : m;
+  }
+  return m;
+}
+// Largest of 16, 8, 4 that divides both a and b.
+constexpr int vec_bytes(int a, int b) { return (a % 16 == 0 && b % 16 == 0) ? 16 : (a % 8 == 0 && b % 8 == 0) ? 8 : 4; }
+
+// Shape of one kernel: head_dim D, K code width WK (0 = q8_0), V code width WV (0 = q8_0).
+template <int D_, int WK_, int WV_>
+struct Fmt {
+  static constexpr int D = D_, WK = WK_, WV = WV_;
+  static constexpr bool KQ8 = WK == 0, VQ8 = WV == 0;
+  static constexpr int KS = D / 16;  // k steps of a score product = m tiles of the V product
+  static constexpr int KPay = KQ8 ? D : D * WK / 8, KHdr = KQ8 ? D / 16 : 4;
+  static constexpr int VPay = VQ8 ? D : D * WV / 8, VHdr = VQ8 ? D / 16 : 2;
+  // K words per thread and token.  turbo: the d W / 4-bit run at bit t d W / 4 (shifted by 16
+  // for odd t when the run is not a whole number of words); q8_0: bytes 8t .. 8t + 7 of each block.
+  static constexpr int KBits = KQ8 ? 0 : D * WK / 4;
+  static constexpr int KLoad = KQ8 ? D / 16 : cover_words(KBits, 4);
+  static constexpr int KRun = KQ8 ? 1 : (KBits + 31) / 32;
+  static constexpr bool KShift = !KQ8 && KBits % 32 != 0;
+  static constexpr int KVec = KQ8 ? 8 : (KShift ? 4 : vec_bytes(KPay, KBits / 8));
+  static constexpr int KHdrW = KQ8 ? D / 64 : 1;  // 32-bit header words per token
+  // V words per thread and token.  turbo: the d W / 8-bit run at bit g d W / 8; q8_0: bytes
+  // g d/8 .. (g+1) d/8 - 1.
+  static constexpr int VBits = VQ8 ? 0 : D * WV / 8;
+  static constexpr int VLoad = VQ8 ? D / 32 : cover_words(VBits, 8);
+  static constexpr int VRun = VQ8 ? 1 : (VBits + 31) / 32;
+  static constexpr bool VShift = !VQ8 && VBits % 32 != 0;
+  static constexpr int VVec = VQ8 ? vec_bytes(VPay, D / 8) : (VShift ? 4 : vec_bytes(VPay, VBits / 8));
+  // Tables: K entries 8 B x 32 lanes, V entries 4 B x 32 lanes, each aligned to its own size.
+  static constexpr uint32_t KLut = KQ8 ? 0u : (256u << (2 * WK));
+  static constexpr uint32_t VLut = VQ8 ? 0u : (128u << (2 * WV));
+  static constexpr uint32_t Big = KLut > VLut ? KLut : VLut, Small = KLut > VLut ? VLut : KLut;
+};
+
+// Launch shape of one kernel: NQ 8-column products per part (1: up to 4 query heads per KV head,
+// 2: up to 8), the warps' query fragments (8 bytes per lane, product and k step) and P' tiles, the
+// tables with the alignment slack of the larger one; 16 warps (d = 256: 8, for its ~180 registers
+// a thread), halved until the shared memory fits.
+constexpr int kSmemLimit = 227 * 1024;
+template <class F, bool HILO>
+struct Shape {
+  static constexpr int NQ = HILO ? 1 : 2;
+  static constexpr int QfBytes = F::KS * 256 * (F::KQ8 ? 1 : 2) * NQ;
+  static constexpr int PsBytes = 512;
+  static constexpr int smem(int warps) { return (int)(2 * F::Big + F::Small) + warps * (PsBytes + QfBytes); }
+  static constexpr int Warps = smem(F::D == 256 ? 8 : 16) <= kSmemLimit ? (F::D == 256 ? 8 : 16)
+                               : smem(F::D == 256 ? 4 : 8) <= kSmemLimit ? (F::D == 256 ? 4 : 8)
+                                                                          : (F::D == 256 ? 2 : 4);
+  static constexpr int Threads = 32 * Warps;
+  static constexpr int Smem = smem(Warps);
+  static_assert(Smem <= kSmemLimit, "shared memory");
+};
+
+// Loads N consecutive words from p (VEC-byte aligned) with the evict-first policy.
+template <int N, int VEC>
+__device__ __forceinline__ void load_words(uint32_t (&w)[N], const unsigned char* p, uint64_t pol) {
+  if constexpr (VEC == 16 && N % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < N; j += 4) {
+      const uint4 v = ld_stream_v4(p + 4 * j, pol);
+      w[j] = v.x; w[j + 1] = v.y; w[j + 2] = v.z; w[j + 3] = v.w;
+    }
+  } else if constexpr (VEC >= 8 && N % 2 == 0) {
+#pragma unroll
+    for (int j = 0; j < N; j += 2) {
+      const uint2 v = ld_stream_v2(p + 4 * j, pol);
+      w[j] = v.x; w[j + 1] = v.y;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < N; ++j) w[j] = ld_stream_u32(p + 4 * j, pol);
+  }
+}
+
+// The run of bits that starts at bit sh of w[0] (sh < 32), as words from bit 0.
+template <int NL, int NR, bool SHIFT>
+__device__ __forceinline__ void make_run(const uint32_t (&w)[NL], uint32_t (&r)[NR], uint32_t sh) {
+#pragma unroll
+  for (int j = 0; j < NR; ++j) {
+    if constexpr (SHIFT) r[j] = j + 1 < NL ? __funnelshift_r(w[j], w[j + 1 < NL ? j + 1 : j], sh) : (w[j] >> sh);
+    else r[j] = w[j];
+  }
+}
+
+// Table address for the N bits at bit p of the run r: base | bits << SH (p a constant once the
+// caller's loop is unrolled; base has zeros in bits SH .. SH + N - 1).
+template <int N, int SH, int NR>
+__device__ __forceinline__ uint32_t run_addr(const uint32_t (&r)[NR], int p, uint32_t base) {
+  const int wi = p >> 5, off = p & 31;
+  uint32_t x;
+  if (off + N <= 32) x = off >= SH ? (r[wi] >> (off - SH)) : (r[wi] << (SH - off));
+  else x = __funnelshift_r(r[wi], r[wi + 1 < NR ? wi + 1 : wi], off) << SH;
+  return (x & (((1u << N) - 1u) << SH)) | base;
+}
+
+struct Cursor {
+  const unsigned char *kp, *kh, *vp, *vh;  // this lane's addresses in the current tile
+  int in_page, page_ord;                   // token offset in its page; logical page
+  bool ok;                                 // page in range
+};
+
+template <class F, bool HILO>
+struct MmaWarp {
+  static constexpr int D = F::D, KS = F::KS;
+  static constexpr int NH = HILO ? 1 : 2;  // query heads per thread: t (and t + 4); = 8-column products per part
+
+  struct KTile {
+    uint32_t a[F::KLoad], b[F::KLoad];  // tokens g, g + 8
+    uint32_t ha[F::KHdrW], hb[F::KHdrW];
+  };
+  struct VTile {
+    uint32_t w[4][F::VLoad];  // tokens t, t + 8, t + 4, t + 12
+    uint32_t h0, h1;          // turbo: norms of tokens g, g + 8; q8_0: scales of t, t + 8 and t + 4, t + 12
+  };
+
+  const DecodeLaunch& k;
+  int lane, g, t;
+  uint32_t ylk, ylv;         // table bases | lane offsets
+  uint32_t psw0, psw1, psr;  // shared addresses of this lane's P' words in the warp's first P' tile
+  uint32_t qf;               // shared address of this lane's query fragments
+  uint32_t ksh, vsh;         // bit offsets of the K and V runs in their first words
+  int kto, vgo;              // byte offsets of this lane's K and V words in a vector
+  int vhdr;                  // byte offset of this lane's V header entry (q8_0: its block's scale)
+  int vwo[F::VLoad];         // byte offsets of the V words from the first (clamped to the payload)
+  bool pf_k, pf_v, pf_h;     // bulk prefetch allowed (16-byte aligned tile starts)
+  uint64_t pol;
+
+  int layer, b, kvh, ntiles, last_valid;
+  Cursor c;
+  float oacc[KS][4];
+  float m[NH], l[NH];
+
+  __device__ __forceinline__ MmaWarp(const DecodeLaunch& k_) : k(k_) {}
+
+  __device__ __forceinline__ void init_lane(int lane_) {
+    lane = lane_;
+    g = lane >> 2;
+    t = lane & 3;
+    if constexpr (F::KQ8) {
+      kto = 8 * t;
+      ksh = 0;
+    } else {
+      kto = 4 * ((t * F::KBits) >> 5);
+      ksh = (uint32_t)(t * F::KBits) & 31u;
+    }
+    if constexpr (F::VQ8) {
+      vgo = g * (D / 8);
+      vsh = 0;
+      vhdr = 2 * ((g * (D / 8)) >> 5);
+#pragma unroll
+      for (int j = 0; j < F::VLoad; ++j) vwo[j] = 4 * j;
+    } else {
+      const int w0 = (g * F::VBits) >> 5, last = F::VPay / 4 - 1;
+      vgo = 4 * w0;
+      vsh = (uint32_t)(g * F::VBits) & 31u;
+      vhdr = 0;
+#pragma unroll
+      for (int j = 0; j < F::VLoad; ++j) vwo[j] = 4 * (min(w0 + j, last) - w0);
+    }
+    const DecodeArgs& a = k.a;
+    const bool pg16 = a.k.page_size % 16 == 0;
+    pf_k = pg16 || F::KPay % 16 == 0;
+    pf_v = pg16 || F::VPay % 16 == 0;
+    pf_h = pg16 && ((reinterpret_cast<uintptr_t>(a.k.header) | reinterpret_cast<uintptr_t>(a.v.header)) & 15) == 0;
+  }
+
+  __device__ __forceinline__ void set_page() {
+    const DecodeArgs& a = k.a;
+    long long page = b;
+    c.ok = true;
+    if (a.block_table) {
+      page = a.block_table[(long long)b * a.max_blocks_per_seq + c.page_ord];
+      if (page < 0 || page >= a.k.num_pages) {
+        if (lane == 0) atomicOr(k.tab.status, kFlagBlockTable);
+        c.ok = false;
+        page = 0;
+      }
+    }
+    const long long base = (((long long)layer * a.k.num_pages + page) * a.k.H + kvh) * a.k.page_size + c.in_page;
+    c.kp = a.k.payload + (base + g) * F::KPay + kto;
+    c.kh = a.k.header + (base + g) * F::KHdr;
+    c.vp = a.v.payload + (base + t) * F::VPay + vgo;
+    c.vh = F::VQ8 ? a.v.header + (base + t) * F::VHdr + vhdr : a.v.header + (base + g) * F::VHdr;
+  }
+
+  __device__ __forceinline__ void advance() {
+    c.in_page += 16;
+    if (c.in_page == k.a.k.page_size) {
+      c.in_page = 0;
+      ++c.page_ord;
+      set_page();
+    } else {
+      c.kp += 16 * F::KPay;
+      c.kh += 16 * F::KHdr;
+      c.vp += 16 * F::VPay;
+      c.vh += 16 * F::VHdr;
+    }
+  }
+
+  // Rows at or beyond nvalid (ragged last tile) re-read row nvalid - 1; their scores are masked.
+  __device__ __forceinline__ void load_k(KTile& K, int nvalid) {
+    int da = 0, db = 8;
+    if (nvalid < 16) {
+      da = min(g, nvalid - 1) - g;
+      db = min(g + 8, nvalid - 1) - g;
+    }
+    const unsigned char* pa = c.kp + da * F::KPay;
+    const unsigned char* pb = c.kp + db * F::KPay;
+    if constexpr (F::KQ8) {
+#pragma unroll
+      for (int blk = 0; blk < D / 32; ++blk) {
+        const uint2 x = ld_stream_v2(pa + 32 * blk, pol), y = ld_stream_v2(pb + 32 * blk, pol);
+        K.a[2 * blk] = x.x; K.a[2 * blk + 1] = x.y;
+        K.b[2 * blk] = y.x; K.b[2 * blk + 1] = y.y;
+      }
+    } else {
+      load_words<F::KLoad, F::KVec>(K.a, pa, pol);
+      load_words<F::KLoad, F::KVec>(K.b, pb, pol);
+    }
+#pragma unroll
+    for (int j = 0; j < F::KHdrW; ++j) {
+      K.ha[j] = ld_stream_u32(c.kh + da * F::KHdr + 4 * j, pol);
+      K.hb[j] = ld_stream_u32(c.kh + db * F::KHdr + 4 * j, pol);
+    }
+  }
+
+  __device__ __forceinline__ void load_v(VTile& V, int nvalid) {
+    const int rows[4] = {t, t + 8, t + 4, t + 12};
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int dr = nvalid < 16 ? min(rows[r], nvalid - 1) - t : rows[r] - t;
+      const unsigned char* p = c.vp + dr * F::VPay;
+      if constexpr (F::VQ8 || F::VLoad == 1 || !F::VShift) {
+        load_words<F::VLoad, F::VVec>(V.w[r], p, pol);
+      } else {
+#pragma unroll
+        for (int j = 0; j < F::VLoad; ++j) V.w[r][j] = ld_stream_u32(p + vwo[j], pol);
+      }
+    }
+    if constexpr (F::VQ8) {
+      uint32_t s[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int dr = nvalid < 16 ? min(rows[r], nvalid - 1) - t : rows[r] - t;
+        s[r] = ld_stream_u16(c.vh + dr * F::VHdr, pol);
+      }
+      V.h0 = s[0] | (s[1] << 16);
+      V.h1 = s[2] | (s[3] << 16);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+#pragma unroll
+        for (int j = 0; j < F::VLoad; ++j) V.w[r][j] ^= 0x80808080u;
+      }
+    } else {
+      const int da = nvalid < 16 ? min(g, nvalid - 1) - g : 0;
+      const int db = nvalid < 16 ? min(g + 8, nvalid - 1) - g : 8;
+      V.h0 = ld_stream_u16(c.vh + da * F::VHdr, pol) | (ld_stream_u16(c.vh + db * F::VHdr, pol) << 16);
+      V.h1 = 0;
+    }
+  }
+
+  // Requests tiles [tile + ahead, tile + ahead + n) into L2, n <= count, clipped to the work
+  // item and to the page (lane 0, whose addresses are the current tile's own).
+  __device__ __forceinline__ void prefetch_tiles(int tile, int ahead, int count) {
+    const int n = min(min(ntiles - tile - ahead, count), (k.a.k.page_size - c.in_page) / 16 - ahead);
+    if (lane != 0 || n <= 0 || !c.ok) return;
+    if (pf_k) prefetch_l2(c.kp + 16 * ahead * F::KPay, 16 * n * F::KPay);
+    if (pf_v) prefetch_l2(c.vp + 16 * ahead * F::VPay, 16 * n * F::VPay);
+    if (pf_h) {
+      prefetch_l2(c.kh + 16 * ahead * F::KHdr, 16 * n * F::KHdr);
+      prefetch_l2(c.vh + 16 * ahead * F::VHdr, 16 * n * F::VHdr);
+    }
+  }
+
+  // Raises the reference of every head whose new scores pass it by 2^8 (warp-uniform decision).
+  __device__ __forceinline__ void raise_reference(float (&mx)[NH]) {
+    bool need = false;
+#pragma unroll
+    for (int h = 0; h < NH; ++h) need |= mx[h] > m[h] + kLazyMax;
+    if (!__any_sync(kFull, need)) return;
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], o));
+      const float mn = fmaxf(m[h], mx[h]);
+      const float al = ex2(m[h] - mn);
+      l[h] *= al;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        if (HILO) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) oacc[mt][e] *= al;
+        } else {
+          oacc[mt][h] *= al;
+          oacc[mt][2 + h] *= al;
+        }
+      }
+      m[h] = mn;
+    }
+  }
+
+  // Score products of a tile: cc[q] = codebook (or int8) part, cs[q] = QJL part of heads
+  // 4q .. 4q + 3 (columns 2h / 2h + 1 = high / low part of head 4q + h).  Query fragments of
+  // product j (turbo: 2q = codebook, 2q + 1 = QJL; q8_0: q) and step ch at qf + 256 (KS j + ch).
+  __device__ __forceinline__ void score(const KTile& K, float (&cc)[NH][4], float (&cs)[NH][4]) {
+    if constexpr (F::KQ8) {
+#pragma unroll
+      for (int blk = 0; blk < D / 32; ++blk) {
+        const uint32_t xa0 = K.a[2 * blk] ^ 0x80808080u, xa1 = K.a[2 * blk + 1] ^ 0x80808080u;
+        const uint32_t xb0 = K.b[2 * blk] ^ 0x80808080u, xb1 = K.b[2 * blk + 1] ^ 0x80808080u;
+        const uint32_t a00 = i8x2_to_h2<0x4140>(xa0), a01 = i8x2_to_h2<0x4140>(xb0);
+        const uint32_t a02 = i8x2_to_h2<0x4342>(xa0), a03 = i8x2_to_h2<0x4342>(xb0);
+        const uint32_t a10 = i8x2_to_h2<0x4140>(xa1), a11 = i8x2_to_h2<0x4140>(xb1);
+        const uint32_t a12 = i8x2_to_h2<0x4342>(xa1), a13 = i8x2_to_h2<0x4342>(xb1);
+        const int sh = 16 * (blk & 1);
+        const float da = __half2float(__ushort_as_half((unsigned short)(K.ha[blk >> 1] >> sh)));
+        const float db = __half2float(__ushort_as_half((unsigned short)(K.hb[blk >> 1] >> sh)));
+#pragma unroll
+        for (int q = 0; q < NH; ++q) {
+          const uint2 f0 = lds64(qf + 256 * (KS * q + 2 * blk)), f1 = lds64(qf + 256 * (KS * q + 2 * blk + 1));
+          float c[4];
+          mma_16816_zc(c, a00, a01, a02, a03, f0.x, f0.y);
+          mma_16816(c, a10, a11, a12, a13, f1.x, f1.y);
+          cc[q][0] = fmaf(da, c[0], cc[q][0]);
+          cc[q][1] = fmaf(da, c[1], cc[q][1]);
+          cc[q][2] = fmaf(db, c[2], cc[q][2]);
+          cc[q][3] = fmaf(db, c[3], cc[q][3]);
+        }
+      }
+    } else {
+      constexpr int N = 2 * F::WK;
+      uint32_t ra[F::KRun], rb[F::KRun];
+      make_run<F::KLoad, F::KRun, F::KShift>(K.a, ra, ksh);
+      make_run<F::KLoad, F::KRun, F::KShift>(K.b, rb, ksh);
+#pragma unroll
+      for (int ch = 0; ch < KS; ++ch) {
+        const int p = 4 * ch * F::WK;
+        const uint2 ea0 = lds64(run_addr<N, 8>(ra, p, ylk)), ea1 = lds64(run_addr<N, 8>(ra, p + N, ylk));
+        const uint2 eb0 = lds64(run_addr<N, 8>(rb, p, ylk)), eb1 = lds64(run_addr<N, 8>(rb, p + N, ylk));
+#pragma unroll
+        for (int q = 0; q < NH; ++q) {
+          const uint2 fq = lds64(qf + 256 * (KS * 2 * q + ch)), fs = lds64(qf + 256 * (KS * (2 * q + 1) + ch));
+          mma_16816(cc[q], ea0.x, eb0.x, ea1.x, eb1.x, fq.x, fq.y);
+          mma_16816(cs[q], ea0.y, eb0.y, ea1.y, eb1.y, fs.x, fs.y);
+        }
+      }
+    }
+  }
+
+  // V product of a tile with the P' fragments bp.
+  __device__ __forceinline__ void accumulate_v(const VTile& V, uint2 bp) {
+    if constexpr (F::VQ8) {
+      const __half2 d01 = u32_as_h2(V.h0), d23 = u32_as_h2(V.h1);
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        const int wi = (2 * mt) >> 2;
+        const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;  // bytes 2mt, 2mt + 1 of two tokens
+        const uint32_t x01 = __byte_perm(V.w[0][wi], V.w[1][wi], sel);
+        const uint32_t x23 = __byte_perm(V.w[2][wi], V.w[3][wi], sel);
+        const uint32_t a0 = h2_as_u32(__hmul2(u32_as_h2(i8x2_to_h2<0x4140>(x01)), d01));
+        const uint32_t a1 = h2_as_u32(__hmul2(u32_as_h2(i8x2_to_h2<0x4342>(x01)), d01));
+        const uint32_t a2 = h2_as_u32(__hmul2(u32_as_h2(i8x2_to_h2<0x4140>(x23)), d23));
+        const uint32_t a3 = h2_as_u32(__hmul2(u32_as_h2(i8x2_to_h2<0x4342>(x23)), d23));
+        mma_16816(oacc[mt], a0, a1, a2, a3, bp.x, bp.y);
+      }
+    } else {
+      constexpr int N = 2 * F::WV;
+      uint32_t r[4][F::VRun];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) make_run<F::VLoad, F::VRun, F::VShift>(V.w[q], r[q], vsh);
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        uint32_t e[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) e[q] = lds32(run_addr<N, 7>(r[q], 2 * mt * F::WV, ylv));
+        // a0/a1: slots 2t, 2t+1 = tokens t, t+8 at coordinate 2mt / 2mt+1; a2/a3: tokens t+4, t+12
+        mma_16816(oacc[mt], __byte_perm(e[0], e[1], 0x5410), __byte_perm(e[0], e[1], 0x7632),
+                  __byte_perm(e[2], e[3], 0x5410), __byte_perm(e[2], e[3], 0x7632), bp.x, bp.y);
+      }
+    }
+  }
+
+  // One tile at the cursor (the caller advances the cursor afterwards).
+  template <int BUF>
+  __device__ __forceinline__ void step(int tile) {
+    const int nvalid = tile == ntiles - 1 ? last_valid : 16;
+    if (!c.ok) {  // warp-uniform: the tile's page was out of range
+      __syncwarp();
+      return;
+    }
+    KTile kc;
+    load_k(kc, nvalid);
+    float cc[NH][4], cs[NH][4];
+#pragma unroll
+    for (int q = 0; q < NH; ++q) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) cc[q][e] = cs[q][e] = 0.f;
+    }
+    score(kc, cc, cs);
+    VTile vc;
+    load_v(vc, nvalid);
+
+    // thread (g, t) and head slot h (head t + 4h): entries 0, 1 of product h = token g, the
+    // high and low parts; entries 2, 3 = token g + 8.
+    float s[NH][2];
+    if constexpr (F::KQ8) {
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        s[h][0] = cc[h][0] + cc[h][1];
+        s[h][1] = cc[h][2] + cc[h][3];
+      }
+    } else {
+      const float2 hA = __half22float2(u32_as_h2(kc.ha[0])), hB = __half22float2(u32_as_h2(kc.hb[0]));
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        s[h][0] = fmaf(hA.x, cc[h][0] + cc[h][1], hA.y * (cs[h][0] + cs[h][1]));
+        s[h][1] = fmaf(hB.x, cc[h][2] + cc[h][3], hB.y * (cs[h][2] + cs[h][3]));
+      }
+    }
+    if (nvalid < 16) {
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        if (g >= nvalid) s[h][0] = -INFINITY;
+        if (g + 8 >= nvalid) s[h][1] = -INFINITY;
+      }
+    }
+
+    // ---- online softmax with a lazily raised reference (base 2) ----
+    {
+      float mx[NH];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) mx[h] = fmaxf(s[h][0], s[h][1]);
+      raise_reference(mx);
+    }
+    float p[NH][2];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      p[h][0] = ex2(s[h][0] - m[h]);
+      p[h][1] = ex2(s[h][1] - m[h]);
+      l[h] += p[h][0] + p[h][1];
+    }
+    // ---- Sparse V: weights below the threshold are dropped; an all-dropped tile skips V ----
+    if (k.a.skip_threshold > 0.f) {
+      const float tau = k.a.skip_threshold;
+      bool any = false;
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        p[h][0] = p[h][0] >= tau ? p[h][0] : 0.f;
+        p[h][1] = p[h][1] >= tau ? p[h][1] : 0.f;
+        any |= (p[h][0] + p[h][1]) > 0.f;
+      }
+      if (!__any_sync(kFull, any)) {
+        __syncwarp();
+        return;
+      }
+    }
+
+    // ---- P' = weight (* V norm for turbo V), one word per (column, token pair g / g + 8) ----
+    float2 nv = make_float2(1.f, 1.f);
+    if constexpr (!F::VQ8) nv = __half22float2(u32_as_h2(vc.h0));
+    constexpr uint32_t kBuf = 256 * BUF;
+    if (HILO) {
+      const float w0 = p[0][0] * nv.x, w1 = p[0][1] * nv.y;
+      const __half2 hi = __floats2half2_rn(w0, w1);
+      const float2 hf = __half22float2(hi);
+      sts32(psw0 + kBuf, h2_as_u32(hi));
+      sts32(psw1 + kBuf, h2_as_u32(__floats2half2_rn(w0 - hf.x, w1 - hf.y)));
+    } else {
+      sts32(psw0 + kBuf, h2_as_u32(__floats2half2_rn(p[0][0] * nv.x, p[0][1] * nv.y)));
+      sts32(psw1 + kBuf, h2_as_u32(__floats2half2_rn(p[NH - 1][0] * nv.x, p[NH - 1][1] * nv.y)));
+    }
+    __syncwarp();
+    accumulate_v(vc, lds64_v(psr + kBuf));
+  }
+
+  __device__ __forceinline__ void run_item(unsigned int item) {
+    const DecodeArgs& a = k.a;
+    const int H = a.k.H, G = k.G, Hq = a.n_q_heads;
+    const int split = (int)(item % k.n_splits);
+    const unsigned int rest = item / k.n_splits;
+    kvh = (int)(rest % H);
+    const int lb = (int)(rest / H);
+    layer = a.layer_begin + lb / a.batch;
+    b = lb % a.batch;
+    int len = a.seq_lens[b];
+    if (len < 0) len = 0;
+    if (len > a.max_ctx) {
+      if (lane == 0) atomicOr(k.tab.status, kFlagSeqLen);
+      len = a.max_ctx;
+    }
+    const int t0 = split * k.split_tokens;
+    const int t1 = min(t0 + k.split_tokens, len);
+    const long long row0 = (long long)lb * Hq + (long long)kvh * G;
+
+    // ---- B fragments of product q, column g: head 4q + g/2, the high (g even) or low (g odd)
+    // fp16 part.  k slots 2t, 2t + 1 (+8) of step ch = the coordinates c0(ch) + {0, 1} ({2, 3})
+    // that the A fragments hold.  Codebook (or int8) product: q' with log2 e (/ lambda for turbo
+    // K); QJL product: S q' with log2 e sqrt(pi/2) / d ----
+#pragma unroll
+    for (int q = 0; q < NH; ++q) {
+      const int head = 4 * q + (g >> 1);
+      const bool lo = g & 1;
+      const bool valid = head < G;
+      const float* qp = k.qprep + (row0 + (valid ? head : 0)) * 2 * D;
+      const float fq = valid ? (F::KQ8 ? kLog2e : kLog2e / k.tab.f16_scale[F::KQ8 ? 0 : F::WK - 2]) : 0.f;
+      const float fs = valid ? kLog2e * kSqrtHalfPi / (float)D : 0.f;
+      const int jq = F::KQ8 ? q : 2 * q;  // product index of the codebook (int8) part
+#pragma unroll
+      for (int ch = 0; ch < KS; ++ch) {
+        const int c0 = F::KQ8 ? 32 * (ch >> 1) + 8 * t + 4 * (ch & 1) : t * (D / 4) + 4 * ch;
+        const float4 v = *reinterpret_cast<const float4*>(qp + c0);
+        sts64(qf + 256 * (KS * jq + ch), pack_part(v.x * fq, v.y * fq, lo), pack_part(v.z * fq, v.w * fq, lo));
+        if constexpr (!F::KQ8) {
+          const float4 u = *reinterpret_cast<const float4*>(qp + D + c0);
+          sts64(qf + 256 * (KS * (jq + 1) + ch), pack_part(u.x * fs, u.y * fs, lo),
+                pack_part(u.z * fs, u.w * fs, lo));
+        }
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+    }
+
+    ntiles = t1 > t0 ? (t1 - t0 + 15) / 16 : 0;
+    last_valid = t1 - t0 - 16 * (ntiles - 1);
+    if (ntiles > 0) {
+      c.page_ord = t0 / a.k.page_size;
+      c.in_page = t0 - c.page_ord * a.k.page_size;
+      set_page();
+      prefetch_tiles(0, 0, kPrefetchTiles);
+      for (int tile = 0; tile < ntiles; tile += 2) {
+        prefetch_tiles(tile, kPrefetchTiles, 2);  // the two tiles that follow the ones already requested
+        step<0>(tile);
+        if (tile + 1 >= ntiles) break;
+        advance();
+        step<1>(tile + 1);
+        if (tile + 2 >= ntiles) break;
+        advance();
+      }
+    }
+
+    // ---- partial of this work item: (m, l, acc) per query head ----
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) l[h] += __shfl_xor_sync(kFull, l[h], o);
+    }
+    const float inv_lam = F::VQ8 ? 1.0f : 1.0f / k.tab.f16_scale[F::VQ8 ? 0 : F::WV - 1];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      const int head = t + 4 * h;
+      if (head >= G) continue;
+      float v[2 * KS];
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        if (HILO) {
+          v[2 * mt] = (oacc[mt][0] + oacc[mt][1]) * inv_lam;
+          v[2 * mt + 1] = (oacc[mt][2] + oacc[mt][3]) * inv_lam;
+        } else {
+          v[2 * mt] = oacc[mt][h] * inv_lam;
+          v[2 * mt + 1] = oacc[mt][2 + h] * inv_lam;
+        }
+      }
+      float* dst = k.partial + ((row0 + head) * k.n_splits + split) * (D + 4);
+      float4* dv = reinterpret_cast<float4*>(dst + 4 + g * (D / 8));
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) dv[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      if (g == 0) {
+        dst[0] = m[h] == -INFINITY ? -INFINITY : m[h] * kLn2;
+        dst[1] = l[h];
+      }
+    }
+  }
+
+  // Two f16 B-fragment halves: the high (or low) fp16 part of x0, x1.
+  static __device__ __forceinline__ uint32_t pack_part(float x0, float x1, bool lo) {
+    const __half2 hi = __floats2half2_rn(x0, x1);
+    if (!lo) return h2_as_u32(hi);
+    const float2 hf = __half22float2(hi);
+    return h2_as_u32(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+  }
+};
+
+template <class F, bool HILO>
+__global__ void __launch_bounds__(Shape<F, HILO>::Threads, 1) attend_mma_kernel(DecodeLaunch k) {
+  using L = Shape<F, HILO>;
+  extern __shared__ __align__(16) unsigned char sm[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // ---- shared layout: the larger table at an offset aligned to its size, the smaller one right
+  // after it (powers of two, so it is aligned to its own size too), the warps' P' tiles, then
+  // the warps' query fragments ----
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(sm));
+  const uint32_t bofs = F::Big ? ((F::Big - (sbase & (F::Big - 1u))) & (F::Big - 1u)) : 0u;
+  const uint32_t kofs = F::KLut >= F::VLut ? bofs : bofs + F::Big;
+  const uint32_t vofs = F::KLut >= F::VLut ? bofs + F::Big : bofs;
+  const uint32_t pofs = bofs + F::Big + F::Small;
+  const uint32_t qofs = pofs + L::Warps * L::PsBytes;
+  if constexpr (!F::KQ8) {
+    constexpr int W = F::WK, n = 1 << (2 * W), cm = (1 << W) - 1, im = (1 << (W - 1)) - 1;
+    const float* cb = k.tab.centroids + (W - 2) * 8;
+    const float lam = k.tab.f16_scale[W - 2];
+    for (int i = tid; i < n * 32; i += L::Threads) {
+      const int e = i >> 5, r = i & 31, c0 = e & cm, c1 = e >> W;
+      uint2 v;
+      v.x = h2_as_u32(__floats2half2_rn(lam * cb[c0 & im], lam * cb[c1 & im]));
+      v.y = h2_as_u32(__floats2half2_rn((c0 >> (W - 1)) ? 1.f : -1.f, (c1 >> (W - 1)) ? 1.f : -1.f));
+      *reinterpret_cast<uint2*>(sm + kofs + e * 256 + r * 8) = v;
+    }
+  }
+  if constexpr (!F::VQ8) {
+    constexpr int W = F::WV, n = 1 << (2 * W), cm = (1 << W) - 1;
+    const float* cb = k.tab.centroids + (W - 1) * 8;
+    const float lam = k.tab.f16_scale[W - 1];
+    for (int i = tid; i < n * 32; i += L::Threads) {
+      const int e = i >> 5, r = i & 31;
+      *reinterpret_cast<uint32_t*>(sm + vofs + e * 128 + r * 4) =
+          h2_as_u32(__floats2half2_rn(lam * cb[e & cm], lam * cb[e >> W]));
+    }
+  }
+  __syncthreads();
+
+  MmaWarp<F, HILO> w(k);
+  w.init_lane(lane);
+  w.ylk = (sbase + kofs) | ((uint32_t)lane << 3);
+  w.ylv = (sbase + vofs) | ((uint32_t)lane << 2);
+  const uint32_t ps = sbase + pofs + warp * L::PsBytes;  // this warp's two P' tiles of 64 words
+  w.psw0 = ps + 4 * ps_word(2 * w.t, w.g);
+  w.psw1 = ps + 4 * ps_word(2 * w.t + 1, w.g);
+  w.psr = ps + 4 * ps_word(w.g, w.t);
+  w.qf = sbase + qofs + warp * (uint32_t)L::QfBytes + lane * 8;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(w.pol));
+
+  const DecodeArgs& a = k.a;
+  const unsigned int n_items = (unsigned int)((long long)a.n_layers * a.batch * a.k.H * k.n_splits);
+  for (;;) {
+    unsigned int item = 0;
+    if (lane == 0) item = atomicAdd(k.counter, 1u);
+    item = __shfl_sync(kFull, item, 0);
+    if (item >= n_items) break;
+    __syncwarp();  // the previous item's P' reads are done before this item's writes
+    w.run_item(item);
+  }
+}
+
+template <class F, bool HILO>
+cudaError_t launch_shape(const DecodeLaunch& k, long long items, int sm_count, cudaStream_t s) {
+  using L = Shape<F, HILO>;
+  long long grid = sm_count;  // one persistent CTA per SM
+  if (items < grid * L::Warps) grid = (items + L::Warps - 1) / L::Warps;
+  if (grid < 1) grid = 1;
+  const cudaError_t e =
+      cudaFuncSetAttribute(attend_mma_kernel<F, HILO>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::Smem);
+  if (e != cudaSuccess) return e;
+  attend_mma_kernel<F, HILO><<<(unsigned)grid, L::Threads, L::Smem, s>>>(k);
+  return cudaGetLastError();
+}
+
+template <class F>
+cudaError_t launch_mma(const DecodeLaunch& k, int sm_count, cudaStream_t s) {
+  const long long items = (long long)k.a.n_layers * k.a.batch * k.a.k.H * k.n_splits;
+  if (items >= (1LL << 32)) return cudaErrorInvalidValue;
+  return k.G <= 4 ? launch_shape<F, true>(k, items, sm_count, s) : launch_shape<F, false>(k, items, sm_count, s);
+}
+
+}  // namespace mmad
+}  // namespace tq

@@ -109,6 +109,16 @@ struct DecodeLaunch {
 bool attend_fast_supported(const DecodeLaunch& k);
 cudaError_t launch_attend_fast(const DecodeLaunch& k, int sm_count, cudaStream_t s);
 
+// Format-parameterised tensor-core split-K attention (tq_decode_mma.cuh): K code width wk
+// (q8_0 = 0, turbo K = index bits + 1), V code width wv (q8_0 = 0, turbo-MSE V = index bits),
+// one translation unit per head_dim.
+bool mma_has_d64(int wk, int wv);
+bool mma_has_d128(int wk, int wv);
+bool mma_has_d256(int wk, int wv);
+cudaError_t mma_launch_d64(const DecodeLaunch& k, int wk, int wv, int sm_count, cudaStream_t s);
+cudaError_t mma_launch_d128(const DecodeLaunch& k, int wk, int wv, int sm_count, cudaStream_t s);
+cudaError_t mma_launch_d256(const DecodeLaunch& k, int wk, int wv, int sm_count, cudaStream_t s);
+
 }  // namespace tq
 
 struct tq_context {

@@ -1,0 +1,120 @@
+// Warp-level helpers of the split-K decode kernels: mma.sync m16n8k16 (f16 in, f32 accumulate),
+// base-2 exponential, shared-memory table and tile accesses, streaming cache loads with an L2
+// policy, bulk L2 prefetch, and the layout of a warp's P' tile.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_fp16.h>
+
+namespace tq {
+namespace wm {
+
+constexpr float kLog2e = 1.4426950408889634074f;
+constexpr float kLn2 = 0.6931471805599453094f;
+constexpr float kLazyMax = 8.0f;
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 2^x for x <= 8 (scores never pass the reference by more); -inf -> 0
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Table reads (the tables do not change after the prologue of the kernel).
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// Query fragments of a work item (written once per item by the lane that reads them).
+__device__ __forceinline__ void sts64(uint32_t addr, uint32_t x, uint32_t y) {
+  asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(addr), "r"(x), "r"(y) : "memory");
+}
+
+// P' tile accesses (ordered by __syncwarp, hence volatile).
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint2 lds64_v(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+
+// Streaming cache loads: no L1 allocation, evict-first in L2.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p, uint64_t pol) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_stream_u16(const void* p, uint64_t pol) {
+  unsigned short v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u16 %0, [%1], %2;" : "=h"(v) : "l"(p), "l"(pol));
+  return v;
+}
+// Bulk request of [p, p + bytes) into L2; p and bytes are multiples of 16.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+
+// Four f32 accumulators = A . B with a zero C (f16 operands).
+__device__ __forceinline__ void mma_16816_zc(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};\n"
+      : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p, uint64_t pol) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0,%1}, [%2], %3;"
+               : "=r"(v.x), "=r"(v.y)
+               : "l"(p), "l"(pol));
+  return v;
+}
+
+// Two signed bytes of x ^ 0x80808080 (bytes 0, 1 for SEL = 0x4140, bytes 2, 3 for 0x4342) as an
+// exact f16 pair: byte u = b + 128 under exponent bits 0x64 is the f16 value 1024 + u, and
+// subtracting 1152 leaves b.
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t i8x2_to_h2(uint32_t xb) {
+  const uint32_t h = __byte_perm(xb, 0x64646464u, SEL);
+  return h2_as_u32(__hsub2(u32_as_h2(h), u32_as_h2(0x64806480u)));
+}
+
+// P' word (column col, token pair k2 = tokens k2 and k2 + 8) in a warp's P' tile:
+// the reader's two words (k2 = t, t + 4) are adjacent, and both the writers'
+// and the reader's accesses fall on distinct banks.
+__device__ __forceinline__ int ps_word(int col, int k2) {
+  return (col * 8 + (k2 & 3) * 2 + (k2 >> 2)) ^ ((col & 4) << 1);
+}
+
+}  // namespace wm
+}  // namespace tq

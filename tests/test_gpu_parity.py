@@ -282,6 +282,55 @@ def test_decode_on_oracle_codes(ctx, kfmt, vfmt):
             assert err.max() < C.ATTN_RTOL, (b, err.max())
 
 
+MMA_K = ["turbo2", "turbo3", "turbo4", "q8_0"]
+MMA_V = ["turbo2_mse", "turbo3_mse", "turbo4_mse", "q8_0"]
+_MMA_LENS = [0, 1, 17, 300, 613]
+_mma_codes = {}
+
+
+def _mma_oracle(ctx, fmt, is_k):
+    """Oracle codes and dequantised vectors of one role (K or V) for every sequence of
+    _MMA_LENS, concatenated; shared by the format pairs of one head_dim."""
+    key = (ctx.d, fmt, is_k)
+    if key not in _mma_codes:
+        T = sum(_MMA_LENS)
+        x16 = W.kv_tensor(T, 2, ctx.d, seed=31 if is_k else 37, outlier_frac=0.01).numpy()
+        enc = C.oracle_encode(fmt, x16, ctx.signs, ctx.S)
+        _mma_codes[key] = (enc, C.oracle_dequant(fmt, enc, ctx.signs, ctx.S))
+    return _mma_codes[key]
+
+
+@pytest.mark.parametrize("G", [4, 8])
+@pytest.mark.parametrize("vfmt", MMA_V)
+@pytest.mark.parametrize("kfmt", MMA_K)
+def test_decode_tensor_core_format_pairs_paged(ctx, kfmt, vfmt, G):
+    """Every K x V format pair of the tensor-core decode kernels at head_dim 64/128/256, with
+    4 query heads per KV head (high/low fp16 query columns) and 8 (two heads per column pair):
+    16-token pages in shuffled order, lengths 0, 1, 17, 300, 613 (ragged tiles, several
+    256-token splits), Sparse V at 1e-6; identical codes on both sides."""
+    d, H, P = ctx.d, 2, 16
+    lens = np.array(_MMA_LENS)
+    bt, npages = W.shuffled_block_table(lens, P, seed=11, extra_pages=3)
+    ek, kt = _mma_oracle(ctx, kfmt, True)
+    ev, vt = _mma_oracle(ctx, vfmt, False)
+    kview = tq.alloc_view(kfmt, d, H, page_size=P, num_pages=npages)
+    vview = tq.alloc_view(vfmt, d, H, page_size=P, num_pages=npages)
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]])
+    slots = np.concatenate([bt[b, np.arange(L) // P] * P + np.arange(L) % P for b, L in enumerate(lens)])
+    C.write_oracle_codes(kview, ek, kfmt, slots)
+    C.write_oracle_codes(vview, ev, vfmt, slots)
+    q = W.normal_tensor((1, len(lens), H * G, d), seed=13, device="cuda")
+    out = C.decode(ctx, q, kview, vview, lens, int(lens.max()), block_table=bt, max_blocks=bt.shape[1], tau=1e-6)
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert torch.all(out[0, b] == 0)
+            continue
+        sl = slice(starts[b], starts[b] + L)
+        o_full, _ = O.decode_attention(q[0, b].cpu().numpy().astype(np.float64), kt[sl], vt[sl], 1.0 / math.sqrt(d))
+        err = C.rel_err_per_head(out[0, b].cpu().numpy(), o_full)
+        assert err.max() < C.ATTN_RTOL, (b, err.max())
+
+
 @pytest.mark.parametrize("G", [1, 8, 16])
 def test_decode_gqa_groups(ctx128, G):
     d, H, T = 128, 2, 333
