@@ -87,16 +87,25 @@ struct Fmt {
 };
 
 // Launch shape of one kernel: NQ 8-column products per part (1: up to 4 query heads per KV head,
-// 2: up to 8), the warps' query fragments (8 bytes per lane, product and k step) and P' tiles, the
-// tables with the alignment slack of the larger one; 16 warps (d = 256: 8, for its ~180 registers
-// a thread), halved until the shared memory fits.
+// 2: up to 8); per warp a block of two P' tiles and the query fragments (8 bytes per lane, product
+// and k step); the two tables.  Shared layout (attend_mma_kernel): the larger table on the first
+// boundary of its size, the smaller table right below it (else right above), as many warp blocks
+// as fit below that from the start, the others above the tables; whatever the start's alignment,
+// that ends within Big + Small + warps * block + max(Small, block) bytes, or 2 Big + Small when the
+// gap below the larger table holds every warp block.  16 warps (d = 256: 8, for its ~180
+// registers a thread), halved until the shared memory fits.
 constexpr int kSmemLimit = 227 * 1024;
 template <class F, bool HILO>
 struct Shape {
   static constexpr int NQ = HILO ? 1 : 2;
   static constexpr int QfBytes = F::KS * 256 * (F::KQ8 ? 1 : 2) * NQ;
   static constexpr int PsBytes = 512;
-  static constexpr int smem(int warps) { return (int)(2 * F::Big + F::Small) + warps * (PsBytes + QfBytes); }
+  static constexpr int Block = PsBytes + QfBytes;
+  static constexpr int smem(int warps) {
+    const int packed = (int)(F::Big + F::Small) + warps * Block + ((int)F::Small > Block ? (int)F::Small : Block);
+    const int gap = (int)(2 * F::Big + F::Small);
+    return packed > gap ? packed : gap;
+  }
   static constexpr int Warps = smem(F::D == 256 ? 8 : 16) <= kSmemLimit ? (F::D == 256 ? 8 : 16)
                                : smem(F::D == 256 ? 4 : 8) <= kSmemLimit ? (F::D == 256 ? 4 : 8)
                                                                           : (F::D == 256 ? 2 : 4);
@@ -646,15 +655,20 @@ __global__ void __launch_bounds__(Shape<F, HILO>::Threads, 1) attend_mma_kernel(
   extern __shared__ __align__(16) unsigned char sm[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  // ---- shared layout: the larger table at an offset aligned to its size, the smaller one right
-  // after it (powers of two, so it is aligned to its own size too), the warps' P' tiles, then
-  // the warps' query fragments ----
+  // ---- shared layout: the larger table on the first boundary of its size, the smaller one right
+  // below it when there is room (both powers of two, so it is aligned to its own size), else right
+  // above; warp blocks (two P' tiles, then the query fragments) from the start up to the smaller
+  // table, the rest above the tables ----
   const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(sm));
   const uint32_t bofs = F::Big ? ((F::Big - (sbase & (F::Big - 1u))) & (F::Big - 1u)) : 0u;
-  const uint32_t kofs = F::KLut >= F::VLut ? bofs : bofs + F::Big;
-  const uint32_t vofs = F::KLut >= F::VLut ? bofs + F::Big : bofs;
-  const uint32_t pofs = bofs + F::Big + F::Small;
-  const uint32_t qofs = pofs + L::Warps * L::PsBytes;
+  const bool small_below = bofs >= F::Small;
+  const uint32_t sofs = small_below ? bofs - F::Small : bofs + F::Big;
+  const uint32_t n_below = (small_below ? sofs : bofs) / (uint32_t)L::Block;
+  const uint32_t above = bofs + F::Big + (small_below ? 0u : F::Small);
+  const uint32_t kofs = F::KLut >= F::VLut ? bofs : sofs;
+  const uint32_t vofs = F::KLut >= F::VLut ? sofs : bofs;
+  const uint32_t wofs = (uint32_t)warp < n_below ? warp * (uint32_t)L::Block
+                                                 : above + (warp - n_below) * (uint32_t)L::Block;
   if constexpr (!F::KQ8) {
     constexpr int W = F::WK, n = 1 << (2 * W), cm = (1 << W) - 1, im = (1 << (W - 1)) - 1;
     const float* cb = k.tab.centroids + (W - 2) * 8;
@@ -683,11 +697,11 @@ __global__ void __launch_bounds__(Shape<F, HILO>::Threads, 1) attend_mma_kernel(
   w.init_lane(lane);
   w.ylk = (sbase + kofs) | ((uint32_t)lane << 3);
   w.ylv = (sbase + vofs) | ((uint32_t)lane << 2);
-  const uint32_t ps = sbase + pofs + warp * L::PsBytes;  // this warp's two P' tiles of 64 words
+  const uint32_t ps = sbase + wofs;  // this warp's two P' tiles of 64 words, then its query fragments
   w.psw0 = ps + 4 * ps_word(2 * w.t, w.g);
   w.psw1 = ps + 4 * ps_word(2 * w.t + 1, w.g);
   w.psr = ps + 4 * ps_word(w.g, w.t);
-  w.qf = sbase + qofs + warp * (uint32_t)L::QfBytes + lane * 8;
+  w.qf = ps + L::PsBytes + lane * 8;
   asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(w.pol));
 
   const DecodeArgs& a = k.a;

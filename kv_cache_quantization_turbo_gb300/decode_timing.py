@@ -1,0 +1,123 @@
+"""Decode-attention timing on the workload recipes that the benchmark step does not cover.
+
+    python -m kv_cache_quantization_turbo_gb300.decode_timing --workload paged-batch64-turbo3 --head-dim 128
+    python -m kv_cache_quantization_turbo_gb300.decode_timing --workload asym-q8k-turbo2v-needles
+
+Builds the recipe's compressed cache on cuda:0 with the library's own encoder (seeded synthetic
+inputs from workloads.py), then times whole decode calls (every layer of the recipe, one query
+per sequence and query head) with CUDA events on the launching stream after warm-up calls, and
+prints one JSON line: algorithmic bytes (the compressed K and V of every attended token, once)
+per second.  The caches are several GB, far larger than L2, so no flush is needed between calls.
+"""
+import argparse
+import json
+import math
+
+import numpy as np
+import torch
+
+from . import tq
+from . import workloads as W
+
+
+def _decode_fn(ctx, q, kview, vview, layer_begin, lens, max_ctx, block_table=None, max_blocks=0, tau=1e-6):
+    L, B, Hq, d = q.shape
+    ws_bytes = tq.tq_decode_workspace_bytes(ctx, L, B, Hq, max_ctx)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty((L, B, Hq, d), dtype=torch.float32, device="cuda")
+    sl = torch.as_tensor(np.asarray(lens, dtype=np.int32), device="cuda")
+    bt = None if block_table is None else torch.as_tensor(block_table.astype(np.int32), device="cuda")
+
+    def run():
+        st = tq.tq_decode_attention(ctx, q, 0, L, B, Hq, kview, vview, layer_begin, sl, max_ctx, bt, max_blocks,
+                                    1.0 / math.sqrt(d), tau, ws, ws_bytes, out)
+        assert st == tq.TQ_OK, tq.tq_status_string(st)
+    return run
+
+
+def _needles(wl):
+    """q8_0 K everywhere; V q8_0 on the boundary layers and the recipe's V format elsewhere; one
+    sequence of wl.ctx tokens with 16 needles per KV head (two decode calls: boundary, middle)."""
+    L, H, d, T, Hq = wl.n_layers, wl.n_kv_heads, wl.head_dim, wl.ctx, wl.n_q_heads
+    boundary = sorted(wl.v_format_layers)
+    middle = [l for l in range(L) if l not in wl.v_format_layers]
+    ctx = tq.tq_context_create(d, wl.wht_seed, wl.qjl_seed, W.wht_signs(wl.wht_seed, d), W.qjl_matrix(wl.qjl_seed, d))
+    views = {"kb": tq.alloc_view(wl.k_format, d, H, page_size=T, num_pages=1, n_layers=len(boundary)),
+             "vb": tq.alloc_view("q8_0", d, H, page_size=T, num_pages=1, n_layers=len(boundary)),
+             "km": tq.alloc_view(wl.k_format, d, H, page_size=T, num_pages=1, n_layers=len(middle)),
+             "vm": tq.alloc_view(wl.v_format, d, H, page_size=T, num_pages=1, n_layers=len(middle))}
+    q = torch.empty((L, 1, Hq, d), dtype=torch.float32, device="cuda")
+    for l in range(L):
+        k, ql, _ = W.needle_workload(T, H, Hq, d, seed=wl.seed * 1000 + 2 * l, device="cuda")
+        v = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * l + 1, device="cuda")
+        q[l, 0] = ql
+        kv, vv, li = (views["kb"], views["vb"], boundary.index(l)) if l in wl.v_format_layers else \
+            (views["km"], views["vm"], middle.index(l))
+        st = tq.tq_encode_kv(ctx, kv, k, vv, v, li, 1, T, T * H * d, H * d)
+        assert st == tq.TQ_OK, tq.tq_status_string(st)
+    fb = _decode_fn(ctx, q[boundary].contiguous(), views["kb"], views["vb"], 0, [T], T)
+    fm = _decode_fn(ctx, q[middle].contiguous(), views["km"], views["vm"], 0, [T], T)
+    vb = lambda f: tq.tq_vector_bytes(f, d)
+    nbytes = H * T * (len(boundary) * (vb(wl.k_format) + vb("q8_0")) + len(middle) * (vb(wl.k_format) +
+                                                                                     vb(wl.v_format)))
+    cfg = {"layers": L, "kv_heads": H, "q_heads": Hq, "head_dim": d, "ctx": T, "k_format": wl.k_format,
+           "v_format": wl.v_format, "boundary_layers_v": "q8_0", "boundary_layers": boundary}
+    return ctx, (lambda: (fb(), fm())), nbytes, cfg
+
+
+def _paged(wl, d):
+    """wl.batch sequences of U[1K, ctx] tokens in shuffled wl.page_size-token pages."""
+    L, H, Hq, B, P = wl.n_layers, wl.n_kv_heads, wl.n_q_heads, wl.batch, wl.page_size
+    lens = W.seq_lens_uniform(B, 1024, wl.ctx, wl.seed)
+    bt, npages = W.shuffled_block_table(lens, P, wl.seed)
+    ctx = tq.tq_context_create(d, wl.wht_seed, wl.qjl_seed, W.wht_signs(wl.wht_seed, d), W.qjl_matrix(wl.qjl_seed, d))
+    kview = tq.alloc_view(wl.k_format, d, H, page_size=P, num_pages=npages, n_layers=L)
+    vview = tq.alloc_view(wl.v_format, d, H, page_size=P, num_pages=npages, n_layers=L)
+    slots = np.concatenate([bt[b, np.arange(lens[b]) // P] * P + np.arange(lens[b]) % P for b in range(B)])
+    slots_d = torch.as_tensor(slots.astype(np.int64), device="cuda")
+    n_tok = int(lens.sum())
+    for l in range(L):
+        k = W.kv_tensor(n_tok, H, d, seed=wl.seed * 1000 + 2 * l, device="cuda")
+        v = W.kv_tensor(n_tok, H, d, seed=wl.seed * 1000 + 2 * l + 1, device="cuda")
+        st = tq.tq_encode_kv(ctx, kview, k, vview, v, l, 1, n_tok, n_tok * H * d, H * d, slots_d)
+        assert st == tq.TQ_OK, tq.tq_status_string(st)
+        del k, v
+    q = W.normal_tensor((L, B, Hq, d), seed=wl.seed * 1000 + 999, device="cuda")
+    f = _decode_fn(ctx, q, kview, vview, 0, lens, int(lens.max()), bt, bt.shape[1])
+    nbytes = L * H * n_tok * (tq.tq_vector_bytes(wl.k_format, d) + tq.tq_vector_bytes(wl.v_format, d))
+    cfg = {"layers": L, "kv_heads": H, "q_heads": Hq, "head_dim": d, "batch": B, "page_size": P,
+           "tokens": n_tok, "max_ctx": int(lens.max()), "k_format": wl.k_format, "v_format": wl.v_format}
+    return ctx, f, nbytes, cfg
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--workload", required=True, choices=["asym-q8k-turbo2v-needles", "paged-batch64-turbo3"])
+    p.add_argument("--head-dim", type=int, default=128, choices=[64, 128, 256], help="paged recipe only")
+    p.add_argument("--calls", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    args = p.parse_args(argv)
+    if not torch.cuda.is_available():
+        raise SystemExit("decode_timing needs a CUDA device")
+    wl = W.WORKLOADS[args.workload]
+    ctx, run, nbytes, cfg = _needles(wl) if args.workload == "asym-q8k-turbo2v-needles" else _paged(wl, args.head_dim)
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.calls):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    dt = e0.elapsed_time(e1) / args.calls / 1e3
+    st, flags = tq.tq_get_status(ctx)
+    assert st == tq.TQ_OK and flags == 0, (st, flags)
+    tq.tq_context_destroy(ctx)
+    print(json.dumps({"metric": "decode_attention_bandwidth", "value": round(nbytes / dt / 1e9, 1), "unit": "GB/s",
+                      "ms_per_call": round(dt * 1e3, 4), "algorithmic_bytes": int(nbytes), "calls": args.calls,
+                      "warmup": args.warmup, "workload": args.workload, "config": cfg, "skip_threshold": 1e-6}))
+
+
+if __name__ == "__main__":
+    main()

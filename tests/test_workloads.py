@@ -34,3 +34,15 @@ def test_seq_lens_and_block_table():
     used = bt[bt >= 0]
     assert len(np.unique(used)) == used.size == n
     assert all((bt[b] >= 0).sum() == (L[b] + 15) // 16 for b in range(64))
+
+
+def test_decode_timing_cli_without_a_device():
+    """The decode-timing module parses its recipes and refuses to run without CUDA (no CPU path)."""
+    import pytest
+    import torch
+    from kv_cache_quantization_turbo_gb300 import decode_timing
+    with pytest.raises(SystemExit):
+        decode_timing.main(["--workload", "no-such-recipe"])
+    if not torch.cuda.is_available():
+        with pytest.raises(SystemExit, match="CUDA"):
+            decode_timing.main(["--workload", "paged-batch64-turbo3", "--head-dim", "64"])
