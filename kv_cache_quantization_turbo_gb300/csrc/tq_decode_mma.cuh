@@ -146,10 +146,12 @@ __device__ __forceinline__ void make_run(const uint32_t (&w)[NL], uint32_t (&r)[
 }
 
 // Table address for the N bits at bit p of the run r: base | bits << SH (p a constant once the
-// caller's loop is unrolled; base has zeros in bits SH .. SH + N - 1).
+// caller's loop is unrolled; base has zeros in bits SH .. SH + N - 1).  A whole byte at bit 8 of
+// a base whose bits 8 .. 15 are zero is one byte permute.
 template <int N, int SH, int NR>
 __device__ __forceinline__ uint32_t run_addr(const uint32_t (&r)[NR], int p, uint32_t base) {
   const int wi = p >> 5, off = p & 31;
+  if (N == 8 && SH == 8 && (off & 7) == 0) return __byte_perm(r[wi], base, 0x7604u | ((uint32_t)(off >> 3) << 4));
   uint32_t x;
   if (off + N <= 32) x = off >= SH ? (r[wi] >> (off - SH)) : (r[wi] << (SH - off));
   else x = __funnelshift_r(r[wi], r[wi + 1 < NR ? wi + 1 : wi], off) << SH;
