@@ -456,7 +456,8 @@ def main():
                      "kernel": "decode attention call (prologue + split-K attention + combine), one launch set "
                                f"over all {wl.n_layers} layers",
                      "traffic": profiled_traffic([os.path.join(ROOT, "kv_cache_quantization_turbo_gb300", "csrc", f)
-                                                  for f in ("tq_decode_fast.cu", "tq_decode.cu", "tq_warp_mma.cuh")])},
+                                                  for f in ("tq_decode_mma.cuh", "tq_decode_mma128.cu", "tq_decode.cu",
+                                                            "tq_warp_mma.cuh")])},
         "roofline_encode": {"bound": "hbm", "achieved": round(encode_bytes(tq, wl) / t_enc / 1e9, 2), "peak": hbm,
                             "unit": "GB/s", "frac": round(encode_bytes(tq, wl) / t_enc / 1e9 / hbm, 4),
                             "peak_source": f"{peak_src} hbm_gbs",

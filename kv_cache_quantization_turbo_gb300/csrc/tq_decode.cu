@@ -1,17 +1,19 @@
 // Decode attention over the compressed cache.
 //
-//   1. prologue (one warp per query head): q' = scale * H diag(s) q  and
+//   1. prologue (one CTA per query row): q' = scale * H diag(s) q  and
 //      Sq' = S q'  for turbo K ("rotate q once"); q' = scale * q for q8_0 K.
-//   2. split-K attention: each CTA takes one (split of the context, KV head,
-//      layer x sequence) and all G query heads of that KV head; it scores the
+//   2. split-K attention: a work item is (split of the context, KV head,
+//      layer x sequence) with all G query heads of that KV head; it scores the
 //      packed K against q' and Sq',
 //        s_j = n_j <q', c[idx_j]> + rnorm_j sqrt(pi/2)/d <Sq', 2 sigma_j - 1>,
 //      keeps an online softmax (running max m, sum l), accumulates V in the
 //      rotated space as exp(s_j - m) n_j c_V[idx_j] unless that weight is below
 //      skip_threshold ("TurboQuant+: 3.8x compression ...", core content item
-//      4, Sparse V), and writes the partial (m, l, acc).
-//   3. combine (one warp per query head): log-sum-exp merge of the partials,
-//      acc / l, then diag(s) H back to the original space for turbo V.
+//      4, Sparse V), and writes the partial (m, l, acc).  Up to 8 query heads
+//      per KV head run on tensor cores (tq_decode_mma.cuh); more, or pages that
+//      are not a multiple of 16 tokens, run attend_generic_kernel below.
+//   3. combine (one CTA of 4 warps per query row): log-sum-exp merge of the
+//      partials, acc / l, then diag(s) H back to the original space for turbo V.
 #include <cmath>
 
 #include <cuda_fp16.h>
@@ -28,7 +30,7 @@ static int next_pow2(long long v) {
 
 DecodePlan plan_decode(int sm_count, int d, int n_layers, int batch, int n_q_heads, int max_ctx) {
   DecodePlan p{};
-  // Split size: aim at ~12 work items per warp of the fast kernel (16 warps per SM,
+  // Split size: aim at ~12 work items per warp of the tensor-core kernel (16 warps per SM,
   // query heads shared by about 4 per KV head), between 256 and 4096 tokens.  Timed on
   // the 32-layer x 32K bench workload: 512-token splits beat 1024 (item count vs. load
   // balance) and 256 (per-item overhead and partial traffic).
@@ -403,9 +405,8 @@ cudaError_t launch_decode_dim(const DecodeKernelArgs& ka, int sm_count, cudaStre
   const DecodeArgs& a = ka.a;
   const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
   qprep_kernel<D><<<(unsigned)rows, D, 0, s>>>(ka);
-  if (attend_fast_supported(ka) || attend_mma_supported(ka, D)) {
-    const cudaError_t e =
-        attend_fast_supported(ka) ? launch_attend_fast(ka, sm_count, s) : launch_attend_mma(ka, D, sm_count, s);
+  if (attend_mma_supported(ka, D)) {
+    const cudaError_t e = launch_attend_mma(ka, D, sm_count, s);
     if (e != cudaSuccess) return e;
     combine_kernel<D><<<(unsigned)rows, 32 * kCombineWarps, 0, s>>>(ka);
     return cudaGetLastError();

@@ -1,11 +1,30 @@
 // Split-K decode attention on tensor cores, parameterised by the cache formats: turbo K with
 // W-bit codes (W - 1 index bits + the QJL sign bit; turbo2/3/4), turbo-MSE V with W-bit indices
-// (turbo2/3/4_mse), and q8_0 K or V, at head_dim 64, 128 or 256.  The turbo4 K + turbo4_mse V
-// pair at head_dim 128 with up to 4 query heads per KV head keeps its hand-specialised kernel
-// (tq_decode_fast.cu); this template takes everything else, with the same contract (one partial
-// (m, l, acc) per query row and split, combined afterwards), the same work items, 16-token tiles,
-// base-2 online softmax with a lazily raised reference, Sparse V skip and L2 prefetch.  What the
-// formats change is how a tile's codes reach the tensor-core fragments.
+// (turbo2/3/4_mse), and q8_0 K or V, at head_dim 64, 128 or 256, up to 8 query heads per KV head.
+// One partial (m, l, acc) per query row and split, combined afterwards.
+//
+// Why tensor cores: at HBM speed one 16-token tile of one KV head (1888 B for turbo4 / turbo4_mse
+// at d = 128) leaves ~350 warp instructions per SM, and scoring it on CUDA cores takes ~3 G d
+// FMAs per token; the contraction over the G query heads of a KV head is a dense (16 tokens x d)
+// x (d x G) product per tile, so it and the V accumulation run on mma.sync m16n8k16 (f16 in, f32
+// accumulate) over operands dequantised by table lookups.
+//
+// Work: a work item is (layer x sequence, KV head, split of the context); each warp takes items
+// from an atomic counter (zeroed by the prologue kernel) and writes one partial per query head
+// and item, so warps never wait for each other.  One persistent CTA per SM.  Per tile of 16
+// tokens: K loads, score products, online softmax in registers (base 2, with a reference raised
+// lazily: only when a score passes it by 2^8 are the sums and accumulators rescaled), Sparse V
+// (a tile whose every weight is below the threshold skips V; inside a kept tile weights below it
+// are zeroed), P' into a per-warp shared tile, V loads, V products.  Memory: every second tile one
+// lane requests the two tiles 4-5 ahead into L2 (cp.async.bulk.prefetch; contiguous caches: the
+// tiles of a page), so a tile's own register loads meet L2; cache loads carry an evict-first L2
+// policy so that the partials stay in L2 for the combine.
+//
+// Tables: entries replicated per lane (lane offset 8 or 4 bytes, entry stride 256 or 128 bytes)
+// so a warp's 32 lookups never collide, each table on a boundary of its own size so that the
+// address is the code bits shifted into place OR (table base | lane offset).  They hold
+// lambda * centroid in fp16, lambda chosen on the host so that every entry is within ~2e-5 of
+// its fp32 value; 1/lambda goes into the query columns (K) and the partial's accumulator (V).
 //
 // Score products (mma.sync m16n8k16, rows = the 16 tokens of a tile, columns 2h / 2h + 1 = the
 // high / low fp16 part of query head h, about 21 significant bits of q'; with 5 to 8 query heads
@@ -28,6 +47,9 @@
 //     (entry stride 128 B); the V norm goes into P' = weight * norm;
 //   * q8_0 V: the signed bytes of two tokens at one coordinate become an f16 pair, multiplied by
 //     the two tokens' block scales (f16); P' = weight.
+// The V product's k slots hold the tokens in the order 0, 8, 1, 9, ..., so one byte permute per
+// register pairs two tokens' table entries at one coordinate (the fragment layout of a contraction
+// over tokens), and each thread stores its two tokens' weights of one column as one 32-bit word.
 // P' columns: up to 4 heads, 2t / 2t + 1 = high / low fp16 part of head t's P'; 5 to 8 heads,
 // heads t and t + 4 in plain fp16 (a relative rounding of 2^-12 per weight; the query side needs
 // the split, since a score's rounding error grows with the score).

@@ -104,12 +104,7 @@ struct DecodeLaunch {
   unsigned int* counter;  // work-item counter (zeroed by the prologue kernel)
 };
 
-// Fast split-K attention (tensor-core contraction over LUT-dequantised tiles)
-// for the formats and shapes it covers; the generic kernel handles the rest.
-bool attend_fast_supported(const DecodeLaunch& k);
-cudaError_t launch_attend_fast(const DecodeLaunch& k, int sm_count, cudaStream_t s);
-
-// Format-parameterised tensor-core split-K attention (tq_decode_mma.cuh): K code width wk
+// Split-K attention on tensor cores (tq_decode_mma.cuh), parameterised by the formats: K code width wk
 // (q8_0 = 0, turbo K = index bits + 1), V code width wv (q8_0 = 0, turbo-MSE V = index bits),
 // one translation unit per head_dim.
 bool mma_has_d64(int wk, int wv);

@@ -1,4 +1,4 @@
-"""Decode-attention timing on the workload recipes that the benchmark step does not cover.
+"""Decode-attention (and paged encode) timing on the workload recipes that the benchmark step does not cover.
 
     python -m kv_cache_quantization_turbo_gb300.decode_timing --workload paged-batch64-turbo3 --head-dim 128
     python -m kv_cache_quantization_turbo_gb300.decode_timing --workload asym-q8k-turbo2v-needles
@@ -7,7 +7,9 @@ Builds the recipe's compressed cache on cuda:0 with the library's own encoder (s
 inputs from workloads.py), then times whole decode calls (every layer of the recipe, one query
 per sequence and query head) with CUDA events on the launching stream after warm-up calls, and
 prints one JSON line: algorithmic bytes (the compressed K and V of every attended token, once)
-per second.  The caches are several GB, far larger than L2, so no flush is needed between calls.
+per second.  The paged recipe also times the encode of one layer (every token of every sequence,
+K and V, written to its slot in the shuffled pages): fp16 read plus codes written per second.
+The caches are several GB, far larger than L2, so no flush is needed between calls.
 """
 import argparse
 import json
@@ -18,6 +20,19 @@ import torch
 
 from . import tq
 from . import workloads as W
+
+
+def _time(fn, calls, warmup):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(calls):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / calls / 1e3
 
 
 def _decode_fn(ctx, q, kview, vview, layer_begin, lens, max_ctx, block_table=None, max_blocks=0, tau=1e-6):
@@ -62,7 +77,7 @@ def _needles(wl):
                                                                                      vb(wl.v_format)))
     cfg = {"layers": L, "kv_heads": H, "q_heads": Hq, "head_dim": d, "ctx": T, "k_format": wl.k_format,
            "v_format": wl.v_format, "boundary_layers_v": "q8_0", "boundary_layers": boundary}
-    return ctx, (lambda: (fb(), fm())), nbytes, cfg
+    return ctx, (lambda: (fb(), fm())), nbytes, cfg, None
 
 
 def _paged(wl, d):
@@ -81,13 +96,20 @@ def _paged(wl, d):
         v = W.kv_tensor(n_tok, H, d, seed=wl.seed * 1000 + 2 * l + 1, device="cuda")
         st = tq.tq_encode_kv(ctx, kview, k, vview, v, l, 1, n_tok, n_tok * H * d, H * d, slots_d)
         assert st == tq.TQ_OK, tq.tq_status_string(st)
+        if l == 0:
+            k0, v0 = k, v  # layer 0's inputs: the encode timing re-encodes them into the same slots
         del k, v
+
+    def encode_layer0():
+        st = tq.tq_encode_kv(ctx, kview, k0, vview, v0, 0, 1, n_tok, n_tok * H * d, H * d, slots_d)
+        assert st == tq.TQ_OK, tq.tq_status_string(st)
+    enc_bytes = n_tok * H * (2 * 2 * d + tq.tq_vector_bytes(wl.k_format, d) + tq.tq_vector_bytes(wl.v_format, d))
     q = W.normal_tensor((L, B, Hq, d), seed=wl.seed * 1000 + 999, device="cuda")
     f = _decode_fn(ctx, q, kview, vview, 0, lens, int(lens.max()), bt, bt.shape[1])
     nbytes = L * H * n_tok * (tq.tq_vector_bytes(wl.k_format, d) + tq.tq_vector_bytes(wl.v_format, d))
     cfg = {"layers": L, "kv_heads": H, "q_heads": Hq, "head_dim": d, "batch": B, "page_size": P,
            "tokens": n_tok, "max_ctx": int(lens.max()), "k_format": wl.k_format, "v_format": wl.v_format}
-    return ctx, f, nbytes, cfg
+    return ctx, f, nbytes, cfg, (encode_layer0, n_tok, enc_bytes)
 
 
 def main(argv=None):
@@ -100,23 +122,21 @@ def main(argv=None):
     if not torch.cuda.is_available():
         raise SystemExit("decode_timing needs a CUDA device")
     wl = W.WORKLOADS[args.workload]
-    ctx, run, nbytes, cfg = _needles(wl) if args.workload == "asym-q8k-turbo2v-needles" else _paged(wl, args.head_dim)
-    for _ in range(args.warmup):
-        run()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.calls):
-        run()
-    e1.record()
-    torch.cuda.synchronize()
-    dt = e0.elapsed_time(e1) / args.calls / 1e3
+    ctx, run, nbytes, cfg, enc = _needles(wl) if args.workload == "asym-q8k-turbo2v-needles" else \
+        _paged(wl, args.head_dim)
+    dt = _time(run, args.calls, args.warmup)
+    line = {"metric": "decode_attention_bandwidth", "value": round(nbytes / dt / 1e9, 1), "unit": "GB/s",
+            "ms_per_call": round(dt * 1e3, 4), "algorithmic_bytes": int(nbytes), "calls": args.calls,
+            "warmup": args.warmup, "workload": args.workload, "config": cfg, "skip_threshold": 1e-6}
+    if enc is not None:
+        encode_layer0, n_tok, enc_bytes = enc
+        te = _time(encode_layer0, args.calls, args.warmup)
+        line["encode_one_layer"] = {"ms": round(te * 1e3, 4), "tokens_per_s": round(n_tok / te, 1),
+                                    "gb_per_s": round(enc_bytes / te / 1e9, 1), "algorithmic_bytes": int(enc_bytes)}
     st, flags = tq.tq_get_status(ctx)
     assert st == tq.TQ_OK and flags == 0, (st, flags)
     tq.tq_context_destroy(ctx)
-    print(json.dumps({"metric": "decode_attention_bandwidth", "value": round(nbytes / dt / 1e9, 1), "unit": "GB/s",
-                      "ms_per_call": round(dt * 1e3, 4), "algorithmic_bytes": int(nbytes), "calls": args.calls,
-                      "warmup": args.warmup, "workload": args.workload, "config": cfg, "skip_threshold": 1e-6}))
+    print(json.dumps(line))
 
 
 if __name__ == "__main__":
