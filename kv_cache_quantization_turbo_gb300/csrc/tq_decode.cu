@@ -139,9 +139,10 @@ __device__ __forceinline__ long long token_vector(const DecodeArgs& a, const Dev
 }
 
 // ---------------------------------------------------------------------------
-// 2. split-K attention, generic form (any supported format and head_dim):
-//    one warp per CTA; lane = token while scoring, lane = coordinates while
-//    accumulating V.
+// 2. split-K attention on CUDA cores, for what the tensor-core kernel does not
+//    take (9 to 16 query heads per KV head, a turbo-MSE format used as K, block
+//    tables over pages that are not a multiple of 16 tokens): one warp per CTA;
+//    lane = token while scoring, lane = coordinates while accumulating V.
 // ---------------------------------------------------------------------------
 constexpr int kGMax = 16;
 
