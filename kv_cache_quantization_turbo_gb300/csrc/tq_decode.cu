@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(D) qprep_kernel(DecodeKernelArgs ka) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const long long row = blockIdx.x;  // (layer, batch, q head)
   const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
-  if (row == 0 && threadIdx.x == 0) *ka.counter = 0u;  // work counter of the attention kernel that follows
+  if (row == 0 && threadIdx.x < 2) ka.counter[threadIdx.x] = 0u;  // work counters of the attention launches
   if (row >= rows) return;  // block-uniform
   __shared__ float q_s[D];
   float* dst = ka.qprep + row * 2 * D;
@@ -375,11 +375,11 @@ int mma_v_width(const DevView& v) {
   return format_is_turbo(v.format) && !v.has_qjl ? v.code_bits : -1;
 }
 
-// The format-parameterised tensor-core kernel takes this launch: up to 8 query heads per KV head,
+// The format-parameterised tensor-core kernel takes this launch: up to 16 query heads per KV head,
 // pages of a multiple of 16 tokens (or a contiguous cache), an instantiated pair of code widths.
 bool attend_mma_supported(const DecodeKernelArgs& ka, int d) {
   const DecodeArgs& a = ka.a;
-  if (ka.G < 1 || ka.G > 8 || ka.split_tokens % 16 != 0) return false;
+  if (ka.G < 1 || ka.G > 16 || ka.split_tokens % 16 != 0) return false;
   if (a.block_table != nullptr && a.k.page_size % 16 != 0) return false;
   const int wk = mma_k_width(a.k), wv = mma_v_width(a.v);
   if (wk < 0 || wv < 0) return false;
@@ -391,7 +391,7 @@ bool attend_mma_supported(const DecodeKernelArgs& ka, int d) {
   return false;
 }
 
-cudaError_t launch_attend_mma(const DecodeKernelArgs& ka, int d, int sm_count, cudaStream_t s) {
+cudaError_t launch_attend_mma_heads(const DecodeKernelArgs& ka, int d, int sm_count, cudaStream_t s) {
   const int wk = mma_k_width(ka.a.k), wv = mma_v_width(ka.a.v);
   switch (d) {
     case 64: return mma_launch_d64(ka, wk, wv, sm_count, s);
@@ -399,6 +399,20 @@ cudaError_t launch_attend_mma(const DecodeKernelArgs& ka, int d, int sm_count, c
     case 256: return mma_launch_d256(ka, wk, wv, sm_count, s);
   }
   return cudaErrorInvalidValue;
+}
+
+// Up to 8 query heads per KV head: one launch.  9 to 16: two launches over the two halves of each
+// KV head's query heads (each reads the cache once), with their own work counters.
+cudaError_t launch_attend_mma(const DecodeKernelArgs& ka, int d, int sm_count, cudaStream_t s) {
+  if (ka.G <= 8) return launch_attend_mma_heads(ka, d, sm_count, s);
+  DecodeKernelArgs lo = ka, hi = ka;
+  lo.g_off = 0;
+  lo.g_cnt = (ka.G + 1) / 2;
+  hi.g_off = lo.g_cnt;
+  hi.g_cnt = ka.G - lo.g_cnt;
+  hi.counter = ka.counter + 1;
+  const cudaError_t e = launch_attend_mma_heads(lo, d, sm_count, s);
+  return e != cudaSuccess ? e : launch_attend_mma_heads(hi, d, sm_count, s);
 }
 
 template <int D>
@@ -434,6 +448,8 @@ cudaError_t launch_decode(const DevTables& t, const DecodeArgs& a, const DecodeP
   ka.split_tokens = plan.split_tokens;
   ka.n_splits = plan.n_splits;
   ka.G = a.n_q_heads / a.k.H;
+  ka.g_off = 0;
+  ka.g_cnt = ka.G;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   ka.qprep = reinterpret_cast<float*>(ws);
   ka.partial = reinterpret_cast<float*>(ws + (plan.qprep_floats * 4 + 255) / 256 * 256);

@@ -1,7 +1,9 @@
 // Split-K decode attention on tensor cores, parameterised by the cache formats: turbo K with
 // W-bit codes (W - 1 index bits + the QJL sign bit; turbo2/3/4), turbo-MSE V with W-bit indices
-// (turbo2/3/4_mse), and q8_0 K or V, at head_dim 64, 128 or 256, up to 8 query heads per KV head.
-// One partial (m, l, acc) per query row and split, combined afterwards.
+// (turbo2/3/4_mse), and q8_0 K or V, at head_dim 64, 128 or 256, up to 8 query heads per KV head
+// per launch (query heads g_off .. g_off + g_cnt - 1 of each KV head's G; with 9 to 16 the decode
+// call launches it on the two halves).  One partial (m, l, acc) per query row and split, combined
+// afterwards.
 //
 // Why tensor cores: at HBM speed one 16-token tile of one KV head (1888 B for turbo4 / turbo4_mse
 // at d = 128) leaves ~350 warp instructions per SM, and scoring it on CUDA cores takes ~3 G d
@@ -587,8 +589,8 @@ struct MmaWarp {
     for (int q = 0; q < NH; ++q) {
       const int head = 4 * q + (g >> 1);
       const bool lo = g & 1;
-      const bool valid = head < G;
-      const float* qp = k.qprep + (row0 + (valid ? head : 0)) * 2 * D;
+      const bool valid = head < k.g_cnt;
+      const float* qp = k.qprep + (row0 + k.g_off + (valid ? head : 0)) * 2 * D;
       const float fq = valid ? (F::KQ8 ? kLog2e : kLog2e / k.tab.f16_scale[F::KQ8 ? 0 : F::WK - 2]) : 0.f;
       const float fs = valid ? kLog2e * kSqrtHalfPi / (float)D : 0.f;
       const int jq = F::KQ8 ? q : 2 * q;  // product index of the codebook (int8) part
@@ -641,7 +643,7 @@ struct MmaWarp {
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
       const int head = t + 4 * h;
-      if (head >= G) continue;
+      if (head >= k.g_cnt) continue;
       float v[2 * KS];
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) {
@@ -653,7 +655,7 @@ struct MmaWarp {
           v[2 * mt + 1] = oacc[mt][2 + h] * inv_lam;
         }
       }
-      float* dst = k.partial + ((row0 + head) * k.n_splits + split) * (D + 4);
+      float* dst = k.partial + ((row0 + k.g_off + head) * k.n_splits + split) * (D + 4);
       float4* dv = reinterpret_cast<float4*>(dst + 4 + g * (D / 8));
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) dv[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
@@ -757,7 +759,7 @@ template <class F>
 cudaError_t launch_mma(const DecodeLaunch& k, int sm_count, cudaStream_t s) {
   const long long items = (long long)k.a.n_layers * k.a.batch * k.a.k.H * k.n_splits;
   if (items >= (1LL << 32)) return cudaErrorInvalidValue;
-  return k.G <= 4 ? launch_shape<F, true>(k, items, sm_count, s) : launch_shape<F, false>(k, items, sm_count, s);
+  return k.g_cnt <= 4 ? launch_shape<F, true>(k, items, sm_count, s) : launch_shape<F, false>(k, items, sm_count, s);
 }
 
 }  // namespace mmad

@@ -99,9 +99,10 @@ struct DecodeLaunch {
   DecodeArgs a;
   DevTables tab;
   int split_tokens, n_splits, G;
+  int g_off, g_cnt;  // tensor-core kernel: query heads [g_off, g_off + g_cnt) of each KV head's G
   float* qprep;    // [rows][2d]: q' then Sq'
   float* partial;  // [rows][n_splits][d + 4]: m (natural log units), l, -, -, acc[d]
-  unsigned int* counter;  // work-item counter (zeroed by the prologue kernel)
+  unsigned int* counter;  // two work-item counters (zeroed by the prologue kernel)
 };
 
 // Split-K attention on tensor cores (tq_decode_mma.cuh), parameterised by the formats: K code width wk

@@ -331,11 +331,12 @@ def test_decode_tensor_core_format_pairs_paged(ctx, kfmt, vfmt, G):
         assert err.max() < C.ATTN_RTOL, (b, err.max())
 
 
-@pytest.mark.parametrize("G", [1, 3, 6, 8, 16])
+@pytest.mark.parametrize("G", [1, 3, 6, 8, 9, 12, 16])
 def test_decode_gqa_groups(ctx128, G):
     """turbo4 / turbo4_mse, 333 tokens: G 1 and 3 leave column pairs of the high / low query
     layout empty, G 6 leaves two of the second product's pairs empty, G 8 fills both products,
-    and G 16 takes the CUDA-core kernel."""
+    and G 9, 12, 16 run two launches over the halves of each KV head's query heads (5 + 4, 6 + 6,
+    8 + 8)."""
     d, H, T = 128, 2, 333
     ek, ev, kt, vt = _oracle_cache(ctx128, "turbo4", "turbo4_mse", T, H, seed=9, frac=0.01)
     kview = tq.alloc_view("turbo4", d, H, page_size=T, num_pages=1)
