@@ -331,6 +331,31 @@ def test_decode_tensor_core_format_pairs_paged(ctx, kfmt, vfmt, G):
         assert err.max() < C.ATTN_RTOL, (b, err.max())
 
 
+def test_decode_pages_not_a_multiple_of_16_tokens(ctx128):
+    """24-token pages in shuffled order (the CUDA-core attention kernel's block-table path), lengths
+    0, 5, 24, 100, 333, GQA 4, Sparse V at 1e-6; identical codes on both sides."""
+    d, H, G, P = 128, 2, 4, 24
+    lens = np.array([0, 5, 24, 100, 333])
+    bt, npages = W.shuffled_block_table(lens, P, seed=21, extra_pages=2)
+    T = int(lens.sum())
+    ek, ev, kt, vt = _oracle_cache(ctx128, "turbo4", "turbo4_mse", T, H, seed=23, frac=0.01)
+    kview = tq.alloc_view("turbo4", d, H, page_size=P, num_pages=npages)
+    vview = tq.alloc_view("turbo4_mse", d, H, page_size=P, num_pages=npages)
+    slots = np.concatenate([bt[b, np.arange(L) // P] * P + np.arange(L) % P for b, L in enumerate(lens)])
+    C.write_oracle_codes(kview, ek, "turbo4", slots)
+    C.write_oracle_codes(vview, ev, "turbo4_mse", slots)
+    q = W.normal_tensor((1, len(lens), H * G, d), seed=25, device="cuda")
+    out = C.decode(ctx128, q, kview, vview, lens, int(lens.max()), block_table=bt, max_blocks=bt.shape[1], tau=1e-6)
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]])
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert torch.all(out[0, b] == 0)
+            continue
+        sl = slice(starts[b], starts[b] + L)
+        o_full, _ = O.decode_attention(q[0, b].cpu().numpy().astype(np.float64), kt[sl], vt[sl], 1.0 / math.sqrt(d))
+        assert C.rel_err_per_head(out[0, b].cpu().numpy(), o_full).max() < C.ATTN_RTOL
+
+
 @pytest.mark.parametrize("G", [1, 3, 6, 8, 9, 12, 16])
 def test_decode_gqa_groups(ctx128, G):
     """turbo4 / turbo4_mse, 333 tokens: G 1 and 3 leave column pairs of the high / low query
