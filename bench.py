@@ -438,7 +438,7 @@ def main():
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f16-operand/f32-accumulate", "data": "synthetic",
         "config": {"workload": WORKLOAD, "layers": wl.n_layers, "kv_heads": wl.n_kv_heads,
                    "q_heads": wl.n_q_heads, "head_dim": wl.head_dim, "ctx": wl.ctx, "batch": 1,
                    "k_format": wl.k_format, "v_format": wl.v_format, "encode_chunk": wl.encode_chunk,

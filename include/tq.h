@@ -261,8 +261,11 @@ tq_status tq_decode_attention(const tq_context* ctx,
  * the library keeps it until exit); a call whose tq_decode_workspace_bytes()
  * exceeds 16 MiB returns TQ_ERR_WORKSPACE and launches nothing.  The first call
  * on a device looks the array's device address up (with that device current)
- * and should come before any stream capture.  All calls share the array: calls
- * that overlap on the GPU race.  The context's device must be current.
+ * and should come before any stream capture; the address is kept for the life
+ * of the process, so the entry point must not be used on a device after
+ * cudaDeviceReset (the library's module, and the array with it, is gone).  All
+ * calls share the array: calls that overlap on the GPU race.  The context's
+ * device must be current.
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  */
 tq_status tq_decode_attention_static(const tq_context* ctx,

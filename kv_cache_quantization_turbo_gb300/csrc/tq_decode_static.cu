@@ -17,7 +17,9 @@
 // array's name is only a host-side stand-in, so its device address is looked
 // up with cudaGetSymbolAddress, once per device, with that device current, on
 // the first call made on that device (that first call should therefore come
-// before any stream capture).  All calls share the one array and it keeps the
+// before any stream capture).  The address is kept for the life of the process:
+// after cudaDeviceReset the module and the array are unloaded and the entry point
+// must not be used on that device again.  All calls share the one array and it keeps the
 // previous call's contents; nothing in it has to start at zero, because the
 // decode kernels write every value they later read within the same call.
 // Calls that overlap on the GPU (other streams, other host threads) race on it.

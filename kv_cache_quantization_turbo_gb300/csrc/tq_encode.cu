@@ -9,14 +9,17 @@
 // the pages' baselines.
 //
 // Work decomposition
-//   - turbo formats: a vector is held by a group of L = d/32 lanes, each lane owning
-//     32 consecutive coordinates, so a warp encodes 32/L vectors at once.  The sign
-//     flips are applied on the fp16 words, five of the WHT stages run inside a lane
-//     and log2(L) across the group (shuffles), 1/(n sqrt(d)) is applied once;
-//   - the Lloyd-Max index is a binary search over the sorted boundaries (the count
-//     of boundaries <= y, ties included as the definition has it), and each lane
+//   - turbo formats at d = 128: encode_tc_kernel (tensor cores; described at the kernel).
+//     The Lloyd-Max index there is step_index, a sum of saturated FMA steps that equals
+//     the count of boundaries <= y exactly (ties included);
+//   - turbo formats at d = 64 and 256: a vector is held by a group of L = d/32 lanes,
+//     each lane owning 32 consecutive coordinates, so a warp encodes 32/L vectors at
+//     once.  The sign flips are applied on the fp16 words, five of the WHT stages run
+//     inside a lane and log2(L) across the group (shuffles), 1/(n sqrt(d)) is applied
+//     once; the Lloyd-Max index is a binary search over the sorted boundaries (the
+//     count of boundaries <= y, ties included as the definition has it), and each lane
 //     packs its 32 codes into its own w words of the stream and stores them;
-//   - turbo K: a CTA encodes a batch of NV = 8192/d vectors: phase A (stage 1, the
+//   - turbo K at d = 64 / 256: a CTA encodes a batch of NV = 8192/d vectors: phase A (stage 1, the
 //     residual r into shared memory), phase B (the whole CTA: the d x d projection
 //     S r on mma.sync m16n8k16, f16 inputs split into high and low parts,
 //     r_hi s_hi + r_lo s_hi + r_hi s_lo accumulated in fp32, which leaves an error

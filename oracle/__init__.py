@@ -7,6 +7,8 @@ Parity status per function (what pins it, from tests/test_oracle.py):
   quantize                        pinned: brute-force nearest centroid
   turbo_encode / turbo_dequant    pinned: hand-derived d=2 case, QJL sign rule with S = I,
                                   distortion vs Lloyd MSE, compressed-domain score identity
+  qjl_stage                       pinned: through turbo_encode; hand-derived d=2 case with another
+                                  index and a non-symmetric S; linearity in the index
   qjl_inner_product_estimate      pinned: Monte-Carlo unbiasedness and variance bound
   q8_0_encode / q8_0_dequant      pinned: exact integer blocks, half-away ties, error <= delta/2
   minmax_encode / minmax_dequant  pinned: the pages' worked examples (codes 0/8/15, 6/6)

@@ -194,12 +194,28 @@ def turbo_encode(x16: np.ndarray, fmt: str, signs: np.ndarray, S: np.ndarray | N
     idx = quantize(y, b)
     out = {"n16": n.astype(np.float16), "idx": idx, "y": y, "n": n}
     if has_qjl:
-        r = y - c[idx]
-        rn = np.sqrt(np.sum(r * r, axis=-1))
-        proj = r @ np.asarray(S, dtype=np.float64).T
-        out.update({"rnorm16": (n * rn).astype(np.float16), "sigma": proj > 0, "proj": proj,
-                    "r": r})
+        out.update(qjl_stage(y, n, idx, bits, S))
     return out
+
+
+def qjl_stage(y: np.ndarray, n: np.ndarray, idx: np.ndarray, bits: int, S) -> dict:
+    """Stage 2 of a K format for given stage-1 indices ([TQ+] Stage 2 step list, [DEEP] 2.3).
+
+    y [..., d]: the rotated unit vectors; n [...]: their norms; idx [..., d]: the
+    stage-1 indices, whoever chose them (``turbo_encode`` passes its own; a
+    parity check passes the indices a GPU stored, so that the rest of a vector
+    whose index was decided differently inside the 1e-6 band is still checked).
+      1. r = y - c[idx] (residual of the stage-1 reconstruction, unit rotated space);
+      2. rnorm = n * ||r||, stored as fp16;
+      3. sigma_j = [(S r)_j > 0].
+    Returns {"rnorm16", "sigma", "proj" (= S r, fp64), "r"}.
+    """
+    d = y.shape[-1]
+    c, _ = codebook(bits, d)
+    r = y - c[np.asarray(idx)]
+    rn = np.sqrt(np.sum(r * r, axis=-1))
+    proj = r @ np.asarray(S, dtype=np.float64).T
+    return {"rnorm16": (np.asarray(n) * rn).astype(np.float16), "sigma": proj > 0, "proj": proj, "r": r}
 
 
 QJL_CONST = math.sqrt(math.pi / 2.0)

@@ -73,13 +73,16 @@ def near_boundary(y, boundaries):
     return np.min(np.abs(y[..., None] - boundaries), axis=-1) < BAND
 
 
-def check_turbo_codes(fmt, d, gpu_pay, gpu_hdr, enc, exact=False, band_limit=True):
+def check_turbo_codes(fmt, d, gpu_pay, gpu_hdr, enc, exact=False, band_limit=True, S=None):
     """Bit-exact comparison with the band exclusion; returns counts for reporting.
 
-    exact=True: no mismatch at all (inputs whose coordinates are exactly zero on
-    both sides, so the tie rule decides identically).  band_limit=False: the
-    band-population limit, a property of random data, is not applied (inputs
-    constructed to put many coordinates on a boundary)."""
+    Indices are compared with the oracle's.  QJL signs and rnorm (K formats, S required) are
+    compared with the oracle's stage 2 run on the indices the GPU stored (O.qjl_stage): where the
+    two sides decided an index differently inside the band, the residual differs, and every sign
+    and the rnorm of that vector are still checked against what the GPU's own index implies.
+    exact=True: no mismatch at all (inputs whose coordinates are exactly zero on both sides, so
+    the tie rule decides identically).  band_limit=False: the band-population limit, a property
+    of random data, is not applied (inputs constructed to put many coordinates on a boundary)."""
     bits, has_qjl = O.TURBO_FORMATS[fmt]
     codes = unpack_codes(gpu_pay, d, code_bits(fmt))
     idx, sigma = split_turbo(codes, fmt)
@@ -94,19 +97,38 @@ def check_turbo_codes(fmt, d, gpu_pay, gpu_hdr, enc, exact=False, band_limit=Tru
         if band_limit:
             assert band.sum() <= max(BAND_FRACTION * n_el, 3), f"band too populated: {band.sum()} of {n_el}"
     hdr = header_halves(gpu_hdr, 2 if has_qjl else 1)
-    vec_ok = ~mism.any(axis=-1)
     from _layout import f16_ulp_diff
     assert f16_ulp_diff(hdr[..., 0], enc["n16"]).max() <= 1
-    out = {"idx_mismatch": int(mism.sum()), "band": int(band.sum()), "elements": n_el}
+    out = {"idx_mismatch": int(mism.sum()), "band": int(band.sum()), "elements": n_el,
+           "vectors_with_band_index": int(mism.any(axis=-1).sum())}
     if has_qjl:
-        sband = np.abs(enc["proj"]) < BAND
-        smism = (sigma != enc["sigma"]) & vec_ok[..., None]
+        assert S is not None, "the QJL check needs the projection matrix"
+        st = O.qjl_stage(enc["y"], enc["n"], idx, bits, S)
+        sband = np.abs(st["proj"]) < BAND
+        smism = sigma != st["sigma"]
         if exact:
             assert not smism.any(), f"{int(smism.sum())} sign mismatches"
-        assert np.all(sband[smism]), f"{int((smism & ~sband).sum())} sign mismatches outside the band"
-        assert f16_ulp_diff(hdr[..., 1][vec_ok], enc["rnorm16"][vec_ok]).max() <= 1
+        else:
+            assert np.all(sband[smism]), f"{int((smism & ~sband).sum())} sign mismatches outside the band"
+            if band_limit:
+                assert sband.sum() <= max(BAND_FRACTION * n_el, 3), f"sign band too populated: {sband.sum()}"
+        assert f16_ulp_diff(hdr[..., 1], st["rnorm16"]).max() <= 1
         out["sigma_mismatch"] = int(smism.sum())
     return out
+
+
+def gpu_codes(fmt, d, gpu_pay, gpu_hdr):
+    """The stored fields of GPU-written vectors in the oracle's form, so that the oracle can
+    dequantise the GPU's own codes: turbo {"idx", "n16"[, "sigma", "rnorm16"]}; q8_0 (q, delta16)."""
+    if fmt == "q8_0":
+        return gpu_pay.view(np.int8), gpu_hdr.view(np.float16)
+    bits, has_qjl = O.TURBO_FORMATS[fmt]
+    idx, sigma = split_turbo(unpack_codes(gpu_pay, d, code_bits(fmt)), fmt)
+    hdr = header_halves(gpu_hdr, 2 if has_qjl else 1)
+    enc = {"idx": idx, "n16": hdr[..., 0].copy()}
+    if has_qjl:
+        enc.update({"sigma": sigma, "rnorm16": hdr[..., 1].copy()})
+    return enc
 
 
 def write_oracle_codes(view, enc, fmt, slots, layer=0, head=None):
@@ -175,16 +197,10 @@ def rel_err_per_head(got, want):
     return num / den
 
 
-def codes_agree(fmt, d, gpu_pay, enc):
-    """Per vector: do the GPU's stored codes equal the oracle's (indices and QJL signs)?
-
-    Codes may legitimately differ inside the 1e-6 boundary band (check_turbo_codes
-    enforces that); attention parity is then judged only where they agree, because
-    one flipped code of a heavily weighted token moves that head's output."""
-    codes = unpack_codes(gpu_pay, d, code_bits(fmt))
-    idx, sigma = split_turbo(codes, fmt)
-    ok = np.all(idx == enc["idx"], axis=-1)
-    if sigma is not None:
-        ok &= np.all(sigma == enc["sigma"], axis=-1)
-    return ok
-
+def oracle_attention_on_gpu_codes(kfmt, vfmt, d, kpay, khdr, vpay, vhdr, q_rows, signs, S, tau=0.0):
+    """Oracle attention (fp64) over the codes a GPU stored for one KV head's tokens:
+    kpay/khdr/vpay/vhdr [T, 1, bytes] read back from the caches, dequantised by the oracle;
+    q_rows [G, d].  Returns (o_full, o_skip) [G, d]."""
+    kt = oracle_dequant(kfmt, gpu_codes(kfmt, d, kpay, khdr), signs, S)
+    vt = oracle_dequant(vfmt, gpu_codes(vfmt, d, vpay, vhdr), signs, S)
+    return O.decode_attention(np.asarray(q_rows, np.float64), kt, vt, 1.0 / math.sqrt(d), tau)

@@ -1,15 +1,20 @@
 """Parity at the benchmark recipes' full sizes, on sampled (layer, KV head) slices.
 
 Each test builds the whole workload on the GPU (all layers, full context) with
-the library's encoder and checks the codes of sampled slices against the oracle
-(bit-exact outside the 1e-6 boundary band, headers within 1 ulp).  At these
-sizes every slice holds a few coordinates inside the band, where the two sides
-may legitimately decide differently, and one flipped code of a heavily weighted
-token moves its head's output; so attention parity is judged on identical codes:
-the oracle's codes are written into the sampled slices, decode attention runs
-over all layers in one call (the benchmark's launch configuration), and the
-sampled heads must agree with the oracle's fp64 attention within 2e-3.  Inputs
-are regenerated from their seeds on the same device and copied to the host.
+the library's encoder and runs decode attention over all layers in one call
+(the benchmark's launch configuration), twice:
+
+1. on the cache as the GPU encoded it.  The codes of each sampled slice are
+   checked against the oracle (indices bit-exact outside the 1e-6 boundary
+   band, QJL signs and rnorm against the oracle's stage 2 on the GPU's own
+   indices, headers within 1 ulp), and every query head of the slice must
+   match the oracle's fp64 attention over the codes the GPU stored (read back
+   and dequantised by the oracle) within 2e-3;
+2. after the oracle's own codes are written into the sampled slices: every
+   query head of the slice must match the oracle end to end (oracle encode,
+   dequantise, attention) within 2e-3.
+
+Inputs are regenerated from their seeds on the same device and copied to the host.
 """
 import math
 
@@ -25,20 +30,29 @@ import gpu_common as C
 pytestmark = pytest.mark.gpu
 
 
-def _check_and_replace(view, layer, fmt, x16, kvh, slot_ids, signs, S):
-    """Checks the GPU codes of one slice against the oracle, then writes the oracle's codes
-    there.  x16: fp16 [n, d] of KV head kvh at the given slots.  Returns the oracle encoding."""
-    enc = C.oracle_encode(fmt, x16[:, None, :], signs, S)
+def _gpu_slice(view, layer, kvh, slot_ids):
+    """The stored payload and header bytes of KV head kvh at the given slots: [n, 1, bytes]."""
     pay, hdr = C.read_vectors(view, layer)
     pay = C.slot_major(pay, slot_ids, view.page_size)[:, kvh][:, None]
     hdr = C.slot_major(hdr, slot_ids, view.page_size)[:, kvh][:, None]
+    return pay, hdr
+
+
+def _check_codes(view, layer, fmt, x16, kvh, slot_ids, signs, S):
+    """Checks the GPU codes of one slice against the oracle.  x16: fp16 [n, d] of KV head kvh at
+    the given slots.  Returns (oracle encoding, the GPU's codes in the oracle's form)."""
+    enc = C.oracle_encode(fmt, x16[:, None, :], signs, S)
+    pay, hdr = _gpu_slice(view, layer, kvh, slot_ids)
     if fmt == "q8_0":
         np.testing.assert_array_equal(pay.view(np.int8), enc[0])
         np.testing.assert_array_equal(hdr.view(np.float16), enc[1])
     else:
-        C.check_turbo_codes(fmt, view.head_dim, pay, hdr, enc)
+        C.check_turbo_codes(fmt, view.head_dim, pay, hdr, enc, S=S)
+    return enc, C.gpu_codes(fmt, view.head_dim, pay, hdr)
+
+
+def _replace(view, layer, fmt, enc, kvh, slot_ids):
     C.write_oracle_codes(view, enc, fmt, slot_ids, layer=layer, head=kvh)
-    return enc
 
 
 def _attention(q_rows, ek, ev, kfmt, vfmt, signs, S, d, tau=0.0):
@@ -63,6 +77,11 @@ def _within_skip_bound(got, o_full, bound):
     return bool(np.all(dev <= bound + C.ATTN_RTOL * np.linalg.norm(o_full, axis=-1)))
 
 
+def _compare(got, want, what):
+    err = C.rel_err_per_head(got, want)
+    assert err.max() < C.ATTN_RTOL, (what, err.max())
+
+
 def test_llama3_8b_32k_turbo4_bench_configuration():
     """32 layers x 8 KV heads x 32768 tokens, d 128, 32 query heads, turbo4 / turbo4_mse,
     built, re-encoded and decoded exactly as bench.py does (one decode call over all layers)."""
@@ -71,37 +90,56 @@ def test_llama3_8b_32k_turbo4_bench_configuration():
     dev = torch.device("cuda", 0)
     w = bench.build_workload(tq, W, torch, dev)
     wl = w["wl"]
-    d, H, T = wl.head_dim, wl.n_kv_heads, wl.ctx
+    d, H, T, L = wl.head_dim, wl.n_kv_heads, wl.ctx, wl.n_layers
     G = wl.n_q_heads // H
+    scale = 1.0 / math.sqrt(d)
+
+    def decode_full():
+        out = torch.empty_like(w["out"])
+        st = tq.tq_decode_attention(w["ctx"], w["q"], 0, L, 1, wl.n_q_heads, w["kview"], w["vview"], 0,
+                                    w["seq_lens"], T, None, 0, scale, 0.0, w["ws"], w["ws_bytes"], out)
+        assert st == tq.TQ_OK
+        torch.cuda.synchronize()
+        return out
+
     try:
         stream = torch.cuda.current_stream()
         bench.encode_step(tq, w, w["k_chunk"], w["v_chunk"], stream)  # the timed encode (last 4096 tokens)
         torch.cuda.synchronize()
         assert tq.tq_get_status(w["ctx"])[0] == tq.TQ_OK
-        refs = {}
+        # 1. the GPU-encoded cache: the timed decode (Sparse V at 1e-6) and the full one
+        bench.decode_step(tq, w, w["q"], w["out"], stream)
+        torch.cuda.synchronize()
+        out_skip = w["out"].clone()
+        out_full = decode_full()
+        encs = {}
         for layer, kvh in ((0, 3), (31, 6)):
             k = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * layer, device=dev,
                             outlier_frac=wl.outlier_frac)[:, kvh].cpu().numpy()
             v = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * layer + 1, device=dev,
                             outlier_frac=wl.outlier_frac)[:, kvh].cpu().numpy()
-            ek = _check_and_replace(w["kview"], layer, wl.k_format, k, kvh, np.arange(T), w["signs"], w["S"])
-            ev = _check_and_replace(w["vview"], layer, wl.v_format, v, kvh, np.arange(T), w["signs"], w["S"])
+            ek, gk = _check_codes(w["kview"], layer, wl.k_format, k, kvh, np.arange(T), w["signs"], w["S"])
+            ev, gv = _check_codes(w["vview"], layer, wl.v_format, v, kvh, np.arange(T), w["signs"], w["S"])
             q = w["q"][layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
-            refs[layer, kvh] = _attention(q, ek, ev, wl.k_format, wl.v_format, w["signs"], w["S"], d, 1e-6)
-        bench.decode_step(tq, w, w["q"], w["out"], stream)  # the timed decode: Sparse V at 1e-6
+            o_full, bound = _attention(q, gk, gv, wl.k_format, wl.v_format, w["signs"], w["S"], d, 1e-6)
+            heads = slice(kvh * G, (kvh + 1) * G)
+            _compare(out_full[layer, 0, heads].cpu().numpy(), o_full, ("gpu codes", layer, kvh))
+            assert _within_skip_bound(out_skip[layer, 0, heads].cpu().numpy(), o_full, bound)
+            encs[layer, kvh] = (ek, ev, q)
+        # 2. the oracle's codes in the sampled slices
+        for (layer, kvh), (ek, ev, q) in encs.items():
+            _replace(w["kview"], layer, wl.k_format, ek, kvh, np.arange(T))
+            _replace(w["vview"], layer, wl.v_format, ev, kvh, np.arange(T))
+        bench.decode_step(tq, w, w["q"], w["out"], stream)
         torch.cuda.synchronize()
         out_skip = w["out"].clone()
-        out_full = torch.empty_like(w["out"])
-        st = tq.tq_decode_attention(w["ctx"], w["q"], 0, wl.n_layers, 1, wl.n_q_heads, w["kview"], w["vview"], 0,
-                                    w["seq_lens"], T, None, 0, 1.0 / math.sqrt(d), 0.0, w["ws"], w["ws_bytes"],
-                                    out_full)
-        assert st == tq.TQ_OK
-        torch.cuda.synchronize()
+        out_full = decode_full()
         assert tq.tq_get_status(w["ctx"])[0] == tq.TQ_OK
-        for (layer, kvh), (o_full, bound) in refs.items():
-            got = out_full[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
-            assert C.rel_err_per_head(got, o_full).max() < C.ATTN_RTOL
-            assert _within_skip_bound(out_skip[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy(), o_full, bound)
+        for (layer, kvh), (ek, ev, q) in encs.items():
+            o_full, bound = _attention(q, ek, ev, wl.k_format, wl.v_format, w["signs"], w["S"], d, 1e-6)
+            heads = slice(kvh * G, (kvh + 1) * G)
+            _compare(out_full[layer, 0, heads].cpu().numpy(), o_full, ("oracle codes", layer, kvh))
+            assert _within_skip_bound(out_skip[layer, 0, heads].cpu().numpy(), o_full, bound)
     finally:
         tq.tq_context_destroy(w["ctx"])
 
@@ -124,20 +162,26 @@ def test_llama_70b_128k_turbo4_sampled():
             assert st == tq.TQ_OK
             del k, v
         q = W.normal_tensor((L, 1, Hq, d), seed=wl.seed * 1000 + 999, device="cuda")
-        refs = {}
+        out = C.decode(ctx, q, kview, vview, [T], T, tau=0.0)  # the GPU-encoded cache
+        encs = {}
         for layer, kvh in ((40, 5), (79, 1)):
             k = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * layer, device="cuda",
                             outlier_frac=wl.outlier_frac)[:, kvh].cpu().numpy()
             v = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * layer + 1, device="cuda",
                             outlier_frac=wl.outlier_frac)[:, kvh].cpu().numpy()
-            ek = _check_and_replace(kview, layer, wl.k_format, k, kvh, np.arange(T), ctx.signs, ctx.S)
-            ev = _check_and_replace(vview, layer, wl.v_format, v, kvh, np.arange(T), ctx.signs, ctx.S)
-            refs[layer, kvh] = _attention(q[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy(), ek, ev, wl.k_format,
-                                          wl.v_format, ctx.signs, ctx.S, d)[0]
+            ek, gk = _check_codes(kview, layer, wl.k_format, k, kvh, np.arange(T), ctx.signs, ctx.S)
+            ev, gv = _check_codes(vview, layer, wl.v_format, v, kvh, np.arange(T), ctx.signs, ctx.S)
+            qr = q[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
+            o_full = _attention(qr, gk, gv, wl.k_format, wl.v_format, ctx.signs, ctx.S, d)[0]
+            _compare(out[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy(), o_full, ("gpu codes", layer, kvh))
+            encs[layer, kvh] = (ek, ev, qr)
+        for (layer, kvh), (ek, ev, qr) in encs.items():
+            _replace(kview, layer, wl.k_format, ek, kvh, np.arange(T))
+            _replace(vview, layer, wl.v_format, ev, kvh, np.arange(T))
         out = C.decode(ctx, q, kview, vview, [T], T, tau=0.0)
-        for (layer, kvh), o_full in refs.items():
-            got = out[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
-            assert C.rel_err_per_head(got, o_full).max() < C.ATTN_RTOL
+        for (layer, kvh), (ek, ev, qr) in encs.items():
+            o_full = _attention(qr, ek, ev, wl.k_format, wl.v_format, ctx.signs, ctx.S, d)[0]
+            _compare(out[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy(), o_full, ("oracle codes", layer, kvh))
         assert tq.tq_get_status(ctx.h)[0] == tq.TQ_OK
     finally:
         ctx.close()
@@ -169,23 +213,39 @@ def test_asymmetric_boundary_layers_needles_sampled():
             else:
                 st = tq.tq_encode_kv(ctx.h, km, k, vm, v, middle.index(l), 1, T, T * H * d, H * d)
             assert st == tq.TQ_OK
-        refs = {}
+
+        def decode_all():
+            return (C.decode(ctx, qs[boundary], kb, vb, [T], T, tau=1e-6),
+                    C.decode(ctx, qs[middle], km, vm, [T], T, tau=1e-6))
+
+        def pick(outs, layer, kvh):
+            o = outs[0][boundary.index(layer)] if layer in wl.v_format_layers else outs[1][middle.index(layer)]
+            return o[0, kvh * G:(kvh + 1) * G].cpu().numpy()
+
+        outs = decode_all()  # the GPU-encoded cache
+        encs = {}
         for layer, kvh in ((1, 2), (30, 0)):
             k, _, _ = W.needle_workload(T, H, Hq, d, seed=wl.seed * 1000 + 2 * layer, device="cuda")
             v = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * layer + 1, device="cuda")
             vfmt = wl.v_format_layers.get(layer, wl.v_format)
             kv_, vv_, li = (kb, vb, boundary.index(layer)) if vfmt == "q8_0" else (km, vm, middle.index(layer))
-            ek = _check_and_replace(kv_, li, "q8_0", k[:, kvh].cpu().numpy(), kvh, np.arange(T), ctx.signs, ctx.S)
-            ev = _check_and_replace(vv_, li, vfmt, v[:, kvh].cpu().numpy(), kvh, np.arange(T), ctx.signs, ctx.S)
-            refs[layer, kvh] = _attention(qs[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy(), ek, ev, "q8_0", vfmt,
-                                          ctx.signs, ctx.S, d, 1e-6)
-        out_b = C.decode(ctx, qs[boundary], kb, vb, [T], T, tau=1e-6)
-        out_m = C.decode(ctx, qs[middle], km, vm, [T], T, tau=1e-6)
-        for (layer, kvh), (o_full, bound) in refs.items():
-            got = out_b[boundary.index(layer)] if layer in wl.v_format_layers else out_m[middle.index(layer)]
-            got = got[0, kvh * G:(kvh + 1) * G].cpu().numpy()
+            ek, gk = _check_codes(kv_, li, "q8_0", k[:, kvh].cpu().numpy(), kvh, np.arange(T), ctx.signs, ctx.S)
+            ev, gv = _check_codes(vv_, li, vfmt, v[:, kvh].cpu().numpy(), kvh, np.arange(T), ctx.signs, ctx.S)
+            qr = qs[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
+            o_full, bound = _attention(qr, gk, gv, "q8_0", vfmt, ctx.signs, ctx.S, d, 1e-6)
+            got = pick(outs, layer, kvh)
             # peaked softmax: what Sparse V drops is far below the parity tolerance
-            assert C.rel_err_per_head(got, o_full).max() < C.ATTN_RTOL
+            _compare(got, o_full, ("gpu codes", layer, kvh))
+            assert _within_skip_bound(got, o_full, bound)
+            encs[layer, kvh] = (kv_, vv_, li, vfmt, ek, ev, qr)
+        for (layer, kvh), (kv_, vv_, li, vfmt, ek, ev, qr) in encs.items():
+            _replace(kv_, li, "q8_0", ek, kvh, np.arange(T))
+            _replace(vv_, li, vfmt, ev, kvh, np.arange(T))
+        outs = decode_all()
+        for (layer, kvh), (kv_, vv_, li, vfmt, ek, ev, qr) in encs.items():
+            o_full, bound = _attention(qr, ek, ev, "q8_0", vfmt, ctx.signs, ctx.S, d, 1e-6)
+            got = pick(outs, layer, kvh)
+            _compare(got, o_full, ("oracle codes", layer, kvh))
             assert _within_skip_bound(got, o_full, bound)
     finally:
         ctx.close()
@@ -217,20 +277,30 @@ def test_paged_batch64_turbo3_sampled(d):
             del k, v
         q = W.normal_tensor((L, B, Hq, d), seed=wl.seed * 1000 + 999, device="cuda")
         offs = np.concatenate([[0], np.cumsum(lens)])
-        refs = {}
+
+        def decode():
+            return C.decode(ctx, q, kview, vview, lens, int(lens.max()), block_table=bt, max_blocks=bt.shape[1])
+
+        out = decode()  # the GPU-encoded cache
+        encs = {}
         for layer, b, kvh in ((3, 0, 1), (17, 37, 7)):
             sl = slots[offs[b]:offs[b + 1]]
             k = W.kv_tensor(T_all, H, d, seed=wl.seed * 1000 + 2 * layer, device="cuda")[offs[b]:offs[b + 1], kvh]
             v = W.kv_tensor(T_all, H, d, seed=wl.seed * 1000 + 2 * layer + 1, device="cuda")[offs[b]:offs[b + 1],
                                                                                                  kvh]
-            ek = _check_and_replace(kview, layer, wl.k_format, k.cpu().numpy(), kvh, sl, ctx.signs, ctx.S)
-            ev = _check_and_replace(vview, layer, wl.v_format, v.cpu().numpy(), kvh, sl, ctx.signs, ctx.S)
-            refs[layer, b, kvh] = _attention(q[layer, b, kvh * G:(kvh + 1) * G].cpu().numpy(), ek, ev, wl.k_format,
-                                             wl.v_format, ctx.signs, ctx.S, d)[0]
-        out = C.decode(ctx, q, kview, vview, lens, int(lens.max()), block_table=bt, max_blocks=bt.shape[1])
-        for (layer, b, kvh), o_full in refs.items():
-            got = out[layer, b, kvh * G:(kvh + 1) * G].cpu().numpy()
-            assert C.rel_err_per_head(got, o_full).max() < C.ATTN_RTOL
+            ek, gk = _check_codes(kview, layer, wl.k_format, k.cpu().numpy(), kvh, sl, ctx.signs, ctx.S)
+            ev, gv = _check_codes(vview, layer, wl.v_format, v.cpu().numpy(), kvh, sl, ctx.signs, ctx.S)
+            qr = q[layer, b, kvh * G:(kvh + 1) * G].cpu().numpy()
+            o_full = _attention(qr, gk, gv, wl.k_format, wl.v_format, ctx.signs, ctx.S, d)[0]
+            _compare(out[layer, b, kvh * G:(kvh + 1) * G].cpu().numpy(), o_full, ("gpu codes", layer, b, kvh))
+            encs[layer, b, kvh] = (sl, ek, ev, qr)
+        for (layer, b, kvh), (sl, ek, ev, qr) in encs.items():
+            _replace(kview, layer, wl.k_format, ek, kvh, sl)
+            _replace(vview, layer, wl.v_format, ev, kvh, sl)
+        out = decode()
+        for (layer, b, kvh), (sl, ek, ev, qr) in encs.items():
+            o_full = _attention(qr, ek, ev, wl.k_format, wl.v_format, ctx.signs, ctx.S, d)[0]
+            _compare(out[layer, b, kvh * G:(kvh + 1) * G].cpu().numpy(), o_full, ("oracle codes", layer, b, kvh))
         st, flags = tq.tq_get_status(ctx.h)
         assert st == tq.TQ_OK, flags
     finally:

@@ -175,6 +175,44 @@ def test_turbo_encode_hand_example_d2():
     np.testing.assert_allclose(xv[0], [0.0, 5 * 2 * 0.564189612865448 / math.sqrt(2)], atol=1e-9)
 
 
+def test_qjl_stage_on_given_indices_hand_example_d2():
+    # The d = 2 case above with the stage-1 indices (1, 1) instead of the encoder's (0, 1), as a
+    # GPU that decided the first coordinate the other way would store them.  By hand:
+    # r = y - (c, c) = (-0.14142135624 - 0.56418961287, 0.98994949366 - 0.56418961287)
+    #   = (-0.70561096911, 0.42575988079); ||r||^2 = 0.49788684 + 0.18127148 = 0.67915832,
+    # ||r|| = 0.82411062; rnorm = 5 ||r|| = 4.1205531 -> fp16 1055 * 2^-8 = 4.12109375.
+    # S = [[1, 2], [0, -1]] (row j = projection j): S r = (r0 + 2 r1, -r1) = (0.14590879, -0.42575988),
+    # sigma = (1, 0); the transposed product would give (-0.706, -1.837), sigma = (0, 0).
+    y = np.array([[-0.2, 1.4]]) / math.sqrt(2)
+    S = np.array([[1.0, 2.0], [0.0, -1.0]])
+    st = O.qjl_stage(y, np.array([5.0]), np.array([[1, 1]]), 1, S)
+    np.testing.assert_allclose(st["r"][0], [-0.70561096911, 0.42575988079], atol=1e-10)
+    assert float(st["rnorm16"][0]) == 4.12109375
+    np.testing.assert_allclose(st["proj"][0], [0.14590879, -0.42575988], atol=1e-7)
+    np.testing.assert_array_equal(st["sigma"][0], [True, False])
+
+
+def test_qjl_stage_index_change_moves_residual_and_projection_linearly():
+    # Changing the stored index of coordinate i from a to b changes the residual by
+    # (c[a] - c[b]) e_i and the projection by (c[a] - c[b]) S[:, i] (linearity of both steps).
+    rng = np.random.default_rng(3)
+    d, bits = 64, 3
+    y = rng.standard_normal((5, d)) / math.sqrt(d)
+    S = rng.standard_normal((d, d))
+    c, b = O.codebook(bits, d)
+    idx = O.quantize(y, b)
+    base = O.qjl_stage(y, np.ones(5), idx, bits, S)
+    for v, i in ((0, 3), (2, 40), (4, 63)):
+        moved = idx.copy()
+        moved[v, i] = (idx[v, i] + 1) % (1 << bits)
+        st = O.qjl_stage(y, np.ones(5), moved, bits, S)
+        delta = c[idx[v, i]] - c[moved[v, i]]
+        np.testing.assert_allclose(st["r"][v] - base["r"][v], delta * np.eye(d)[i], atol=1e-15)
+        np.testing.assert_allclose(st["proj"][v] - base["proj"][v], delta * S[:, i], atol=1e-12)
+        others = np.arange(5) != v
+        np.testing.assert_array_equal(st["proj"][others], base["proj"][others])
+
+
 def test_qjl_sign_rule_identity_projection():
     # With S = I the sketch is the sign pattern of the residual; exact zero -> bit 0
     rng = np.random.default_rng(5)
