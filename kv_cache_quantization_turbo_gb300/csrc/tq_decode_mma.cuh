@@ -122,17 +122,20 @@ constexpr int kSmemLimit = 227 * 1024;
 template <class F, bool HILO>
 struct Shape {
   static constexpr int NQ = HILO ? 1 : 2;
+  // Tiles a warp works on at once: two (two independent chains of loads, lookups and products,
+  // one query-fragment read for both) where the registers allow it, that is with up to 4 query
+  // heads per KV head at d <= 128, run with 12 warps of up to 168 registers; else one.
+  static constexpr int NT = (HILO && F::D <= 128) ? 2 : 1;
   static constexpr int QfBytes = F::KS * 256 * (F::KQ8 ? 1 : 2) * NQ;
-  static constexpr int PsBytes = 512;
+  static constexpr int PsBytes = 512 * NT;
   static constexpr int Block = PsBytes + QfBytes;
   static constexpr int smem(int warps) {
     const int packed = (int)(F::Big + F::Small) + warps * Block + ((int)F::Small > Block ? (int)F::Small : Block);
     const int gap = (int)(2 * F::Big + F::Small);
     return packed > gap ? packed : gap;
   }
-  static constexpr int Warps = smem(F::D == 256 ? 8 : 16) <= kSmemLimit ? (F::D == 256 ? 8 : 16)
-                               : smem(F::D == 256 ? 4 : 8) <= kSmemLimit ? (F::D == 256 ? 4 : 8)
-                                                                          : (F::D == 256 ? 2 : 4);
+  static constexpr int W0 = F::D == 256 ? 8 : (NT == 2 ? 12 : 16);
+  static constexpr int Warps = smem(W0) <= kSmemLimit ? W0 : smem(W0 / 2) <= kSmemLimit ? W0 / 2 : W0 / 4;
   static constexpr int Threads = 32 * Warps;
   static constexpr int Smem = smem(Warps);
   static_assert(Smem <= kSmemLimit, "shared memory");
@@ -178,6 +181,7 @@ __device__ __forceinline__ uint32_t run_addr(const uint32_t (&r)[NR], int p, uin
   if (N == 8 && SH == 8 && (off & 7) == 0) return __byte_perm(r[wi], base, 0x7604u | ((uint32_t)(off >> 3) << 4));
   uint32_t x;
   if (off + N <= 32) x = off >= SH ? (r[wi] >> (off - SH)) : (r[wi] << (SH - off));
+  else if (off >= SH) x = __funnelshift_r(r[wi], r[wi + 1 < NR ? wi + 1 : wi], off - SH);
   else x = __funnelshift_r(r[wi], r[wi + 1 < NR ? wi + 1 : wi], off) << SH;
   return (x & (((1u << N) - 1u) << SH)) | base;
 }
@@ -216,6 +220,8 @@ struct MmaWarp {
 
   int layer, b, kvh, ntiles, last_valid;
   Cursor c;
+  KTile kn[2];  // the next pair's K and V, loaded one phase ahead (pipelined pair steps)
+  VTile vn[2];
   float oacc[KS][4];
   float m[NH], l[NH];
 
@@ -253,43 +259,45 @@ struct MmaWarp {
     pf_h = pg16 && ((reinterpret_cast<uintptr_t>(a.k.header) | reinterpret_cast<uintptr_t>(a.v.header)) & 15) == 0;
   }
 
-  __device__ __forceinline__ void set_page() {
+  __device__ __forceinline__ void set_page(Cursor& cu) {
     const DecodeArgs& a = k.a;
     long long page = b;
-    c.ok = true;
+    cu.ok = true;
     if (a.block_table) {
-      page = a.block_table[(long long)b * a.max_blocks_per_seq + c.page_ord];
+      page = a.block_table[(long long)b * a.max_blocks_per_seq + cu.page_ord];
       if (page < 0 || page >= a.k.num_pages) {
         if (lane == 0) atomicOr(k.tab.status, kFlagBlockTable);
-        c.ok = false;
+        cu.ok = false;
         page = 0;
       }
     }
-    const long long base = (((long long)layer * a.k.num_pages + page) * a.k.H + kvh) * a.k.page_size + c.in_page;
-    c.kp = a.k.payload + (base + g) * F::KPay + kto;
-    c.kh = a.k.header + (base + g) * F::KHdr;
-    c.vp = a.v.payload + (base + t) * F::VPay + vgo;
-    c.vh = F::VQ8 ? a.v.header + (base + t) * F::VHdr + vhdr : a.v.header + (base + g) * F::VHdr;
+    const long long base = (((long long)layer * a.k.num_pages + page) * a.k.H + kvh) * a.k.page_size + cu.in_page;
+    cu.kp = a.k.payload + (base + g) * F::KPay + kto;
+    cu.kh = a.k.header + (base + g) * F::KHdr;
+    cu.vp = a.v.payload + (base + t) * F::VPay + vgo;
+    cu.vh = F::VQ8 ? a.v.header + (base + t) * F::VHdr + vhdr : a.v.header + (base + g) * F::VHdr;
   }
 
-  __device__ __forceinline__ void advance() {
-    c.in_page += 16;
-    if (c.in_page == k.a.k.page_size) {
-      c.in_page = 0;
-      ++c.page_ord;
-      set_page();
+  __device__ __forceinline__ void advance(Cursor& cu) {
+    cu.in_page += 16;
+    if (cu.in_page == k.a.k.page_size) {
+      cu.in_page = 0;
+      ++cu.page_ord;
+      set_page(cu);
     } else {
-      c.kp += 16 * F::KPay;
-      c.kh += 16 * F::KHdr;
-      c.vp += 16 * F::VPay;
-      c.vh += 16 * F::VHdr;
+      cu.kp += 16 * F::KPay;
+      cu.kh += 16 * F::KHdr;
+      cu.vp += 16 * F::VPay;
+      cu.vh += 16 * F::VHdr;
     }
   }
 
   // Rows at or beyond nvalid (ragged last tile) re-read row nvalid - 1; their scores are masked.
-  __device__ __forceinline__ void load_k(KTile& K, int nvalid) {
+  // FULL: a whole tile, every row offset a constant.
+  template <bool FULL>
+  __device__ __forceinline__ void load_k(KTile& K, const Cursor& c, int nvalid) {
     int da = 0, db = 8;
-    if (nvalid < 16) {
+    if (!FULL) {
       da = min(g, nvalid - 1) - g;
       db = min(g + 8, nvalid - 1) - g;
     }
@@ -313,11 +321,12 @@ struct MmaWarp {
     }
   }
 
-  __device__ __forceinline__ void load_v(VTile& V, int nvalid) {
+  template <bool FULL>
+  __device__ __forceinline__ void load_v(VTile& V, const Cursor& c, int nvalid) {
     const int rows[4] = {t, t + 8, t + 4, t + 12};
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const int dr = nvalid < 16 ? min(rows[r], nvalid - 1) - t : rows[r] - t;
+      const int dr = !FULL ? min(rows[r], nvalid - 1) - t : rows[r] - t;
       const unsigned char* p = c.vp + dr * F::VPay;
       if constexpr (F::VQ8 || F::VLoad == 1 || !F::VShift) {
         load_words<F::VLoad, F::VVec>(V.w[r], p, pol);
@@ -330,7 +339,7 @@ struct MmaWarp {
       uint32_t s[4];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int dr = nvalid < 16 ? min(rows[r], nvalid - 1) - t : rows[r] - t;
+        const int dr = !FULL ? min(rows[r], nvalid - 1) - t : rows[r] - t;
         s[r] = ld_stream_u16(c.vh + dr * F::VHdr, pol);
       }
       V.h0 = s[0] | (s[1] << 16);
@@ -341,8 +350,8 @@ struct MmaWarp {
         for (int j = 0; j < F::VLoad; ++j) V.w[r][j] ^= 0x80808080u;
       }
     } else {
-      const int da = nvalid < 16 ? min(g, nvalid - 1) - g : 0;
-      const int db = nvalid < 16 ? min(g + 8, nvalid - 1) - g : 8;
+      const int da = !FULL ? min(g, nvalid - 1) - g : 0;
+      const int db = !FULL ? min(g + 8, nvalid - 1) - g : 8;
       V.h0 = ld_stream_u16(c.vh + da * F::VHdr, pol) | (ld_stream_u16(c.vh + db * F::VHdr, pol) << 16);
       V.h1 = 0;
     }
@@ -388,49 +397,71 @@ struct MmaWarp {
     }
   }
 
-  // Score products of a tile: cc[q] = codebook (or int8) part, cs[q] = QJL part of heads
-  // 4q .. 4q + 3 (columns 2h / 2h + 1 = high / low part of head 4q + h).  Query fragments of
-  // product j (turbo: 2q = codebook, 2q + 1 = QJL; q8_0: q) and step ch at qf + 256 (KS j + ch).
-  __device__ __forceinline__ void score(const KTile& K, float (&cc)[NH][4], float (&cs)[NH][4]) {
+  // Score products of NT tiles: cc[j][q] = codebook (or int8) part, cs[j][q] = QJL part of tile j
+  // and heads 4q .. 4q + 3 (columns 2h / 2h + 1 = high / low part of head 4q + h).  Query
+  // fragments of head block q and step ch (read once for all NT tiles): turbo K at
+  // qf + 512 (KS q + ch), 16 bytes a lane (the q' pair, then the S q' pair); q8_0 at
+  // qf + 256 (KS q + ch), 8 bytes a lane.  A turbo K table entry holds the codebook pair of each
+  // lane at lane * 4 and the sign pair at 128 + lane * 4, so both reads of a lookup share one
+  // address and land in the product's operand registers directly.
+  template <int NT>
+  __device__ __forceinline__ void score(const KTile (&K)[NT], float (&cc)[NT][NH][4], float (&cs)[NT][NH][4]) {
     if constexpr (F::KQ8) {
 #pragma unroll
       for (int blk = 0; blk < D / 32; ++blk) {
-        const uint32_t xa0 = K.a[2 * blk] ^ 0x80808080u, xa1 = K.a[2 * blk + 1] ^ 0x80808080u;
-        const uint32_t xb0 = K.b[2 * blk] ^ 0x80808080u, xb1 = K.b[2 * blk + 1] ^ 0x80808080u;
-        const uint32_t a00 = i8x2_to_h2<0x4140>(xa0), a01 = i8x2_to_h2<0x4140>(xb0);
-        const uint32_t a02 = i8x2_to_h2<0x4342>(xa0), a03 = i8x2_to_h2<0x4342>(xb0);
-        const uint32_t a10 = i8x2_to_h2<0x4140>(xa1), a11 = i8x2_to_h2<0x4140>(xb1);
-        const uint32_t a12 = i8x2_to_h2<0x4342>(xa1), a13 = i8x2_to_h2<0x4342>(xb1);
-        const int sh = 16 * (blk & 1);
-        const float da = __half2float(__ushort_as_half((unsigned short)(K.ha[blk >> 1] >> sh)));
-        const float db = __half2float(__ushort_as_half((unsigned short)(K.hb[blk >> 1] >> sh)));
+        uint2 f0[NH], f1[NH];
 #pragma unroll
         for (int q = 0; q < NH; ++q) {
-          const uint2 f0 = lds64(qf + 256 * (KS * q + 2 * blk)), f1 = lds64(qf + 256 * (KS * q + 2 * blk + 1));
-          float c[4];
-          mma_16816_zc(c, a00, a01, a02, a03, f0.x, f0.y);
-          mma_16816(c, a10, a11, a12, a13, f1.x, f1.y);
-          cc[q][0] = fmaf(da, c[0], cc[q][0]);
-          cc[q][1] = fmaf(da, c[1], cc[q][1]);
-          cc[q][2] = fmaf(db, c[2], cc[q][2]);
-          cc[q][3] = fmaf(db, c[3], cc[q][3]);
+          f0[q] = lds64(qf + 256 * (KS * q + 2 * blk));
+          f1[q] = lds64(qf + 256 * (KS * q + 2 * blk + 1));
+        }
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const uint32_t xa0 = K[j].a[2 * blk] ^ 0x80808080u, xa1 = K[j].a[2 * blk + 1] ^ 0x80808080u;
+          const uint32_t xb0 = K[j].b[2 * blk] ^ 0x80808080u, xb1 = K[j].b[2 * blk + 1] ^ 0x80808080u;
+          const uint32_t a00 = i8x2_to_h2<0x4140>(xa0), a01 = i8x2_to_h2<0x4140>(xb0);
+          const uint32_t a02 = i8x2_to_h2<0x4342>(xa0), a03 = i8x2_to_h2<0x4342>(xb0);
+          const uint32_t a10 = i8x2_to_h2<0x4140>(xa1), a11 = i8x2_to_h2<0x4140>(xb1);
+          const uint32_t a12 = i8x2_to_h2<0x4342>(xa1), a13 = i8x2_to_h2<0x4342>(xb1);
+          const int sh = 16 * (blk & 1);
+          const float da = __half2float(__ushort_as_half((unsigned short)(K[j].ha[blk >> 1] >> sh)));
+          const float db = __half2float(__ushort_as_half((unsigned short)(K[j].hb[blk >> 1] >> sh)));
+#pragma unroll
+          for (int q = 0; q < NH; ++q) {
+            float c[4];
+            mma_16816_zc(c, a00, a01, a02, a03, f0[q].x, f0[q].y);
+            mma_16816(c, a10, a11, a12, a13, f1[q].x, f1[q].y);
+            cc[j][q][0] = fmaf(da, c[0], cc[j][q][0]);
+            cc[j][q][1] = fmaf(da, c[1], cc[j][q][1]);
+            cc[j][q][2] = fmaf(db, c[2], cc[j][q][2]);
+            cc[j][q][3] = fmaf(db, c[3], cc[j][q][3]);
+          }
         }
       }
     } else {
       constexpr int N = 2 * F::WK;
-      uint32_t ra[F::KRun], rb[F::KRun];
-      make_run<F::KLoad, F::KRun, F::KShift>(K.a, ra, ksh);
-      make_run<F::KLoad, F::KRun, F::KShift>(K.b, rb, ksh);
+      uint32_t ra[NT][F::KRun], rb[NT][F::KRun];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        make_run<F::KLoad, F::KRun, F::KShift>(K[j].a, ra[j], ksh);
+        make_run<F::KLoad, F::KRun, F::KShift>(K[j].b, rb[j], ksh);
+      }
 #pragma unroll
       for (int ch = 0; ch < KS; ++ch) {
         const int p = 4 * ch * F::WK;
-        const uint2 ea0 = lds64(run_addr<N, 8>(ra, p, ylk)), ea1 = lds64(run_addr<N, 8>(ra, p + N, ylk));
-        const uint2 eb0 = lds64(run_addr<N, 8>(rb, p, ylk)), eb1 = lds64(run_addr<N, 8>(rb, p + N, ylk));
+        uint4 f[NH];
 #pragma unroll
-        for (int q = 0; q < NH; ++q) {
-          const uint2 fq = lds64(qf + 256 * (KS * 2 * q + ch)), fs = lds64(qf + 256 * (KS * (2 * q + 1) + ch));
-          mma_16816(cc[q], ea0.x, eb0.x, ea1.x, eb1.x, fq.x, fq.y);
-          mma_16816(cs[q], ea0.y, eb0.y, ea1.y, eb1.y, fs.x, fs.y);
+        for (int q = 0; q < NH; ++q) f[q] = lds128(qf + 512 * (KS * q + ch));  // q' high/low, then S q'
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const uint32_t aa0 = run_addr<N, 8>(ra[j], p, ylk), aa1 = run_addr<N, 8>(ra[j], p + N, ylk);
+          const uint32_t ab0 = run_addr<N, 8>(rb[j], p, ylk), ab1 = run_addr<N, 8>(rb[j], p + N, ylk);
+#pragma unroll
+          for (int q = 0; q < NH; ++q) {
+            mma_16816(cc[j][q], lds32(aa0), lds32(ab0), lds32(aa1), lds32(ab1), f[q].x, f[q].y);
+            mma_16816(cs[j][q], lds32(aa0 + 128), lds32(ab0 + 128), lds32(aa1 + 128), lds32(ab1 + 128), f[q].z,
+                      f[q].w);
+          }
         }
       }
     }
@@ -469,48 +500,70 @@ struct MmaWarp {
     }
   }
 
-  // One tile at the cursor (the caller advances the cursor afterwards).
-  template <int BUF>
-  __device__ __forceinline__ void step(int tile) {
-    const int nvalid = tile == ntiles - 1 ? last_valid : 16;
-    if (!c.ok) {  // warp-uniform: the tile's page was out of range
-      __syncwarp();
-      return;
-    }
-    KTile kc;
-    load_k(kc, nvalid);
-    float cc[NH][4], cs[NH][4];
+  // NT tiles at the cursors cu[0 .. NT - 1] (consecutive tiles of the work item, pages in range);
+  // the last one holds nlast valid rows (a whole tile when FULLLAST).  P' tiles at kBuf + 256 j
+  // in the warp's P' block.  Whole tiles run with constant row offsets.
+  template <int NT, bool FULLLAST>
+  __device__ __forceinline__ void step_tiles(const Cursor (&cu)[NT], int nlast, uint32_t kBuf) {
+    KTile kc[NT];
+    VTile vc[NT];
 #pragma unroll
-    for (int q = 0; q < NH; ++q) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) cc[q][e] = cs[q][e] = 0.f;
+    for (int j = 0; j < NT; ++j) {
+      if (j < NT - 1 || FULLLAST) load_k<true>(kc[j], cu[j], 16);
+      else load_k<false>(kc[j], cu[j], nlast);
     }
-    score(kc, cc, cs);
-    VTile vc;
-    load_v(vc, nvalid);
+    // Up to 4 query heads: V loads in flight with K's (one load latency per tile); with two
+    // products per part the registers are short, and V is loaded after the score products.
+    if constexpr (HILO) {
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        if (j < NT - 1 || FULLLAST) load_v<true>(vc[j], cu[j], 16);
+        else load_v<false>(vc[j], cu[j], nlast);
+      }
+    }
+    float cc[NT][NH][4], cs[NT][NH][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+      for (int q = 0; q < NH; ++q) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cc[j][q][e] = cs[j][q][e] = 0.f;
+      }
+    }
+    score<NT>(kc, cc, cs);
+    if constexpr (!HILO) {
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        if (j < NT - 1 || FULLLAST) load_v<true>(vc[j], cu[j], 16);
+        else load_v<false>(vc[j], cu[j], nlast);
+      }
+    }
 
     // thread (g, t) and head slot h (head t + 4h): entries 0, 1 of product h = token g, the
     // high and low parts; entries 2, 3 = token g + 8.
-    float s[NH][2];
-    if constexpr (F::KQ8) {
+    float s[NT][NH][2];
 #pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        s[h][0] = cc[h][0] + cc[h][1];
-        s[h][1] = cc[h][2] + cc[h][3];
-      }
-    } else {
-      const float2 hA = __half22float2(u32_as_h2(kc.ha[0])), hB = __half22float2(u32_as_h2(kc.hb[0]));
+    for (int j = 0; j < NT; ++j) {
+      if constexpr (F::KQ8) {
 #pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        s[h][0] = fmaf(hA.x, cc[h][0] + cc[h][1], hA.y * (cs[h][0] + cs[h][1]));
-        s[h][1] = fmaf(hB.x, cc[h][2] + cc[h][3], hB.y * (cs[h][2] + cs[h][3]));
+        for (int h = 0; h < NH; ++h) {
+          s[j][h][0] = cc[j][h][0] + cc[j][h][1];
+          s[j][h][1] = cc[j][h][2] + cc[j][h][3];
+        }
+      } else {
+        const float2 hA = __half22float2(u32_as_h2(kc[j].ha[0])), hB = __half22float2(u32_as_h2(kc[j].hb[0]));
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          s[j][h][0] = fmaf(hA.x, cc[j][h][0] + cc[j][h][1], hA.y * (cs[j][h][0] + cs[j][h][1]));
+          s[j][h][1] = fmaf(hB.x, cc[j][h][2] + cc[j][h][3], hB.y * (cs[j][h][2] + cs[j][h][3]));
+        }
       }
     }
-    if (nvalid < 16) {
+    if (!FULLLAST) {
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
-        if (g >= nvalid) s[h][0] = -INFINITY;
-        if (g + 8 >= nvalid) s[h][1] = -INFINITY;
+        if (g >= nlast) s[NT - 1][h][0] = -INFINITY;
+        if (g + 8 >= nlast) s[NT - 1][h][1] = -INFINITY;
       }
     }
 
@@ -518,25 +571,36 @@ struct MmaWarp {
     {
       float mx[NH];
 #pragma unroll
-      for (int h = 0; h < NH; ++h) mx[h] = fmaxf(s[h][0], s[h][1]);
+      for (int h = 0; h < NH; ++h) {
+        mx[h] = fmaxf(s[0][h][0], s[0][h][1]);
+#pragma unroll
+        for (int j = 1; j < NT; ++j) mx[h] = fmaxf(mx[h], fmaxf(s[j][h][0], s[j][h][1]));
+      }
       raise_reference(mx);
     }
-    float p[NH][2];
+    float p[NT][NH][2];
 #pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      p[h][0] = ex2(s[h][0] - m[h]);
-      p[h][1] = ex2(s[h][1] - m[h]);
-      l[h] += p[h][0] + p[h][1];
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        p[j][h][0] = ex2(s[j][h][0] - m[h]);
+        p[j][h][1] = ex2(s[j][h][1] - m[h]);
+        l[h] += p[j][h][0] + p[j][h][1];
+      }
     }
-    // ---- Sparse V: weights below the threshold are dropped; an all-dropped tile skips V ----
+    // ---- Sparse V: weights below the threshold are dropped; a step whose weights are all
+    // dropped skips V ----
     if (k.a.skip_threshold > 0.f) {
       const float tau = k.a.skip_threshold;
       bool any = false;
 #pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        p[h][0] = p[h][0] >= tau ? p[h][0] : 0.f;
-        p[h][1] = p[h][1] >= tau ? p[h][1] : 0.f;
-        any |= (p[h][0] + p[h][1]) > 0.f;
+      for (int j = 0; j < NT; ++j) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          p[j][h][0] = p[j][h][0] >= tau ? p[j][h][0] : 0.f;
+          p[j][h][1] = p[j][h][1] >= tau ? p[j][h][1] : 0.f;
+          any |= (p[j][h][0] + p[j][h][1]) > 0.f;
+        }
       }
       if (!__any_sync(kFull, any)) {
         __syncwarp();
@@ -545,21 +609,127 @@ struct MmaWarp {
     }
 
     // ---- P' = weight (* V norm for turbo V), one word per (column, token pair g / g + 8) ----
-    float2 nv = make_float2(1.f, 1.f);
-    if constexpr (!F::VQ8) nv = __half22float2(u32_as_h2(vc.h0));
-    constexpr uint32_t kBuf = 256 * BUF;
-    if (HILO) {
-      const float w0 = p[0][0] * nv.x, w1 = p[0][1] * nv.y;
-      const __half2 hi = __floats2half2_rn(w0, w1);
-      const float2 hf = __half22float2(hi);
-      sts32(psw0 + kBuf, h2_as_u32(hi));
-      sts32(psw1 + kBuf, h2_as_u32(__floats2half2_rn(w0 - hf.x, w1 - hf.y)));
-    } else {
-      sts32(psw0 + kBuf, h2_as_u32(__floats2half2_rn(p[0][0] * nv.x, p[0][1] * nv.y)));
-      sts32(psw1 + kBuf, h2_as_u32(__floats2half2_rn(p[NH - 1][0] * nv.x, p[NH - 1][1] * nv.y)));
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      float2 nv = make_float2(1.f, 1.f);
+      if constexpr (!F::VQ8) nv = __half22float2(u32_as_h2(vc[j].h0));
+      const uint32_t buf = kBuf + 256 * j;
+      if (HILO) {
+        const float w0 = p[j][0][0] * nv.x, w1 = p[j][0][1] * nv.y;
+        const __half2 hi = __floats2half2_rn(w0, w1);
+        const float2 hf = __half22float2(hi);
+        sts32(psw0 + buf, h2_as_u32(hi));
+        sts32(psw1 + buf, h2_as_u32(__floats2half2_rn(w0 - hf.x, w1 - hf.y)));
+      } else {
+        sts32(psw0 + buf, h2_as_u32(__floats2half2_rn(p[j][0][0] * nv.x, p[j][0][1] * nv.y)));
+        sts32(psw1 + buf, h2_as_u32(__floats2half2_rn(p[j][NH - 1][0] * nv.x, p[j][NH - 1][1] * nv.y)));
+      }
     }
     __syncwarp();
-    accumulate_v(vc, lds64_v(psr + kBuf));
+#pragma unroll
+    for (int j = 0; j < NT; ++j) accumulate_v(vc[j], lds64_v(psr + kBuf + 256 * j));
+  }
+
+  // A pair of whole tiles whose K and V were loaded into kn / vn by the previous step; their
+  // cursors cu (a tile whose page is out of range has its scores masked: its loads read page 0).
+  // With MORE, the next pair's loads (cursors nx) are issued into kn as soon as the score
+  // products have consumed K, and into vn once the V products have consumed V, so each load has
+  // about half a step to land before it is needed.
+  template <bool MORE>
+  __device__ __forceinline__ void step_pipelined(const Cursor (&cu)[2], const Cursor (&nx)[2], uint32_t kBuf) {
+    KTile kc[2] = {kn[0], kn[1]};
+    VTile vc[2] = {vn[0], vn[1]};
+    float cc[2][NH][4], cs[2][NH][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+      for (int q = 0; q < NH; ++q) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cc[j][q][e] = cs[j][q][e] = 0.f;
+      }
+    }
+    score<2>(kc, cc, cs);
+    if (MORE) {
+      load_k<true>(kn[0], nx[0], 16);
+      load_k<true>(kn[1], nx[1], 16);
+    }
+    float s[2][NH][2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float2 hA = __half22float2(u32_as_h2(kc[j].ha[0])), hB = __half22float2(u32_as_h2(kc[j].hb[0]));
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        if constexpr (F::KQ8) {
+          s[j][h][0] = cc[j][h][0] + cc[j][h][1];
+          s[j][h][1] = cc[j][h][2] + cc[j][h][3];
+        } else {
+          s[j][h][0] = fmaf(hA.x, cc[j][h][0] + cc[j][h][1], hA.y * (cs[j][h][0] + cs[j][h][1]));
+          s[j][h][1] = fmaf(hB.x, cc[j][h][2] + cc[j][h][3], hB.y * (cs[j][h][2] + cs[j][h][3]));
+        }
+        if (!cu[j].ok) s[j][h][0] = s[j][h][1] = -INFINITY;  // warp-uniform
+      }
+    }
+    float mx[NH];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) mx[h] = fmaxf(fmaxf(s[0][h][0], s[0][h][1]), fmaxf(s[1][h][0], s[1][h][1]));
+    raise_reference(mx);
+    float p[2][NH][2];
+    bool any = false;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        p[j][h][0] = ex2(s[j][h][0] - m[h]);
+        p[j][h][1] = ex2(s[j][h][1] - m[h]);
+        l[h] += p[j][h][0] + p[j][h][1];
+      }
+    }
+    // Sparse V: weights below the threshold are dropped; a pair whose weights are all dropped
+    // skips the V products (its next V loads are issued all the same)
+    const float tau = k.a.skip_threshold;
+    if (tau > 0.f) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          p[j][h][0] = p[j][h][0] >= tau ? p[j][h][0] : 0.f;
+          p[j][h][1] = p[j][h][1] >= tau ? p[j][h][1] : 0.f;
+          any |= (p[j][h][0] + p[j][h][1]) > 0.f;
+        }
+      }
+    }
+    if (tau <= 0.f || __any_sync(kFull, any)) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float2 nv = make_float2(1.f, 1.f);
+        if constexpr (!F::VQ8) nv = __half22float2(u32_as_h2(vc[j].h0));
+        const uint32_t buf = kBuf + 256 * j;
+        const float w0 = p[j][0][0] * nv.x, w1 = p[j][0][1] * nv.y;
+        const __half2 hi = __floats2half2_rn(w0, w1);
+        const float2 hf = __half22float2(hi);
+        sts32(psw0 + buf, h2_as_u32(hi));
+        sts32(psw1 + buf, h2_as_u32(__floats2half2_rn(w0 - hf.x, w1 - hf.y)));
+      }
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 2; ++j) accumulate_v(vc[j], lds64_v(psr + kBuf + 256 * j));
+    }
+    __syncwarp();
+    if (MORE) {
+      load_v<true>(vn[0], nx[0], 16);
+      load_v<true>(vn[1], nx[1], 16);
+    }
+  }
+
+  // One tile at cursor cu, skipped when its page is out of range.
+  __device__ __forceinline__ void step_one(const Cursor& cu, bool last, uint32_t kBuf) {
+    if (!cu.ok) {  // warp-uniform
+      __syncwarp();
+      return;
+    }
+    const Cursor one[1] = {cu};
+    if (last && last_valid < 16) step_tiles<1, false>(one, last_valid, kBuf);
+    else step_tiles<1, true>(one, 16, kBuf);
   }
 
   __device__ __forceinline__ void run_item(unsigned int item) {
@@ -593,16 +763,16 @@ struct MmaWarp {
       const float* qp = k.qprep + (row0 + k.g_off + (valid ? head : 0)) * 2 * D;
       const float fq = valid ? (F::KQ8 ? kLog2e : kLog2e / k.tab.f16_scale[F::KQ8 ? 0 : F::WK - 2]) : 0.f;
       const float fs = valid ? kLog2e * kSqrtHalfPi / (float)D : 0.f;
-      const int jq = F::KQ8 ? q : 2 * q;  // product index of the codebook (int8) part
 #pragma unroll
       for (int ch = 0; ch < KS; ++ch) {
         const int c0 = F::KQ8 ? 32 * (ch >> 1) + 8 * t + 4 * (ch & 1) : t * (D / 4) + 4 * ch;
         const float4 v = *reinterpret_cast<const float4*>(qp + c0);
-        sts64(qf + 256 * (KS * jq + ch), pack_part(v.x * fq, v.y * fq, lo), pack_part(v.z * fq, v.w * fq, lo));
-        if constexpr (!F::KQ8) {
+        if constexpr (F::KQ8) {
+          sts64(qf + 256 * (KS * q + ch), pack_part(v.x * fq, v.y * fq, lo), pack_part(v.z * fq, v.w * fq, lo));
+        } else {
           const float4 u = *reinterpret_cast<const float4*>(qp + D + c0);
-          sts64(qf + 256 * (KS * (jq + 1) + ch), pack_part(u.x * fs, u.y * fs, lo),
-                pack_part(u.z * fs, u.w * fs, lo));
+          sts128(qf + 512 * (KS * q + ch), pack_part(v.x * fq, v.y * fq, lo), pack_part(v.z * fq, v.w * fq, lo),
+                 pack_part(u.x * fs, u.y * fs, lo), pack_part(u.z * fs, u.w * fs, lo));
         }
       }
     }
@@ -620,16 +790,77 @@ struct MmaWarp {
     if (ntiles > 0) {
       c.page_ord = t0 / a.k.page_size;
       c.in_page = t0 - c.page_ord * a.k.page_size;
-      set_page();
+      set_page(c);
       prefetch_tiles(0, 0, kPrefetchTiles);
-      for (int tile = 0; tile < ntiles; tile += 2) {
+      // P' tiles: consecutive steps alternate between the two halves of the warp's P' block, so a
+      // step's writes never meet the previous step's reads
+      // (every step call uses buf, then flips it)
+      uint32_t buf = 0;
+      constexpr uint32_t kHalf = 256 * Shape<F, HILO>::NT;
+      int tile = 0;
+      if constexpr (Shape<F, HILO>::NT == 2) {
+        // leading pairs of whole tiles, pipelined; the rest (at most two tiles, the last one
+        // possibly ragged) runs below
+        const int np = (last_valid == 16 ? ntiles : ntiles - 1) / 2;
+        if (np > 0) {
+          Cursor c1 = c;
+          advance(c1);
+          load_k<true>(kn[0], c, 16);
+          load_k<true>(kn[1], c1, 16);
+          load_v<true>(vn[0], c, 16);
+          load_v<true>(vn[1], c1, 16);
+          for (int pi = 0; pi < np; ++pi) {
+            prefetch_tiles(tile, kPrefetchTiles, 2);
+            const Cursor cur[2] = {c, c1};
+            const bool more = pi + 1 < np;
+            if (more || tile + 2 < ntiles) {
+              c = c1;
+              advance(c);  // tile + 2
+            }
+            if (more) {
+              c1 = c;
+              advance(c1);  // tile + 3
+              const Cursor nx[2] = {c, c1};
+              step_pipelined<true>(cur, nx, buf);
+            } else {
+              step_pipelined<false>(cur, cur, buf);
+            }
+            buf ^= kHalf;
+            tile += 2;
+          }
+        }
+      }
+      for (; tile < ntiles; tile += 2) {
         prefetch_tiles(tile, kPrefetchTiles, 2);  // the two tiles that follow the ones already requested
-        step<0>(tile);
-        if (tile + 1 >= ntiles) break;
-        advance();
-        step<1>(tile + 1);
-        if (tile + 2 >= ntiles) break;
-        advance();
+        if (tile + 1 >= ntiles) {
+          step_one(c, true, buf);
+          break;
+        }
+        const bool last = tile + 2 >= ntiles;
+        if constexpr (Shape<F, HILO>::NT == 2) {
+          Cursor c1 = c;
+          advance(c1);
+          if (c.ok && c1.ok) {
+            const Cursor two[2] = {c, c1};
+            if (last && last_valid < 16) step_tiles<2, false>(two, last_valid, buf);
+            else step_tiles<2, true>(two, 16, buf);
+            buf ^= kHalf;
+          } else {
+            step_one(c, false, buf);
+            buf ^= kHalf;
+            step_one(c1, last, buf);
+            buf ^= kHalf;
+          }
+          c = c1;
+        } else {
+          step_one(c, false, buf);
+          buf ^= kHalf;
+          advance(c);
+          step_one(c, last, buf);
+          buf ^= kHalf;
+        }
+        if (last) break;
+        advance(c);
       }
     }
 
@@ -701,10 +932,10 @@ __global__ void __launch_bounds__(Shape<F, HILO>::Threads, 1) attend_mma_kernel(
     const float lam = k.tab.f16_scale[W - 2];
     for (int i = tid; i < n * 32; i += L::Threads) {
       const int e = i >> 5, r = i & 31, c0 = e & cm, c1 = e >> W;
-      uint2 v;
-      v.x = h2_as_u32(__floats2half2_rn(lam * cb[c0 & im], lam * cb[c1 & im]));
-      v.y = h2_as_u32(__floats2half2_rn((c0 >> (W - 1)) ? 1.f : -1.f, (c1 >> (W - 1)) ? 1.f : -1.f));
-      *reinterpret_cast<uint2*>(sm + kofs + e * 256 + r * 8) = v;
+      *reinterpret_cast<uint32_t*>(sm + kofs + e * 256 + r * 4) =
+          h2_as_u32(__floats2half2_rn(lam * cb[c0 & im], lam * cb[c1 & im]));
+      *reinterpret_cast<uint32_t*>(sm + kofs + e * 256 + 128 + r * 4) =
+          h2_as_u32(__floats2half2_rn((c0 >> (W - 1)) ? 1.f : -1.f, (c1 >> (W - 1)) ? 1.f : -1.f));
     }
   }
   if constexpr (!F::VQ8) {
@@ -721,13 +952,13 @@ __global__ void __launch_bounds__(Shape<F, HILO>::Threads, 1) attend_mma_kernel(
 
   MmaWarp<F, HILO> w(k);
   w.init_lane(lane);
-  w.ylk = (sbase + kofs) | ((uint32_t)lane << 3);
+  w.ylk = (sbase + kofs) | ((uint32_t)lane << 2);
   w.ylv = (sbase + vofs) | ((uint32_t)lane << 2);
   const uint32_t ps = sbase + wofs;  // this warp's two P' tiles of 64 words, then its query fragments
   w.psw0 = ps + 4 * ps_word(2 * w.t, w.g);
   w.psw1 = ps + 4 * ps_word(2 * w.t + 1, w.g);
   w.psr = ps + 4 * ps_word(w.g, w.t);
-  w.qf = ps + L::PsBytes + lane * 8;
+  w.qf = ps + L::PsBytes + lane * (F::KQ8 ? 8 : 16);
   asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(w.pol));
 
   const DecodeArgs& a = k.a;
