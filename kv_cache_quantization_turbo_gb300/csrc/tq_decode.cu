@@ -9,9 +9,10 @@
 //      keeps an online softmax (running max m, sum l), accumulates V in the
 //      rotated space as exp(s_j - m) n_j c_V[idx_j] unless that weight is below
 //      skip_threshold ("TurboQuant+: 3.8x compression ...", core content item
-//      4, Sparse V), and writes the partial (m, l, acc).  Up to 8 query heads
-//      per KV head run on tensor cores (tq_decode_mma.cuh); more, or pages that
-//      are not a multiple of 16 tokens, run attend_generic_kernel below.
+//      4, Sparse V), and writes the partial (m, l, acc).  Up to 16 query heads
+//      per KV head run on tensor cores (tq_decode_mma.cuh); a turbo-MSE format
+//      used as K, or pages that are not a multiple of 16 tokens, run
+//      attend_generic_kernel below.
 //   3. combine (one CTA of 4 warps per query row): log-sum-exp merge of the
 //      partials, acc / l, then diag(s) H back to the original space for turbo V.
 #include <cmath>
@@ -401,18 +402,17 @@ cudaError_t launch_attend_mma_heads(const DecodeKernelArgs& ka, int d, int sm_co
   return cudaErrorInvalidValue;
 }
 
-// Up to 8 query heads per KV head: one launch.  9 to 16: two launches over the two halves of each
-// KV head's query heads (each reads the cache once), with their own work counters.
+// Up to 8 query heads per KV head: one work item per (layer x sequence, KV head, split).  9 to 16:
+// each item runs twice, on the two halves of the KV head's query heads (ceil(G/2) and the rest),
+// as consecutive values of the work counter, so the two halves of an item run at about the same
+// time and the second read of each tile is served by L2: the cache is read from HBM about once.
 cudaError_t launch_attend_mma(const DecodeKernelArgs& ka, int d, int sm_count, cudaStream_t s) {
   if (ka.G <= 8) return launch_attend_mma_heads(ka, d, sm_count, s);
-  DecodeKernelArgs lo = ka, hi = ka;
-  lo.g_off = 0;
-  lo.g_cnt = (ka.G + 1) / 2;
-  hi.g_off = lo.g_cnt;
-  hi.g_cnt = ka.G - lo.g_cnt;
-  hi.counter = ka.counter + 1;
-  const cudaError_t e = launch_attend_mma_heads(lo, d, sm_count, s);
-  return e != cudaSuccess ? e : launch_attend_mma_heads(hi, d, sm_count, s);
+  DecodeKernelArgs two = ka;
+  two.g_off = 0;
+  two.g_cnt = (ka.G + 1) / 2;
+  two.g_halves = 2;
+  return launch_attend_mma_heads(two, d, sm_count, s);
 }
 
 template <int D>
@@ -450,6 +450,7 @@ cudaError_t launch_decode(const DevTables& t, const DecodeArgs& a, const DecodeP
   ka.G = a.n_q_heads / a.k.H;
   ka.g_off = 0;
   ka.g_cnt = ka.G;
+  ka.g_halves = 1;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   ka.qprep = reinterpret_cast<float*>(ws);
   ka.partial = reinterpret_cast<float*>(ws + (plan.qprep_floats * 4 + 255) / 256 * 256);

@@ -1,9 +1,9 @@
 // Split-K decode attention on tensor cores, parameterised by the cache formats: turbo K with
 // W-bit codes (W - 1 index bits + the QJL sign bit; turbo2/3/4), turbo-MSE V with W-bit indices
 // (turbo2/3/4_mse), and q8_0 K or V, at head_dim 64, 128 or 256, up to 8 query heads per KV head
-// per launch (query heads g_off .. g_off + g_cnt - 1 of each KV head's G; with 9 to 16 the decode
-// call launches it on the two halves).  One partial (m, l, acc) per query row and split, combined
-// afterwards.
+// per work item (query heads g_off .. g_off + g_cnt - 1 of each KV head's G; with 9 to 16 every
+// item runs twice, on the two halves, as consecutive work-counter values).  One partial (m, l,
+// acc) per query row and split, combined afterwards.
 //
 // Why tensor cores: at HBM speed one 16-token tile of one KV head (1888 B for turbo4 / turbo4_mse
 // at d = 128) leaves ~350 warp instructions per SM, and scoring it on CUDA cores takes ~3 G d
@@ -219,6 +219,7 @@ struct MmaWarp {
   uint64_t pol;
 
   int layer, b, kvh, ntiles, last_valid;
+  int gof, gcn;  // this item's query heads: [gof, gof + gcn) of the KV head's G
   Cursor c;
   KTile kn[2];  // the next pair's K and V, loaded one phase ahead (pipelined pair steps)
   VTile vn[2];
@@ -735,6 +736,14 @@ struct MmaWarp {
   __device__ __forceinline__ void run_item(unsigned int item) {
     const DecodeArgs& a = k.a;
     const int H = a.k.H, G = k.G, Hq = a.n_q_heads;
+    gof = k.g_off;
+    gcn = k.g_cnt;
+    if (k.g_halves == 2) {  // consecutive counter values: the two head halves of one item
+      const bool hi = item & 1u;
+      item >>= 1;
+      gof = hi ? k.g_cnt : 0;
+      gcn = hi ? G - k.g_cnt : k.g_cnt;
+    }
     const int split = (int)(item % k.n_splits);
     const unsigned int rest = item / k.n_splits;
     kvh = (int)(rest % H);
@@ -759,8 +768,8 @@ struct MmaWarp {
     for (int q = 0; q < NH; ++q) {
       const int head = 4 * q + (g >> 1);
       const bool lo = g & 1;
-      const bool valid = head < k.g_cnt;
-      const float* qp = k.qprep + (row0 + k.g_off + (valid ? head : 0)) * 2 * D;
+      const bool valid = head < gcn;
+      const float* qp = k.qprep + (row0 + gof + (valid ? head : 0)) * 2 * D;
       const float fq = valid ? (F::KQ8 ? kLog2e : kLog2e / k.tab.f16_scale[F::KQ8 ? 0 : F::WK - 2]) : 0.f;
       const float fs = valid ? kLog2e * kSqrtHalfPi / (float)D : 0.f;
 #pragma unroll
@@ -874,7 +883,7 @@ struct MmaWarp {
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
       const int head = t + 4 * h;
-      if (head >= k.g_cnt) continue;
+      if (head >= gcn) continue;
       float v[2 * KS];
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) {
@@ -886,7 +895,7 @@ struct MmaWarp {
           v[2 * mt + 1] = oacc[mt][2 + h] * inv_lam;
         }
       }
-      float* dst = k.partial + ((row0 + k.g_off + head) * k.n_splits + split) * (D + 4);
+      float* dst = k.partial + ((row0 + gof + head) * k.n_splits + split) * (D + 4);
       float4* dv = reinterpret_cast<float4*>(dst + 4 + g * (D / 8));
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) dv[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
@@ -962,7 +971,7 @@ __global__ void __launch_bounds__(Shape<F, HILO>::Threads, 1) attend_mma_kernel(
   asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(w.pol));
 
   const DecodeArgs& a = k.a;
-  const unsigned int n_items = (unsigned int)((long long)a.n_layers * a.batch * a.k.H * k.n_splits);
+  const unsigned int n_items = (unsigned int)((long long)a.n_layers * a.batch * a.k.H * k.n_splits * k.g_halves);
   for (;;) {
     unsigned int item = 0;
     if (lane == 0) item = atomicAdd(k.counter, 1u);
@@ -988,7 +997,7 @@ cudaError_t launch_shape(const DecodeLaunch& k, long long items, int sm_count, c
 
 template <class F>
 cudaError_t launch_mma(const DecodeLaunch& k, int sm_count, cudaStream_t s) {
-  const long long items = (long long)k.a.n_layers * k.a.batch * k.a.k.H * k.n_splits;
+  const long long items = (long long)k.a.n_layers * k.a.batch * k.a.k.H * k.n_splits * k.g_halves;
   if (items >= (1LL << 32)) return cudaErrorInvalidValue;
   return k.g_cnt <= 4 ? launch_shape<F, true>(k, items, sm_count, s) : launch_shape<F, false>(k, items, sm_count, s);
 }

@@ -100,6 +100,7 @@ struct DecodeLaunch {
   DevTables tab;
   int split_tokens, n_splits, G;
   int g_off, g_cnt;  // tensor-core kernel: query heads [g_off, g_off + g_cnt) of each KV head's G
+  int g_halves;      // 2: every work item runs twice, on heads [0, g_cnt) and [g_cnt, G) (9 to 16 heads)
   float* qprep;    // [rows][2d]: q' then Sq'
   float* partial;  // [rows][n_splits][d + 4]: m (natural log units), l, -, -, acc[d]
   unsigned int* counter;  // two work-item counters (zeroed by the prologue kernel)

@@ -2,6 +2,7 @@
 
     python -m kv_cache_quantization_turbo_gb300.decode_timing --workload paged-batch64-turbo3 --head-dim 128
     python -m kv_cache_quantization_turbo_gb300.decode_timing --workload asym-q8k-turbo2v-needles
+    python -m kv_cache_quantization_turbo_gb300.decode_timing --workload contiguous --kv-heads 4 --q-heads 64
 
 Builds the recipe's compressed cache on cuda:0 with the library's own encoder (seeded synthetic
 inputs from workloads.py), then times whole decode calls (every layer of the recipe, one query
@@ -112,18 +113,49 @@ def _paged(wl, d):
     return ctx, f, nbytes, cfg, (encode_layer0, n_tok, enc_bytes)
 
 
+def _contiguous(a):
+    """One sequence of a.ctx tokens per layer, contiguous cache, any query-head grouping and format
+    pair (e.g. 4 KV heads with 64 query heads: 16 query heads per KV head)."""
+    L, H, Hq, d, T = a.layers, a.kv_heads, a.q_heads, a.head_dim, a.ctx
+    ctx = tq.tq_context_create(d, 1, 2, W.wht_signs(1, d), W.qjl_matrix(2, d))
+    kview = tq.alloc_view(a.k_format, d, H, page_size=T, num_pages=1, n_layers=L)
+    vview = tq.alloc_view(a.v_format, d, H, page_size=T, num_pages=1, n_layers=L)
+    for l in range(L):
+        k = W.kv_tensor(T, H, d, seed=7000 + 2 * l, device="cuda", outlier_frac=0.01)
+        v = W.kv_tensor(T, H, d, seed=7001 + 2 * l, device="cuda", outlier_frac=0.01)
+        st = tq.tq_encode_kv(ctx, kview, k, vview, v, l, 1, T, T * H * d, H * d)
+        assert st == tq.TQ_OK, tq.tq_status_string(st)
+        del k, v
+    q = W.normal_tensor((L, 1, Hq, d), seed=7999, device="cuda")
+    f = _decode_fn(ctx, q, kview, vview, 0, [T], T)
+    nbytes = L * H * T * (tq.tq_vector_bytes(a.k_format, d) + tq.tq_vector_bytes(a.v_format, d))
+    cfg = {"layers": L, "kv_heads": H, "q_heads": Hq, "head_dim": d, "ctx": T, "k_format": a.k_format,
+           "v_format": a.v_format}
+    return ctx, f, nbytes, cfg, None
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    p.add_argument("--workload", required=True, choices=["asym-q8k-turbo2v-needles", "paged-batch64-turbo3"])
-    p.add_argument("--head-dim", type=int, default=128, choices=[64, 128, 256], help="paged recipe only")
+    p.add_argument("--workload", required=True, choices=["asym-q8k-turbo2v-needles", "paged-batch64-turbo3",
+                                                         "contiguous"])
+    p.add_argument("--head-dim", type=int, default=128, choices=[64, 128, 256], help="paged and contiguous")
+    p.add_argument("--layers", type=int, default=32, help="contiguous only (as the next five)")
+    p.add_argument("--kv-heads", type=int, default=4)
+    p.add_argument("--q-heads", type=int, default=64)
+    p.add_argument("--ctx", type=int, default=32768)
+    p.add_argument("--k-format", default="turbo4")
+    p.add_argument("--v-format", default="turbo4_mse")
     p.add_argument("--calls", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     args = p.parse_args(argv)
     if not torch.cuda.is_available():
         raise SystemExit("decode_timing needs a CUDA device")
-    wl = W.WORKLOADS[args.workload]
-    ctx, run, nbytes, cfg, enc = _needles(wl) if args.workload == "asym-q8k-turbo2v-needles" else \
-        _paged(wl, args.head_dim)
+    if args.workload == "contiguous":
+        ctx, run, nbytes, cfg, enc = _contiguous(args)
+    else:
+        wl = W.WORKLOADS[args.workload]
+        ctx, run, nbytes, cfg, enc = _needles(wl) if args.workload == "asym-q8k-turbo2v-needles" else \
+            _paged(wl, args.head_dim)
     dt = _time(run, args.calls, args.warmup)
     line = {"metric": "decode_attention_bandwidth", "value": round(nbytes / dt / 1e9, 1), "unit": "GB/s",
             "ms_per_call": round(dt * 1e3, 4), "algorithmic_bytes": int(nbytes), "calls": args.calls,
