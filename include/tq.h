@@ -278,6 +278,54 @@ tq_status tq_decode_attention_static(const tq_context* ctx,
                                      float softmax_scale, float skip_threshold,
                                      float* out, tq_stream_t stream);
 
+/* ---- per-layer views: a K and a V format per layer ---- */
+
+/*
+ * Layer policies that give some layers another format, as in Boundary V ("TurboQuant+: 3.8x
+ * compression ...", core content item 3: q8_0 V on the first 2 and last 2 layers, turbo2 V
+ * elsewhere; "TurboQuant+ deep dive", section 3.2, layer-wise V strategy), or asymmetric K/V
+ * pairs per layer (same page's item 2; deep dive section 3.1), are expressed with one view per
+ * layer: layer l is stored at layer k_view_layers[l] of k_views[l] (host arrays [n_layers]) and
+ * at layer v_view_layers[l] of v_views[l].  Views may repeat (a view holding several layers).
+ * Every layer's views must share head_dim (the context's) and n_kv_heads; the K and V views of a
+ * layer must share page_size and num_pages.
+ */
+
+/*
+ * tq_encode_kv over per-layer views: input layer l (at k + l * in_layer_stride elements, same for
+ * v) is encoded into layer k_view_layers[l] of k_views[l] (and v_*).  k_views (with k_view_layers
+ * and k) or v_views (with v_view_layers and v) may be NULL, not both.  Every layer is validated
+ * before anything is launched; then runs of consecutive layers that share their views at
+ * consecutive view layers are encoded by one call of tq_encode_kv each.  Errors as tq_encode_kv.
+ */
+tq_status tq_encode_kv_layers(const tq_context* ctx,
+                              const tq_cache_view* k_views, const int32_t* k_view_layers,
+                              const tq_cache_view* v_views, const int32_t* v_view_layers, int n_layers,
+                              const void* k, const void* v, int n_tokens,
+                              int64_t in_layer_stride, int64_t in_token_stride,
+                              const int64_t* slots, int64_t slot_begin, tq_stream_t stream);
+
+/*
+ * tq_decode_attention over per-layer views, in one call: q, out, seq_lens, block_table, the scale,
+ * the skip threshold and the workspace as for tq_decode_attention (layer l of q and out is query
+ * layer l), the workspace sized by tq_decode_workspace_bytes(ctx, n_layers, batch, n_q_heads,
+ * max_ctx).  Every layer is validated before anything is launched (TQ_ERR_INVALID_ARG /
+ * TQ_ERR_UNSUPPORTED / TQ_ERR_WORKSPACE as for tq_decode_attention; more than 65535 layers or
+ * view layers: TQ_ERR_UNSUPPORTED); then the layers are grouped by their (K view, V view) pair,
+ * wherever they sit, and each group (128 layers at most per launch) runs the decode kernels once,
+ * with the split plan tq_decode_attention would take for that group alone when it fits in the
+ * workspace, else the whole call's.  The result then equals tq_decode_attention run on each group.
+ */
+tq_status tq_decode_attention_layers(const tq_context* ctx, const void* q, int q_is_fp16,
+                                     int n_layers, int batch, int n_q_heads,
+                                     const tq_cache_view* k_views, const int32_t* k_view_layers,
+                                     const tq_cache_view* v_views, const int32_t* v_view_layers,
+                                     const int32_t* seq_lens, int max_ctx,
+                                     const int32_t* block_table, int max_blocks_per_seq,
+                                     float softmax_scale, float skip_threshold,
+                                     void* workspace, size_t workspace_bytes,
+                                     float* out, tq_stream_t stream);
+
 /* ---- dequantize (reconstruction; test and debugging path) ---- */
 
 /*
@@ -291,6 +339,62 @@ tq_status tq_decode_attention_static(const tq_context* ctx,
 tq_status tq_dequantize(const tq_context* ctx, const tq_cache_view* view, int layer,
                         const int64_t* slots, int64_t slot_begin, int n,
                         int include_qjl, float* out, tq_stream_t stream);
+
+/* ---- persistence of a compressed cache (host; out of the hot path) ---- */
+
+/*
+ * A compressed cache saved to disk and read back ("mac-code TurboQuant analysis",
+ * section 2.4: the compressed arrays are serialised with a small JSON metadata
+ * record; here both go into one file).  File layout:
+ *   the 9 bytes "TQCACHE1\n";
+ *   one JSON object on one line followed by "\n", with the keys version, format,
+ *     format_id, head_dim, n_kv_heads, page_size, num_pages, n_layers, bits,
+ *     payload_bytes, header_bytes, wht_seed, qjl_seed, tables_hash (16 hex
+ *     digits), data_hash (16 hex digits) and layout;
+ *   zero bytes up to the next multiple of 4096;
+ *   the view's payload array (all its layers, in the view's own order), then its
+ *     header array.
+ * tables_hash is FNV-1a 64 over head_dim (int32), the sign diagonal (int8 [d]),
+ * the QJL matrix (float [d*d]) and the codebook tables (float [3][8], [3][7]) of
+ * the context; data_hash is FNV-1a 64 over the two arrays as 64-bit
+ * little-endian words, taken in blocks of 64 MiB per array (each block's trailing
+ * bytes one at a time).  Codes are only meaningful with the tables they were made
+ * with, so a load checks tables_hash against its context.
+ */
+
+/* FNV-1a 64 hash of the context's tables (the file's tables_hash). */
+tq_status tq_context_tables_hash(const tq_context* ctx, uint64_t* hash);
+
+/*
+ * Writes every layer of `view` to `path` (created or replaced: written to
+ * path + ".partial" and renamed on success).  host_memory = 0: the view's arrays
+ * are device memory of the current device (the device is synchronised, the
+ * arrays are copied through a host buffer of at most 64 MiB); 1: host memory.
+ * ctx (may be NULL: seeds and tables_hash are then written as 0) supplies the
+ * seeds and the tables hash; its head_dim must match the view's.  Synchronous.
+ * Errors: TQ_ERR_INVALID_ARG (bad view, I/O failure), TQ_ERR_OOM, TQ_ERR_CUDA.
+ */
+tq_status tq_cache_save(const tq_context* ctx, const tq_cache_view* view, int host_memory, const char* path);
+
+/*
+ * Reads the geometry of a file written by tq_cache_save: format, head_dim,
+ * n_kv_heads, page_size, num_pages, n_layers and bits into *geometry (payload and
+ * header set to NULL), the tables hash into *tables_hash (may be NULL), so that a
+ * caller can allocate the view to load into.  TQ_ERR_INVALID_ARG if the file is
+ * missing or not such a file.
+ */
+tq_status tq_cache_file_info(const char* path, tq_cache_view* geometry, uint64_t* tables_hash);
+
+/*
+ * Reads a file written by tq_cache_save into `view`, whose format, head_dim,
+ * n_kv_heads, page_size, num_pages, n_layers and bits must equal the file's
+ * (host_memory as for tq_cache_save).  With a context, the file's tables_hash
+ * must equal the context's.  The data hash is checked after the copy; on any
+ * mismatch (geometry, tables, size, trailing bytes, data hash) the call returns
+ * TQ_ERR_INVALID_ARG, and when the data hash alone fails the view already holds
+ * the file's (corrupt) bytes.  Synchronous.
+ */
+tq_status tq_cache_load(const tq_context* ctx, const tq_cache_view* view, int host_memory, const char* path);
 
 #ifdef __cplusplus
 }

@@ -7,6 +7,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <algorithm>
 #include <vector>
 
 #include <cuda_fp16.h>
@@ -236,6 +237,8 @@ tq_status tq_context_create(int head_dim, uint32_t wht_seed, uint32_t qjl_seed, 
   if (!ctx) return TQ_ERR_OOM;
   const int d = head_dim;
   ctx->d = d;
+  ctx->wht_seed = wht_seed;
+  ctx->qjl_seed = qjl_seed;
   if (cudaGetDevice(&ctx->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&ctx->sm_count, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess) {
     delete ctx;
@@ -457,6 +460,166 @@ tq_status tq_decode_attention(const tq_context* ctx, const void* q, int q_is_fp1
   a.out = out;
   return cuda_status(launch_decode(ctx->tables, a, plan, workspace, ctx->sm_count,
                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// ---------------------------------------------------------------------------
+// per-layer views (a format per layer, e.g. Boundary V)
+// ---------------------------------------------------------------------------
+
+// The view of one layer: the view with its arrays advanced to layer `layer` and n_layers = 1.
+static bool layer_view(const tq_cache_view* v, int layer, int run, DevView* out) {
+  if (!make_dev_view(v, out) || layer < 0 || run < 1 || layer + run > out->n_layers) return false;
+  const long long vecs = (long long)out->num_pages * out->H * out->page_size;
+  out->payload += (size_t)layer * vecs * out->pay_bytes;
+  out->header += (size_t)layer * vecs * out->hdr_bytes;
+  out->n_layers = run;
+  return true;
+}
+
+static bool same_view(const tq_cache_view& a, const tq_cache_view& b) {
+  return a.format == b.format && a.head_dim == b.head_dim && a.n_kv_heads == b.n_kv_heads &&
+         a.page_size == b.page_size && a.num_pages == b.num_pages && a.n_layers == b.n_layers && a.bits == b.bits &&
+         a.payload == b.payload && a.header == b.header;
+}
+
+// Length of the run of layers from l that share their views at consecutive view layers.
+static int layer_run(const tq_cache_view* kv, const int32_t* kl, const tq_cache_view* vv, const int32_t* vl, int l,
+                     int n) {
+  int r = l + 1;
+  while (r < n && (!kv || (same_view(kv[r], kv[l]) && kl[r] == kl[r - 1] + 1)) &&
+         (!vv || (same_view(vv[r], vv[l]) && vl[r] == vl[r - 1] + 1)))
+    ++r;
+  return r - l;
+}
+
+tq_status tq_encode_kv_layers(const tq_context* ctx, const tq_cache_view* k_views, const int32_t* k_view_layers,
+                              const tq_cache_view* v_views, const int32_t* v_view_layers, int n_layers,
+                              const void* k, const void* v, int n_tokens, int64_t in_layer_stride,
+                              int64_t in_token_stride, const int64_t* slots, int64_t slot_begin, tq_stream_t stream) {
+  if (!ctx || n_layers < 0 || (!k_views && !v_views)) return TQ_ERR_INVALID_ARG;
+  if ((k_views && (!k_view_layers || !k)) || (v_views && (!v_view_layers || !v))) return TQ_ERR_INVALID_ARG;
+  // every layer validated before anything is launched
+  for (int l = 0; l < n_layers; ++l) {
+    DevView dv{};
+    if (k_views && !layer_view(&k_views[l], k_view_layers[l], 1, &dv)) return TQ_ERR_INVALID_ARG;
+    if (v_views && !layer_view(&v_views[l], v_view_layers[l], 1, &dv)) return TQ_ERR_INVALID_ARG;
+  }
+  const size_t esz = 2;  // fp16 inputs
+  for (int l = 0; l < n_layers;) {
+    const int run = layer_run(k_views, k_view_layers, v_views, v_view_layers, l, n_layers);
+    const unsigned char* kp = static_cast<const unsigned char*>(k);
+    const unsigned char* vp = static_cast<const unsigned char*>(v);
+    // one call of tq_encode_kv per run: K and V of the run may sit at different layers of their views,
+    // so they go as two calls when they do
+    const int kb = k_views ? k_view_layers[l] : 0, vb = v_views ? v_view_layers[l] : 0;
+    tq_status st = TQ_OK;
+    if (k_views && v_views && kb == vb) {
+      st = tq_encode_kv(ctx, &k_views[l], kp + (size_t)l * in_layer_stride * esz, &v_views[l],
+                        vp + (size_t)l * in_layer_stride * esz, kb, run, n_tokens, in_layer_stride, in_token_stride,
+                        slots, slot_begin, stream);
+    } else {
+      if (k_views)
+        st = tq_encode_kv(ctx, &k_views[l], kp + (size_t)l * in_layer_stride * esz, nullptr, nullptr, kb, run,
+                          n_tokens, in_layer_stride, in_token_stride, slots, slot_begin, stream);
+      if (st == TQ_OK && v_views)
+        st = tq_encode_kv(ctx, nullptr, nullptr, &v_views[l], vp + (size_t)l * in_layer_stride * esz, vb, run,
+                          n_tokens, in_layer_stride, in_token_stride, slots, slot_begin, stream);
+    }
+    if (st != TQ_OK) return st;
+    l += run;
+  }
+  return TQ_OK;
+}
+
+tq_status tq_decode_attention_layers(const tq_context* ctx, const void* q, int q_is_fp16, int n_layers, int batch,
+                                     int n_q_heads, const tq_cache_view* k_views, const int32_t* k_view_layers,
+                                     const tq_cache_view* v_views, const int32_t* v_view_layers,
+                                     const int32_t* seq_lens, int max_ctx, const int32_t* block_table,
+                                     int max_blocks_per_seq, float softmax_scale, float skip_threshold,
+                                     void* workspace, size_t workspace_bytes, float* out, tq_stream_t stream) {
+  if (!ctx || !q || !out || !seq_lens || !k_views || !v_views || !k_view_layers || !v_view_layers)
+    return TQ_ERR_INVALID_ARG;
+  if (n_layers < 0 || batch < 0 || n_q_heads < 1 || max_ctx < 0) return TQ_ERR_INVALID_ARG;
+  if (q_is_fp16 != 0 && q_is_fp16 != 1) return TQ_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale) || !(skip_threshold >= 0.0f) || !std::isfinite(skip_threshold))
+    return TQ_ERR_INVALID_ARG;
+  if (n_layers > 65535) return TQ_ERR_UNSUPPORTED;  // layer maps hold 16-bit indices
+  const int d = ctx->d;
+  int H = 0;
+  for (int l = 0; l < n_layers; ++l) {  // every layer validated before anything is launched
+    DevView kd{}, vd{};
+    if (!layer_view(&k_views[l], k_view_layers[l], 1, &kd) || !layer_view(&v_views[l], v_view_layers[l], 1, &vd))
+      return TQ_ERR_INVALID_ARG;
+    if (k_view_layers[l] > 65535 || v_view_layers[l] > 65535) return TQ_ERR_UNSUPPORTED;
+    if (kd.d != d || vd.d != d || kd.H != vd.H || (l > 0 && kd.H != H)) return TQ_ERR_INVALID_ARG;
+    H = kd.H;
+    if (kd.page_size != vd.page_size || kd.num_pages != vd.num_pages) return TQ_ERR_INVALID_ARG;
+    const bool k_ok = format_is_turbo(kd.format) || kd.format == TQ_FMT_Q8_0;
+    const bool v_ok = (format_is_turbo(vd.format) && !vd.has_qjl) || vd.format == TQ_FMT_Q8_0;
+    if (!k_ok || !v_ok) return TQ_ERR_UNSUPPORTED;
+    if (block_table) {
+      if (max_blocks_per_seq < 1 || (int64_t)max_blocks_per_seq * kd.page_size < max_ctx) return TQ_ERR_INVALID_ARG;
+    } else if (max_ctx > kd.page_size || batch > kd.num_pages) {
+      return TQ_ERR_INVALID_ARG;
+    }
+  }
+  if (n_layers == 0 || batch == 0) return TQ_OK;
+  if (n_q_heads % H != 0 || n_q_heads / H > 16) return TQ_ERR_UNSUPPORTED;
+  // one plan for the whole call, so the workspace of tq_decode_workspace_bytes(n_layers, ...) holds every run
+  const DecodePlan plan = plan_decode(ctx->sm_count, d, n_layers, batch, n_q_heads, max_ctx);
+  if (!workspace || workspace_bytes < plan.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return TQ_ERR_WORKSPACE;
+  // layers grouped by their (K view, V view) pair, in order of first appearance; one launch set per
+  // group (at most DecodeArgs::kMapMax layers each) with a layer map
+  std::vector<int> done(n_layers, 0);
+  for (int l0 = 0; l0 < n_layers; ++l0) {
+    if (done[l0]) continue;
+    std::vector<int> group;
+    for (int l = l0; l < n_layers; ++l)
+      if (!done[l] && same_view(k_views[l], k_views[l0]) && same_view(v_views[l], v_views[l0])) {
+        group.push_back(l);
+        done[l] = 1;
+      }
+    for (size_t c0 = 0; c0 < group.size(); c0 += DecodeArgs::kMapMax) {
+      const int cnt = (int)std::min(group.size() - c0, (size_t)DecodeArgs::kMapMax);
+      DecodeArgs a{};
+      make_dev_view(&k_views[l0], &a.k);
+      make_dev_view(&v_views[l0], &a.v);
+      a.n_map = cnt;
+      for (int i = 0; i < cnt; ++i) {
+        const int l = group[c0 + i];
+        a.k_layer[i] = (uint16_t)k_view_layers[l];
+        a.v_layer[i] = (uint16_t)v_view_layers[l];
+        a.q_layer[i] = (uint16_t)l;
+      }
+      a.q = q;
+      a.q_is_fp16 = q_is_fp16;
+      a.n_layers = cnt;
+      a.batch = batch;
+      a.n_q_heads = n_q_heads;
+      a.layer_begin = 0;
+      a.seq_lens = seq_lens;
+      a.max_ctx = max_ctx;
+      a.block_table = block_table;
+      a.max_blocks_per_seq = block_table ? max_blocks_per_seq : 1;
+      a.softmax_scale = softmax_scale;
+      a.skip_threshold = skip_threshold;
+      a.out = out;
+      // the group's own split plan when it fits in the workspace (a few boundary layers want shorter
+      // splits than the whole call to fill the GPU), else the whole call's splits for its rows only
+      DecodePlan rp = plan_decode(ctx->sm_count, d, cnt, batch, n_q_heads, max_ctx);
+      if (rp.bytes > workspace_bytes) {
+        rp = plan;
+        const size_t rows = (size_t)cnt * batch * n_q_heads;
+        rp.qprep_floats = rows * 2 * d;
+        rp.partial_floats = rows * plan.n_splits * (d + 4);
+      }
+      const tq_status st = cuda_status(
+          launch_decode(ctx->tables, a, rp, workspace, ctx->sm_count, reinterpret_cast<cudaStream_t>(stream)));
+      if (st != TQ_OK) return st;
+    }
+  }
+  return TQ_OK;
 }
 
 }  // extern "C"

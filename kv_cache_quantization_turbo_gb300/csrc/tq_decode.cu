@@ -74,11 +74,11 @@ __global__ void __launch_bounds__(D) qprep_kernel(DecodeKernelArgs ka) {
   if (w == 0) {
     float x[E];
     if (a.q_is_fp16) {
-      const __half* q = static_cast<const __half*>(a.q) + row * D;
+      const __half* q = static_cast<const __half*>(a.q) + io_row_of(a, row) * D;
 #pragma unroll
       for (int e = 0; e < E; ++e) x[e] = __half2float(q[E * lane + e]);
     } else {
-      const float* q = static_cast<const float*>(a.q) + row * D;
+      const float* q = static_cast<const float*>(a.q) + io_row_of(a, row) * D;
 #pragma unroll
       for (int e = 0; e < E; ++e) x[e] = q[E * lane + e];
     }
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(32) attend_generic_kernel(DecodeKernelArgs ka)
   const int lane = threadIdx.x;
   const int split = blockIdx.x, kvh = blockIdx.y;
   const int lb = blockIdx.z, layer_rel = lb / a.batch, b = lb % a.batch;
-  const int layer = a.layer_begin + layer_rel;
+  const int layer = k_layer_of(a, layer_rel), layer_v = v_layer_of(a, layer_rel);
   const int G = ka.G;
   const int Hq = a.n_q_heads;
   // dynamic shared memory: q' [G][D], Sq' [G][D], acc [G][D], two codebooks
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(32) attend_generic_kernel(DecodeKernelArgs ka)
         keep |= (g < G) && pj[g] > 0.f && pj[g] >= a.skip_threshold;
       }
       if (!keep) continue;  // warp-uniform: every V term of this token is below the threshold
-      const long long vv = token_vector(a, a.v, layer, b, tb + jj, kvh, ka.tab.status);
+      const long long vv = token_vector(a, a.v, layer_v, b, tb + jj, kvh, ka.tab.status);
       if (vv < 0) continue;
       const unsigned char* hdr = a.v.header + vv * a.v.hdr_bytes;
       const unsigned char* pay = a.v.payload + vv * a.v.pay_bytes;
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(DecodeKerne
 #pragma unroll
     for (int e = 0; e < E; ++e) x[e] *= (float)ka.tab.signs[E * lane + e];
   }
-  float* dst = a.out + row * D;
+  float* dst = a.out + io_row_of(a, row) * D;
 #pragma unroll
   for (int e = 0; e < E; ++e) dst[E * lane + e] = x[e];
 }

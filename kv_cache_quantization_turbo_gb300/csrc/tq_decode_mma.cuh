@@ -218,7 +218,7 @@ struct MmaWarp {
   bool pf_k, pf_v, pf_h;     // bulk prefetch allowed (16-byte aligned tile starts)
   uint64_t pol;
 
-  int layer, b, kvh, ntiles, last_valid;
+  int layer, layer_v, b, kvh, ntiles, last_valid;  // layer: of the K view; layer_v: of the V view
   int gof, gcn;  // this item's query heads: [gof, gof + gcn) of the KV head's G
   Cursor c;
   KTile kn[2];  // the next pair's K and V, loaded one phase ahead (pipelined pair steps)
@@ -272,11 +272,13 @@ struct MmaWarp {
         page = 0;
       }
     }
-    const long long base = (((long long)layer * a.k.num_pages + page) * a.k.H + kvh) * a.k.page_size + cu.in_page;
+    const long long pv = ((long long)page * a.k.H + kvh) * a.k.page_size + cu.in_page;  // vector in its layer
+    const long long lv = (long long)a.k.num_pages * a.k.H * a.k.page_size;               // vectors per layer
+    const long long base = layer * lv + pv, vbase = layer_v * lv + pv;
     cu.kp = a.k.payload + (base + g) * F::KPay + kto;
     cu.kh = a.k.header + (base + g) * F::KHdr;
-    cu.vp = a.v.payload + (base + t) * F::VPay + vgo;
-    cu.vh = F::VQ8 ? a.v.header + (base + t) * F::VHdr + vhdr : a.v.header + (base + g) * F::VHdr;
+    cu.vp = a.v.payload + (vbase + t) * F::VPay + vgo;
+    cu.vh = F::VQ8 ? a.v.header + (vbase + t) * F::VHdr + vhdr : a.v.header + (vbase + g) * F::VHdr;
   }
 
   __device__ __forceinline__ void advance(Cursor& cu) {
@@ -748,7 +750,8 @@ struct MmaWarp {
     const unsigned int rest = item / k.n_splits;
     kvh = (int)(rest % H);
     const int lb = (int)(rest / H);
-    layer = a.layer_begin + lb / a.batch;
+    layer = k_layer_of(a, lb / a.batch);
+    layer_v = v_layer_of(a, lb / a.batch);
     b = lb % a.batch;
     int len = a.seq_lens[b];
     if (len < 0) len = 0;

@@ -79,7 +79,27 @@ struct DecodeArgs {
   int max_blocks_per_seq;
   float softmax_scale, skip_threshold;
   float* out;
+  // Layer map of a launch over layers that are not consecutive in their views (per-layer views):
+  // launch layer i reads layer k_layer[i] of the K view, v_layer[i] of the V view, and query and
+  // output layer q_layer[i].  n_map = 0: layer_begin + i in both views, i for q and out.
+  static constexpr int kMapMax = 128;
+  int n_map;
+  uint16_t k_layer[kMapMax], v_layer[kMapMax], q_layer[kMapMax];
 };
+
+__host__ __device__ __forceinline__ int k_layer_of(const DecodeArgs& a, int i) {
+  return a.n_map ? (int)a.k_layer[i] : a.layer_begin + i;
+}
+__host__ __device__ __forceinline__ int v_layer_of(const DecodeArgs& a, int i) {
+  return a.n_map ? (int)a.v_layer[i] : a.layer_begin + i;
+}
+// Row of q / out for launch row `row` = (launch layer, sequence, query head).
+__host__ __device__ __forceinline__ long long io_row_of(const DecodeArgs& a, long long row) {
+  if (!a.n_map) return row;
+  const long long per_layer = (long long)a.batch * a.n_q_heads;
+  const long long i = row / per_layer;
+  return (long long)a.q_layer[i] * per_layer + (row - i * per_layer);
+}
 
 // Split-K plan for a decode call: tokens per split and the number of splits.
 struct DecodePlan {
@@ -122,6 +142,7 @@ struct tq_context {
   int device;
   int d;
   int sm_count;
+  uint32_t wht_seed, qjl_seed;  // as given at creation (informational when the tables were passed in)
   // host copies
   int8_t signs_h[tq::kMaxDim];
   float centroids_h[3][8];

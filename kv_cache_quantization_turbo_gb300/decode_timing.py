@@ -53,32 +53,41 @@ def _decode_fn(ctx, q, kview, vview, layer_begin, lens, max_ctx, block_table=Non
 
 def _needles(wl):
     """q8_0 K everywhere; V q8_0 on the boundary layers and the recipe's V format elsewhere; one
-    sequence of wl.ctx tokens with 16 needles per KV head (two decode calls: boundary, middle)."""
+    sequence of wl.ctx tokens with 16 needles per KV head.  A per-layer format table: one K view of
+    every layer, a boundary V view and a middle V view, decoded in one tq_decode_attention_layers call."""
     L, H, d, T, Hq = wl.n_layers, wl.n_kv_heads, wl.head_dim, wl.ctx, wl.n_q_heads
     boundary = sorted(wl.v_format_layers)
     middle = [l for l in range(L) if l not in wl.v_format_layers]
     ctx = tq.tq_context_create(d, wl.wht_seed, wl.qjl_seed, W.wht_signs(wl.wht_seed, d), W.qjl_matrix(wl.qjl_seed, d))
-    views = {"kb": tq.alloc_view(wl.k_format, d, H, page_size=T, num_pages=1, n_layers=len(boundary)),
-             "vb": tq.alloc_view("q8_0", d, H, page_size=T, num_pages=1, n_layers=len(boundary)),
-             "km": tq.alloc_view(wl.k_format, d, H, page_size=T, num_pages=1, n_layers=len(middle)),
-             "vm": tq.alloc_view(wl.v_format, d, H, page_size=T, num_pages=1, n_layers=len(middle))}
+    kview = tq.alloc_view(wl.k_format, d, H, page_size=T, num_pages=1, n_layers=L)
+    vb = tq.alloc_view("q8_0", d, H, page_size=T, num_pages=1, n_layers=len(boundary))
+    vm = tq.alloc_view(wl.v_format, d, H, page_size=T, num_pages=1, n_layers=len(middle))
+    v_views = [vb if l in wl.v_format_layers else vm for l in range(L)]
+    v_layers = [boundary.index(l) if l in wl.v_format_layers else middle.index(l) for l in range(L)]
     q = torch.empty((L, 1, Hq, d), dtype=torch.float32, device="cuda")
     for l in range(L):
         k, ql, _ = W.needle_workload(T, H, Hq, d, seed=wl.seed * 1000 + 2 * l, device="cuda")
         v = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * l + 1, device="cuda")
         q[l, 0] = ql
-        kv, vv, li = (views["kb"], views["vb"], boundary.index(l)) if l in wl.v_format_layers else \
-            (views["km"], views["vm"], middle.index(l))
-        st = tq.tq_encode_kv(ctx, kv, k, vv, v, li, 1, T, T * H * d, H * d)
+        st = tq.tq_encode_kv_layers(ctx, [kview], [l], [v_views[l]], [v_layers[l]], 1, k, v, T, T * H * d, H * d)
         assert st == tq.TQ_OK, tq.tq_status_string(st)
-    fb = _decode_fn(ctx, q[boundary].contiguous(), views["kb"], views["vb"], 0, [T], T)
-    fm = _decode_fn(ctx, q[middle].contiguous(), views["km"], views["vm"], 0, [T], T)
-    vb = lambda f: tq.tq_vector_bytes(f, d)
-    nbytes = H * T * (len(boundary) * (vb(wl.k_format) + vb("q8_0")) + len(middle) * (vb(wl.k_format) +
-                                                                                     vb(wl.v_format)))
+    ws_bytes = tq.tq_decode_workspace_bytes(ctx, L, 1, Hq, T)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty((L, 1, Hq, d), dtype=torch.float32, device="cuda")
+    sl = torch.tensor([T], dtype=torch.int32, device="cuda")
+    k_views, k_layers = [kview] * L, list(range(L))
+
+    def run():
+        st = tq.tq_decode_attention_layers(ctx, q, 0, L, 1, Hq, k_views, k_layers, v_views, v_layers, sl, T, None, 0,
+                                           1.0 / math.sqrt(d), 1e-6, ws, ws_bytes, out)
+        assert st == tq.TQ_OK, tq.tq_status_string(st)
+    vb_ = lambda f: tq.tq_vector_bytes(f, d)
+    nbytes = H * T * (len(boundary) * (vb_(wl.k_format) + vb_("q8_0")) + len(middle) * (vb_(wl.k_format) +
+                                                                                        vb_(wl.v_format)))
     cfg = {"layers": L, "kv_heads": H, "q_heads": Hq, "head_dim": d, "ctx": T, "k_format": wl.k_format,
-           "v_format": wl.v_format, "boundary_layers_v": "q8_0", "boundary_layers": boundary}
-    return ctx, (lambda: (fb(), fm())), nbytes, cfg, None
+           "v_format": wl.v_format, "boundary_layers_v": "q8_0", "boundary_layers": boundary,
+           "calls": "one tq_decode_attention_layers call per decode step"}
+    return ctx, run, nbytes, cfg, None
 
 
 def _paged(wl, d):

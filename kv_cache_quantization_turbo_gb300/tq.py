@@ -62,6 +62,13 @@ _SIGS = {
                                  _P, _P]),
     "tq_dequantize": (_I, [_P, _VP, _I, _P, _I64, _I, _I, _P, _P]),
     "tq_decode_attention_static": (_I, [_P, _P, _I, _I, _I, _I, _VP, _VP, _I, _P, _I, _P, _I, _F, _F, _P, _P]),
+    "tq_encode_kv_layers": (_I, [_P, _VP, _P, _VP, _P, _I, _P, _P, _I, _I64, _I64, _P, _I64, _P]),
+    "tq_decode_attention_layers": (_I, [_P, _P, _I, _I, _I, _I, _VP, _P, _VP, _P, _P, _I, _P, _I, _F, _F, _P, _SZ,
+                                        _P, _P]),
+    "tq_context_tables_hash": (_I, [_P, ctypes.POINTER(ctypes.c_uint64)]),
+    "tq_cache_save": (_I, [_P, _VP, _I, ctypes.c_char_p]),
+    "tq_cache_file_info": (_I, [ctypes.c_char_p, _VP, ctypes.POINTER(ctypes.c_uint64)]),
+    "tq_cache_load": (_I, [_P, _VP, _I, ctypes.c_char_p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -282,3 +289,82 @@ def tq_dequantize(ctx: int, view, layer: int, slots, slot_begin: int, n: int, in
     va = _view_arg(view)
     return _lib.tq_dequantize(ctx, va[0], layer, _ptr(slots), slot_begin, n, include_qjl, _ptr(out),
                               _stream(stream))
+
+
+# ---- persistence ----
+
+def _host_view(v) -> tuple:
+    """(c view, host_memory flag) for a CacheView over torch tensors or numpy arrays."""
+    cv = v.c_view() if isinstance(v, CacheView) else v
+    host = 1
+    if isinstance(v, CacheView) and hasattr(v.payload, "is_cuda") and v.payload.is_cuda:
+        host = 0
+    return cv, host
+
+
+def tq_context_tables_hash(ctx: int) -> int:
+    h = ctypes.c_uint64(0)
+    _check(_lib.tq_context_tables_hash(ctx, ctypes.byref(h)), "tq_context_tables_hash")
+    return h.value
+
+
+def tq_cache_save(ctx, view, path: str) -> int:
+    """Saves a view (device tensors or host arrays); ctx may be None.  Returns the status."""
+    cv, host = _host_view(view)
+    return _lib.tq_cache_save(ctx, ctypes.byref(cv), host, os.fsencode(path))
+
+
+def tq_cache_file_info(path: str):
+    """Returns (status, geometry dict, tables_hash)."""
+    cv = tq_cache_view()
+    h = ctypes.c_uint64(0)
+    st = _lib.tq_cache_file_info(os.fsencode(path), ctypes.byref(cv), ctypes.byref(h))
+    geo = {k: getattr(cv, k) for k in ("format", "head_dim", "n_kv_heads", "page_size", "num_pages", "n_layers",
+                                       "bits")}
+    return st, geo, h.value
+
+
+def tq_cache_load(ctx, view, path: str) -> int:
+    """Loads a file into a view of the same geometry (device tensors or host arrays); ctx may be None."""
+    cv, host = _host_view(view)
+    return _lib.tq_cache_load(ctx, ctypes.byref(cv), host, os.fsencode(path))
+
+
+# ---- per-layer views ----
+
+def _view_array(views):
+    """(ctypes array of tq_cache_view, keep-alive) for a list of CacheView, or (None, None)."""
+    if views is None:
+        return None, None
+    arr = (tq_cache_view * len(views))(*[v.c_view() if isinstance(v, CacheView) else v for v in views])
+    return arr, arr
+
+
+def _layer_array(layers):
+    if layers is None:
+        return None
+    return (ctypes.c_int32 * len(layers))(*[int(x) for x in layers])
+
+
+def tq_encode_kv_layers(ctx: int, k_views, k_view_layers, v_views, v_view_layers, n_layers: int, k, v,
+                        n_tokens: int, in_layer_stride: int, in_token_stride: int, slots=None, slot_begin: int = 0,
+                        stream=None) -> int:
+    """k_views / v_views: lists of n_layers CacheView (or None); *_view_layers: lists of ints."""
+    ka, kkeep = _view_array(k_views)
+    va, vkeep = _view_array(v_views)
+    kl, vl = _layer_array(k_view_layers), _layer_array(v_view_layers)
+    return _lib.tq_encode_kv_layers(ctx, ka, kl, va, vl, n_layers, _ptr(k), _ptr(v), n_tokens, in_layer_stride,
+                                    in_token_stride, _ptr(slots), slot_begin, _stream(stream))
+
+
+def tq_decode_attention_layers(ctx: int, q, q_is_fp16: int, n_layers: int, batch: int, n_q_heads: int, k_views,
+                               k_view_layers, v_views, v_view_layers, seq_lens, max_ctx: int, block_table,
+                               max_blocks_per_seq: int, softmax_scale: float, skip_threshold: float, workspace,
+                               workspace_bytes: int, out, stream=None) -> int:
+    ka, kkeep = _view_array(k_views)
+    va, vkeep = _view_array(v_views)
+    return _lib.tq_decode_attention_layers(ctx, _ptr(q), q_is_fp16, n_layers, batch, n_q_heads, ka,
+                                           _layer_array(k_view_layers), va, _layer_array(v_view_layers),
+                                           _ptr(seq_lens), max_ctx, _ptr(block_table), max_blocks_per_seq,
+                                           softmax_scale, skip_threshold, _ptr(workspace), workspace_bytes, _ptr(out),
+                                           _stream(stream))

@@ -190,7 +190,9 @@ def test_llama_70b_128k_turbo4_sampled():
 def test_asymmetric_boundary_layers_needles_sampled():
     """64 layers x 4 KV heads x 32768 tokens, 32 query heads (GQA 8): K q8_0; V turbo2_mse
     except the first 2 and last 2 layers (q8_0); queries aligned with 16 needles x8;
-    skip threshold 1e-6.  One decode call per V-format group."""
+    skip threshold 1e-6.  A per-layer format table: one K view of all 64 layers, a 4-layer q8_0 V
+    view for the boundary layers and a 60-layer turbo2_mse V view, decoded in one
+    tq_decode_attention_layers call."""
     C.require_cuda()
     wl = W.WORKLOADS["asym-q8k-turbo2v-needles"]
     L, H, d, T, Hq = wl.n_layers, wl.n_kv_heads, wl.head_dim, wl.ctx, wl.n_q_heads
@@ -199,54 +201,60 @@ def test_asymmetric_boundary_layers_needles_sampled():
     middle = [l for l in range(L) if l not in wl.v_format_layers]
     ctx = C.Ctx(d, wl.wht_seed, wl.qjl_seed)
     try:
-        kb = tq.alloc_view("q8_0", d, H, page_size=T, num_pages=1, n_layers=len(boundary))
+        kview = tq.alloc_view("q8_0", d, H, page_size=T, num_pages=1, n_layers=L)
         vb = tq.alloc_view("q8_0", d, H, page_size=T, num_pages=1, n_layers=len(boundary))
-        km = tq.alloc_view("q8_0", d, H, page_size=T, num_pages=1, n_layers=len(middle))
         vm = tq.alloc_view(wl.v_format, d, H, page_size=T, num_pages=1, n_layers=len(middle))
+        v_views = [vb if l in wl.v_format_layers else vm for l in range(L)]
+        v_layers = [boundary.index(l) if l in wl.v_format_layers else middle.index(l) for l in range(L)]
         qs = torch.empty((L, 1, Hq, d), dtype=torch.float32, device="cuda")
         for l in range(L):
             k, q, _ = W.needle_workload(T, H, Hq, d, seed=wl.seed * 1000 + 2 * l, device="cuda")
             v = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * l + 1, device="cuda")
             qs[l, 0] = q
-            if l in wl.v_format_layers:
-                st = tq.tq_encode_kv(ctx.h, kb, k, vb, v, boundary.index(l), 1, T, T * H * d, H * d)
-            else:
-                st = tq.tq_encode_kv(ctx.h, km, k, vm, v, middle.index(l), 1, T, T * H * d, H * d)
+            st = tq.tq_encode_kv_layers(ctx.h, [kview], [l], [v_views[l]], [v_layers[l]], 1, k, v, T, T * H * d,
+                                        H * d)
             assert st == tq.TQ_OK
+        nbytes = tq.tq_decode_workspace_bytes(ctx.h, L, 1, Hq, T)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        lens = torch.tensor([T], dtype=torch.int32, device="cuda")
 
         def decode_all():
-            return (C.decode(ctx, qs[boundary], kb, vb, [T], T, tau=1e-6),
-                    C.decode(ctx, qs[middle], km, vm, [T], T, tau=1e-6))
+            out = torch.full((L, 1, Hq, d), float("nan"), dtype=torch.float32, device="cuda")
+            st = tq.tq_decode_attention_layers(ctx.h, qs, 0, L, 1, Hq, [kview] * L, list(range(L)), v_views, v_layers,
+                                               lens, T, None, 0, 1.0 / math.sqrt(d), 1e-6, ws, nbytes, out)
+            assert st == tq.TQ_OK
+            torch.cuda.synchronize()
+            return out
 
-        def pick(outs, layer, kvh):
-            o = outs[0][boundary.index(layer)] if layer in wl.v_format_layers else outs[1][middle.index(layer)]
-            return o[0, kvh * G:(kvh + 1) * G].cpu().numpy()
+        def pick(out, layer, kvh):
+            return out[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
 
-        outs = decode_all()  # the GPU-encoded cache
+        out = decode_all()  # the GPU-encoded cache
         encs = {}
-        for layer, kvh in ((1, 2), (30, 0)):
+        for layer, kvh in ((1, 2), (30, 0), (63, 3)):
             k, _, _ = W.needle_workload(T, H, Hq, d, seed=wl.seed * 1000 + 2 * layer, device="cuda")
             v = W.kv_tensor(T, H, d, seed=wl.seed * 1000 + 2 * layer + 1, device="cuda")
             vfmt = wl.v_format_layers.get(layer, wl.v_format)
-            kv_, vv_, li = (kb, vb, boundary.index(layer)) if vfmt == "q8_0" else (km, vm, middle.index(layer))
-            ek, gk = _check_codes(kv_, li, "q8_0", k[:, kvh].cpu().numpy(), kvh, np.arange(T), ctx.signs, ctx.S)
+            vv_, li = v_views[layer], v_layers[layer]
+            ek, gk = _check_codes(kview, layer, "q8_0", k[:, kvh].cpu().numpy(), kvh, np.arange(T), ctx.signs, ctx.S)
             ev, gv = _check_codes(vv_, li, vfmt, v[:, kvh].cpu().numpy(), kvh, np.arange(T), ctx.signs, ctx.S)
             qr = qs[layer, 0, kvh * G:(kvh + 1) * G].cpu().numpy()
             o_full, bound = _attention(qr, gk, gv, "q8_0", vfmt, ctx.signs, ctx.S, d, 1e-6)
-            got = pick(outs, layer, kvh)
+            got = pick(out, layer, kvh)
             # peaked softmax: what Sparse V drops is far below the parity tolerance
             _compare(got, o_full, ("gpu codes", layer, kvh))
             assert _within_skip_bound(got, o_full, bound)
-            encs[layer, kvh] = (kv_, vv_, li, vfmt, ek, ev, qr)
-        for (layer, kvh), (kv_, vv_, li, vfmt, ek, ev, qr) in encs.items():
-            _replace(kv_, li, "q8_0", ek, kvh, np.arange(T))
+            encs[layer, kvh] = (vv_, li, vfmt, ek, ev, qr)
+        for (layer, kvh), (vv_, li, vfmt, ek, ev, qr) in encs.items():
+            _replace(kview, layer, "q8_0", ek, kvh, np.arange(T))
             _replace(vv_, li, vfmt, ev, kvh, np.arange(T))
-        outs = decode_all()
-        for (layer, kvh), (kv_, vv_, li, vfmt, ek, ev, qr) in encs.items():
+        out = decode_all()
+        for (layer, kvh), (vv_, li, vfmt, ek, ev, qr) in encs.items():
             o_full, bound = _attention(qr, ek, ev, "q8_0", vfmt, ctx.signs, ctx.S, d, 1e-6)
-            got = pick(outs, layer, kvh)
+            got = pick(out, layer, kvh)
             _compare(got, o_full, ("oracle codes", layer, kvh))
             assert _within_skip_bound(got, o_full, bound)
+        assert tq.tq_get_status(ctx.h)[0] == tq.TQ_OK
     finally:
         ctx.close()
 

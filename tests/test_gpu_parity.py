@@ -507,3 +507,57 @@ def test_decode_rejects_bad_arguments(ctx128):
     # context capacity exceeded without a block table
     assert tq.tq_decode_attention(ctx128.h, q, 0, 1, 1, 4, kview, vview, 0, sl, 65, None, 0, 1.0, 0.0, ws,
                                   ws.numel(), out) == tq.TQ_ERR_INVALID_ARG
+
+
+def test_per_layer_views_boundary_v_in_one_call(ctx128):
+    """A per-layer format table: 6 layers, K turbo4 in one view; V q8_0 on the first and the last
+    layer (a 2-layer view) and turbo2_mse between (a 4-layer view).  One tq_encode_kv_layers call
+    and one tq_decode_attention_layers call; the result equals the per-group calls bit for bit (the
+    same 256-token splits) and every query head matches oracle attention over the stored codes."""
+    d, H, Hq, T, L = 128, 2, 8, 700, 6
+    G = Hq // H
+    kview = tq.alloc_view("turbo4", d, H, page_size=T, num_pages=1, n_layers=L)
+    vb = tq.alloc_view("q8_0", d, H, page_size=T, num_pages=1, n_layers=2)
+    vm = tq.alloc_view("turbo2_mse", d, H, page_size=T, num_pages=1, n_layers=4)
+    v_views = [vb, vm, vm, vm, vm, vb]
+    v_layers = [0, 0, 1, 2, 3, 1]
+    k = torch.stack([W.kv_tensor(T, H, d, seed=90 + l, device="cuda", outlier_frac=0.01) for l in range(L)])
+    v = torch.stack([W.kv_tensor(T, H, d, seed=190 + l, device="cuda", outlier_frac=0.01) for l in range(L)])
+    st = tq.tq_encode_kv_layers(ctx128.h, [kview] * L, list(range(L)), v_views, v_layers, L, k, v, T, T * H * d, H * d)
+    assert st == tq.TQ_OK, tq.tq_status_string(st)
+    q = W.normal_tensor((L, 1, Hq, d), seed=91, device="cuda")
+    lens = torch.tensor([T], dtype=torch.int32, device="cuda")
+    nbytes = tq.tq_decode_workspace_bytes(ctx128.h, L, 1, Hq, T)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out = torch.full((L, 1, Hq, d), float("nan"), dtype=torch.float32, device="cuda")
+    st = tq.tq_decode_attention_layers(ctx128.h, q, 0, L, 1, Hq, [kview] * L, list(range(L)), v_views, v_layers,
+                                       lens, T, None, 0, 1 / math.sqrt(d), 1e-6, ws, nbytes, out)
+    assert st == tq.TQ_OK, tq.tq_status_string(st)
+    # the same layers decoded group by group with the plain entry point
+    ref = torch.empty_like(out)
+    for (l0, n, vv, vl0) in ((0, 1, vb, 0), (1, 4, vm, 0), (5, 1, vb, 1)):
+        o = torch.empty((n, 1, Hq, d), dtype=torch.float32, device="cuda")
+        # layer l0 of the K view and layer vl0 of the V view: views advanced by whole layers
+        kvec = H * T
+        ksub = tq.CacheView("turbo4", d, H, T, 1, n,
+                            kview.payload[l0 * kvec * 64:], kview.header[l0 * kvec * 4:])
+        pb, hb = tq.tq_payload_bytes(vv.fmt, d), tq.tq_header_bytes(vv.fmt, d)
+        vsub = tq.CacheView(vv.fmt, d, H, T, 1, n, vv.payload[vl0 * kvec * pb:], vv.header[vl0 * kvec * hb:])
+        ws2 = torch.empty(tq.tq_decode_workspace_bytes(ctx128.h, n, 1, Hq, T), dtype=torch.uint8, device="cuda")
+        assert tq.tq_decode_attention(ctx128.h, q[l0:l0 + n].contiguous(), 0, n, 1, Hq, ksub, vsub, 0, lens, T, None,
+                                      0, 1 / math.sqrt(d), 1e-6, ws2, ws2.numel(), o) == tq.TQ_OK
+        ref[l0:l0 + n] = o
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    # every head against the oracle over the codes stored in each layer's views
+    for l in range(L):
+        vv, vl = v_views[l], v_layers[l]
+        kp, kh = C.read_vectors(kview, l)
+        vp, vh = C.read_vectors(vv, vl)
+        for h in range(H):
+            sl = (0, h)  # page 0, KV head h: [T, bytes]
+            want, _ = C.oracle_attention_on_gpu_codes("turbo4", vv.fmt, d, kp[sl][:, None], kh[sl][:, None],
+                                                      vp[sl][:, None], vh[sl][:, None],
+                                                      q[l, 0, h * G:(h + 1) * G].cpu().numpy(), ctx128.signs,
+                                                      ctx128.S)
+            assert C.rel_err_per_head(out[l, 0, h * G:(h + 1) * G].cpu().numpy(), want).max() < C.ATTN_RTOL, (l, h)
