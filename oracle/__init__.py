@@ -15,4 +15,6 @@ Parity status per function (what pins it, from tests/test_oracle.py):
   decode_attention                pinned: single token, identical keys, tau = 0, GQA mapping,
                                   scipy softmax
   compressed_scores               pinned: equals scale <q, k~> of the dequantised cache
+  prefill_attention               pinned: a one-token chunk equals decode_attention, brute-force
+                                  scalar loops on a tiny input, causality
 """

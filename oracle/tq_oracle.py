@@ -349,6 +349,32 @@ def decode_attention(q: np.ndarray, k_tilde: np.ndarray, v_tilde: np.ndarray,
     return o_full, o_skip
 
 
+def prefill_attention(q: np.ndarray, k_tilde: np.ndarray, v_tilde: np.ndarray, start: int,
+                      scale: float) -> np.ndarray:
+    """Chunked-prefill attention over a dequantised cache, fp64.
+
+    A chunk of C new tokens at positions start .. start + C - 1 attends to the cache, which already
+    holds them ("TurboQuant+: 3.8x compression ...", core content item 1: prefill reads the
+    quantised cache; reading: causal, each token attends to every cached token up to and including
+    its own position).  q [C, Hq, d]; k_tilde, v_tilde [T, Hkv, d] with T >= start + C.  Query
+    head h reads KV head floor(h / G) (reading, as for decode).  For chunk token i:
+    s_j = scale <q_i, k~_j> for j <= start + i; p = softmax(s); o_i = sum_j p_j v~_j.
+    Returns o [C, Hq, d].
+    """
+    C, Hq, d = q.shape
+    T, Hkv, _ = k_tilde.shape
+    G = Hq // Hkv
+    out = np.zeros((C, Hq, d))
+    for i in range(C):
+        n = start + i + 1
+        for h in range(Hq):
+            kv = h // G
+            s = scale * (k_tilde[:n, kv, :] @ np.asarray(q[i, h], dtype=np.float64))
+            e = np.exp(s - np.max(s))
+            out[i, h] = (e / np.sum(e)) @ v_tilde[:n, kv, :]
+    return out
+
+
 def compressed_scores(q: np.ndarray, k_enc: dict, fmt: str, signs, S, scale: float):
     """Scores computed in the compressed domain, without reconstructing K.
 

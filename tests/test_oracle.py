@@ -427,6 +427,55 @@ def test_attention_special_cases():
     np.testing.assert_array_equal(o_full, o_skip)
 
 
+def test_prefill_one_token_chunk_is_decode_attention():
+    # a chunk of one token at position P attends to tokens 0 .. P: the decode step over a cache of
+    # P + 1 tokens
+    rng = np.random.default_rng(11)
+    T, Hkv, Hq, d = 40, 2, 6, 16
+    k = rng.standard_normal((T, Hkv, d))
+    v = rng.standard_normal((T, Hkv, d))
+    for P in (0, 7, 39):
+        q = rng.standard_normal((1, Hq, d))
+        got = O.prefill_attention(q, k, v, P, 0.25)[0]
+        want, _ = O.decode_attention(q[0], k[:P + 1], v[:P + 1], 0.25)
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-14)
+
+
+def test_prefill_matches_brute_force_loops():
+    # every output written out with scalar loops and math.exp (no array softmax, no matrix products)
+    rng = np.random.default_rng(12)
+    T, Hkv, Hq, d, start, C = 9, 2, 4, 3, 5, 4
+    k = rng.standard_normal((T, Hkv, d))
+    v = rng.standard_normal((T, Hkv, d))
+    q = rng.standard_normal((C, Hq, d))
+    got = O.prefill_attention(q, k, v, start, 0.7)
+    for i in range(C):
+        for h in range(Hq):
+            kv = h // (Hq // Hkv)
+            scores = [0.7 * sum(q[i, h, c] * k[j, kv, c] for c in range(d)) for j in range(start + i + 1)]
+            mx = max(scores)
+            w = [math.exp(x - mx) for x in scores]
+            z = sum(w)
+            for c in range(d):
+                assert abs(got[i, h, c] - sum(w[j] * v[j, kv, c] for j in range(len(w))) / z) < 1e-12
+
+
+def test_prefill_is_causal():
+    # a chunk token never sees later tokens: changing keys and values after its position leaves it alone
+    rng = np.random.default_rng(13)
+    T, Hkv, Hq, d, start, C = 30, 1, 2, 8, 20, 10
+    k = rng.standard_normal((T, Hkv, d))
+    v = rng.standard_normal((T, Hkv, d))
+    q = rng.standard_normal((C, Hq, d))
+    a = O.prefill_attention(q, k, v, start, 0.3)
+    k2, v2 = k.copy(), v.copy()
+    k2[25:] += 5.0
+    v2[25:] -= 3.0
+    b = O.prefill_attention(q, k2, v2, start, 0.3)
+    np.testing.assert_array_equal(a[:5], b[:5])  # positions 20 .. 24
+    assert np.abs(a[5:] - b[5:]).max() > 1e-3
+
+
 def test_sparse_v_skip_bound():
     # o_skip differs from o_full by at most tau * sum ||v_j|| (dropped weights < tau each)
     rng = np.random.default_rng(41)
