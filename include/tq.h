@@ -326,6 +326,33 @@ tq_status tq_decode_attention_layers(const tq_context* ctx, const void* q, int q
                                      void* workspace, size_t workspace_bytes,
                                      float* out, tq_stream_t stream);
 
+/* ---- chunked-prefill attention ---- */
+
+/* Bytes of workspace tq_prefill_attention needs (the prepared queries). */
+size_t tq_prefill_workspace_bytes(const tq_context* ctx, int n_tokens, int n_q_heads);
+
+/*
+ * Attention of a prefill chunk over the compressed cache ("TurboQuant+: 3.8x compression ...",
+ * core content item 1: prefill reads the quantised cache).  The chunk's n_tokens tokens sit at
+ * positions start .. start + n_tokens - 1 of one sequence and are already encoded into the cache
+ * (tq_encode_kv); chunk token i attends to the cached tokens 0 .. start + i (causal, its own
+ * token included), with the same compressed-domain scores as tq_decode_attention (q rotated once,
+ * n_j <q', c[idx_j]> + rnorm_j sqrt(pi/2)/d <S q', sign_j>) and no Sparse V.
+ *   q:   device [n_tokens][n_q_heads][d], fp32 (q_is_fp16 = 0) or fp16 (1).
+ *   out: device float [n_tokens][n_q_heads][d].
+ *   Query head h reads KV head h / (n_q_heads / n_kv_heads).
+ *   The sequence: layer `layer` of k_view and v_view; block_table (device int32 [max_blocks],
+ *   logical page -> physical page) or NULL for page `seq` of a contiguous cache.
+ *   workspace: device, tq_prefill_workspace_bytes() bytes, 256-byte aligned.
+ * This build: head_dim 128, K turbo2/3/4 (with the QJL stage), V turbo2/3/4_mse; other formats or
+ * head_dims return TQ_ERR_UNSUPPORTED.  The products run on the fifth-generation tensor cores.
+ * A block-table entry out of range sets status bit 2, and its keys are left out.
+ */
+tq_status tq_prefill_attention(const tq_context* ctx, const void* q, int q_is_fp16, int n_tokens, int n_q_heads,
+                               const tq_cache_view* k_view, const tq_cache_view* v_view, int layer, int seq,
+                               const int32_t* block_table, int max_blocks, int start, float softmax_scale,
+                               void* workspace, size_t workspace_bytes, float* out, tq_stream_t stream);
+
 /* ---- dequantize (reconstruction; test and debugging path) ---- */
 
 /*

@@ -622,4 +622,56 @@ tq_status tq_decode_attention_layers(const tq_context* ctx, const void* q, int q
   return TQ_OK;
 }
 
+// ---------------------------------------------------------------------------
+// chunked-prefill attention
+// ---------------------------------------------------------------------------
+
+size_t tq_prefill_workspace_bytes(const tq_context* ctx, int n_tokens, int n_q_heads) {
+  if (!ctx || n_tokens < 0 || n_q_heads < 1) return 0;
+  return prefill_workspace(n_tokens, n_q_heads, ctx->d);
+}
+
+tq_status tq_prefill_attention(const tq_context* ctx, const void* q, int q_is_fp16, int n_tokens, int n_q_heads,
+                               const tq_cache_view* k_view, const tq_cache_view* v_view, int layer, int seq,
+                               const int32_t* block_table, int max_blocks, int start, float softmax_scale,
+                               void* workspace, size_t workspace_bytes, float* out, tq_stream_t stream) {
+  if (!ctx || !q || !out || !k_view || !v_view) return TQ_ERR_INVALID_ARG;
+  if (q_is_fp16 != 0 && q_is_fp16 != 1) return TQ_ERR_INVALID_ARG;
+  if (n_tokens < 0 || n_q_heads < 1 || start < 0 || layer < 0 || !std::isfinite(softmax_scale))
+    return TQ_ERR_INVALID_ARG;
+  DevView k{}, v{};
+  if (!make_dev_view(k_view, &k) || !make_dev_view(v_view, &v)) return TQ_ERR_INVALID_ARG;
+  if (k.d != ctx->d || v.d != ctx->d || k.H != v.H || k.page_size != v.page_size || k.num_pages != v.num_pages)
+    return TQ_ERR_INVALID_ARG;
+  if (layer >= k.n_layers || layer >= v.n_layers) return TQ_ERR_INVALID_ARG;
+  if (ctx->d != 128) return TQ_ERR_UNSUPPORTED;
+  if (!(format_is_turbo(k.format) && k.has_qjl) || !(format_is_turbo(v.format) && !v.has_qjl))
+    return TQ_ERR_UNSUPPORTED;  // turbo K with its QJL stage, turbo-MSE V
+  if (n_q_heads % k.H != 0) return TQ_ERR_UNSUPPORTED;
+  const long long keys = (long long)start + n_tokens;
+  if (block_table) {
+    if (max_blocks < 1 || (long long)max_blocks * k.page_size < keys) return TQ_ERR_INVALID_ARG;
+  } else if (seq < 0 || seq >= k.num_pages || keys > k.page_size) {
+    return TQ_ERR_INVALID_ARG;  // contiguous: sequence seq is page seq of capacity page_size
+  }
+  if (keys >= (1LL << 31) || (long long)n_tokens * n_q_heads >= (1LL << 31)) return TQ_ERR_UNSUPPORTED;
+  if (n_tokens == 0) return TQ_OK;
+  if (!workspace || workspace_bytes < prefill_workspace(n_tokens, n_q_heads, ctx->d) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return TQ_ERR_WORKSPACE;
+  DecodeArgs qa{};
+  qa.q = q;
+  qa.q_is_fp16 = q_is_fp16;
+  qa.n_layers = 1;
+  qa.batch = n_tokens;
+  qa.n_q_heads = n_q_heads;
+  qa.k = k;
+  qa.v = v;
+  qa.softmax_scale = softmax_scale;
+  qa.out = out;
+  return cuda_status(launch_prefill(ctx->tables, qa, k, v, layer, seq, block_table, max_blocks, start,
+                                    ctx->f16_scale_h[k.idx_bits - 1], ctx->f16_scale_h[v.idx_bits - 1], workspace,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

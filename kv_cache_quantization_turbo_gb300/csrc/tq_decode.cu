@@ -440,6 +440,24 @@ cudaError_t launch_decode_dim(const DecodeKernelArgs& ka, int sm_count, cudaStre
 
 }  // namespace
 
+cudaError_t launch_qprep(const DevTables& t, const DecodeArgs& a, float* qprep, unsigned int* counter,
+                         cudaStream_t s) {
+  DecodeKernelArgs ka{};
+  ka.a = a;
+  ka.tab = t;
+  ka.qprep = qprep;
+  ka.counter = counter;
+  const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
+  if (rows <= 0) return cudaSuccess;
+  switch (t.d) {
+    case 64: qprep_kernel<64><<<(unsigned)rows, 64, 0, s>>>(ka); break;
+    case 128: qprep_kernel<128><<<(unsigned)rows, 128, 0, s>>>(ka); break;
+    case 256: qprep_kernel<256><<<(unsigned)rows, 256, 0, s>>>(ka); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DevTables& t, const DecodeArgs& a, const DecodePlan& plan, void* workspace,
                           int sm_count, cudaStream_t s) {
   DecodeKernelArgs ka;

@@ -111,6 +111,19 @@ struct DecodePlan {
 };
 DecodePlan plan_decode(int sm_count, int d, int n_layers, int batch, int n_q_heads, int max_ctx);
 
+// The decode prologue (q' = scale H diag(s) q, S q') for the rows of a: writes qprep [rows][2d]
+// and zeroes counter[0..1].  Shared by the prefill attention.
+cudaError_t launch_qprep(const DevTables& t, const DecodeArgs& a, float* qprep, unsigned int* counter,
+                         cudaStream_t s);
+
+// Chunked-prefill attention (tq_prefill.cu), head_dim 128, turbo K and turbo-MSE V: the rows of qa
+// (batch = chunk tokens, n_layers = 1) against layer `layer` of k and v; lam_k / lam_v are the
+// fp16 table scales of the K and V index widths.
+size_t prefill_workspace(int n_tokens, int n_q_heads, int d);
+cudaError_t launch_prefill(const DevTables& t, const DecodeArgs& qa, const DevView& k, const DevView& v, int layer,
+                           int seq, const int32_t* block_table, int max_blocks, int start, float lam_k, float lam_v,
+                           void* workspace, cudaStream_t s);
+
 cudaError_t launch_decode(const DevTables& t, const DecodeArgs& a, const DecodePlan& plan,
                           void* workspace, int sm_count, cudaStream_t s);
 

@@ -143,10 +143,54 @@ def _contiguous(a):
     return ctx, f, nbytes, cfg, None
 
 
+def _prefill(a):
+    """Chunked prefill: one sequence of a.ctx cached tokens per layer, the last a.chunk of them the
+    chunk's own; every layer's chunk attends causally over the compressed cache (one
+    tq_prefill_attention call per layer).  Returns the call plus its attention FLOPs: per chunk
+    token i, 2 d (QK) + 2 d (PV) per attended key and query head, and the tensor-core FLOPs the
+    kernel issues (score products with high and low query parts of both score parts: 4 QK
+    products, plus PV; 64-key tiles up to each 128-row tile's last position)."""
+    L, H, Hq, d, T, C = a.layers, a.kv_heads, a.q_heads, a.head_dim, a.ctx, a.chunk
+    start = T - C
+    ctx = tq.tq_context_create(d, 1, 2, W.wht_signs(1, d), W.qjl_matrix(2, d))
+    kview = tq.alloc_view(a.k_format, d, H, page_size=T, num_pages=1, n_layers=L)
+    vview = tq.alloc_view(a.v_format, d, H, page_size=T, num_pages=1, n_layers=L)
+    for l in range(L):
+        k = W.kv_tensor(T, H, d, seed=8000 + 2 * l, device="cuda", outlier_frac=0.01)
+        v = W.kv_tensor(T, H, d, seed=8001 + 2 * l, device="cuda", outlier_frac=0.01)
+        st = tq.tq_encode_kv(ctx, kview, k, vview, v, l, 1, T, T * H * d, H * d)
+        assert st == tq.TQ_OK, tq.tq_status_string(st)
+        del k, v
+    q = W.normal_tensor((L, C, Hq, d), seed=8999, device="cuda")
+    ws_bytes = tq.tq_prefill_workspace_bytes(ctx, C, Hq)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty((L, C, Hq, d), dtype=torch.float32, device="cuda")
+
+    def run():
+        for l in range(L):
+            st = tq.tq_prefill_attention(ctx, q[l], 0, C, Hq, kview, vview, l, 0, None, 0, start, 1.0 / math.sqrt(d),
+                                         ws, ws_bytes, out[l])
+            assert st == tq.TQ_OK, tq.tq_status_string(st)
+    attended = sum(start + i + 1 for i in range(C))
+    useful = L * Hq * attended * 4 * d
+    G = Hq // H
+    rows = C * G
+    tiles = 0
+    for r0 in range(0, rows, 128):
+        last = min(r0 + 128, rows) - 1
+        tiles += (start + last // G + 1 + 63) // 64
+    issued = L * H * tiles * 128 * 64 * d * 2 * 5  # four QK products and one PV product per tile
+    nbytes = L * H * T * (tq.tq_vector_bytes(a.k_format, d) + tq.tq_vector_bytes(a.v_format, d))
+    cfg = {"layers": L, "kv_heads": H, "q_heads": Hq, "head_dim": d, "ctx": T, "chunk": C, "start": start,
+           "k_format": a.k_format, "v_format": a.v_format, "useful_flops": useful, "tensor_flops": issued}
+    return ctx, run, nbytes, cfg, None
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("--workload", required=True, choices=["asym-q8k-turbo2v-needles", "paged-batch64-turbo3",
-                                                         "contiguous"])
+                                                         "contiguous", "prefill"])
+    p.add_argument("--chunk", type=int, default=4096, help="prefill only: chunk tokens (the last of --ctx)")
     p.add_argument("--head-dim", type=int, default=128, choices=[64, 128, 256], help="paged and contiguous")
     p.add_argument("--layers", type=int, default=32, help="contiguous only (as the next five)")
     p.add_argument("--kv-heads", type=int, default=4)
@@ -161,6 +205,8 @@ def main(argv=None):
         raise SystemExit("decode_timing needs a CUDA device")
     if args.workload == "contiguous":
         ctx, run, nbytes, cfg, enc = _contiguous(args)
+    elif args.workload == "prefill":
+        ctx, run, nbytes, cfg, enc = _prefill(args)
     else:
         wl = W.WORKLOADS[args.workload]
         ctx, run, nbytes, cfg, enc = _needles(wl) if args.workload == "asym-q8k-turbo2v-needles" else \
@@ -169,6 +215,12 @@ def main(argv=None):
     line = {"metric": "decode_attention_bandwidth", "value": round(nbytes / dt / 1e9, 1), "unit": "GB/s",
             "ms_per_call": round(dt * 1e3, 4), "algorithmic_bytes": int(nbytes), "calls": args.calls,
             "warmup": args.warmup, "workload": args.workload, "config": cfg, "skip_threshold": 1e-6}
+    if args.workload == "prefill":
+        line["metric"] = "prefill_attention"
+        line["tokens_per_s"] = round(cfg["chunk"] * cfg["layers"] / dt, 1)
+        line["useful_tflops"] = round(cfg["useful_flops"] / dt / 1e12, 2)
+        line["tensor_tflops"] = round(cfg["tensor_flops"] / dt / 1e12, 2)
+        line["skip_threshold"] = 0.0
     if enc is not None:
         encode_layer0, n_tok, enc_bytes = enc
         te = _time(encode_layer0, args.calls, args.warmup)

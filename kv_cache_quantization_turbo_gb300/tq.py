@@ -65,6 +65,8 @@ _SIGS = {
     "tq_encode_kv_layers": (_I, [_P, _VP, _P, _VP, _P, _I, _P, _P, _I, _I64, _I64, _P, _I64, _P]),
     "tq_decode_attention_layers": (_I, [_P, _P, _I, _I, _I, _I, _VP, _P, _VP, _P, _P, _I, _P, _I, _F, _F, _P, _SZ,
                                         _P, _P]),
+    "tq_prefill_workspace_bytes": (_SZ, [_P, _I, _I]),
+    "tq_prefill_attention": (_I, [_P, _P, _I, _I, _I, _VP, _VP, _I, _I, _P, _I, _I, _F, _P, _SZ, _P, _P]),
     "tq_context_tables_hash": (_I, [_P, ctypes.POINTER(ctypes.c_uint64)]),
     "tq_cache_save": (_I, [_P, _VP, _I, ctypes.c_char_p]),
     "tq_cache_file_info": (_I, [ctypes.c_char_p, _VP, ctypes.POINTER(ctypes.c_uint64)]),
@@ -368,3 +370,18 @@ def tq_decode_attention_layers(ctx: int, q, q_is_fp16: int, n_layers: int, batch
                                            _ptr(seq_lens), max_ctx, _ptr(block_table), max_blocks_per_seq,
                                            softmax_scale, skip_threshold, _ptr(workspace), workspace_bytes, _ptr(out),
                                            _stream(stream))
+
+
+# ---- chunked-prefill attention ----
+
+def tq_prefill_workspace_bytes(ctx: int, n_tokens: int, n_q_heads: int) -> int:
+    return _lib.tq_prefill_workspace_bytes(ctx, n_tokens, n_q_heads)
+
+
+def tq_prefill_attention(ctx: int, q, q_is_fp16: int, n_tokens: int, n_q_heads: int, k_view, v_view, layer: int,
+                         seq: int, block_table, max_blocks: int, start: int, softmax_scale: float, workspace,
+                         workspace_bytes: int, out, stream=None) -> int:
+    ka, va = _view_arg(k_view), _view_arg(v_view)
+    return _lib.tq_prefill_attention(ctx, _ptr(q), q_is_fp16, n_tokens, n_q_heads, ka[0], va[0], layer, seq,
+                                     _ptr(block_table), max_blocks, start, softmax_scale, _ptr(workspace),
+                                     workspace_bytes, _ptr(out), _stream(stream))
