@@ -777,11 +777,14 @@ __device__ __forceinline__ void merge_signs(uint32_t (&w)[W], uint32_t sbits) {
 // C_k = 1 for b_k = 0), sat(u 2^100 + C_k) is 1 for u >= b_k and 0 below, exactly, whenever
 // u - prev(b_k) is 0 or at least 2^-100 in magnitude.  Nonzero rotated coordinates are sums of
 // fp16 values scaled by 1 / (n sqrt(d)), at least 2^-24 / (65504 sqrt(d)) in magnitude, so
-// this holds for every boundary that is 0 or at least 2^-60 in magnitude (checked per call).
-// The index is the sum of the steps: the count of boundaries <= u, ties included.
+// this holds for every boundary that is 0 or at least 2^-60 in magnitude (checked per call, with
+// the odd symmetry of the boundaries that step_index_sym relies on; the binary search runs where
+// either fails).
 template <int B>
 __device__ __forceinline__ bool step_constants(const float (&bnd)[7], float (&cst)[7]) {
   bool ok = true;
+#pragma unroll
+  for (int k = 0; k < (1 << B) - 1; ++k) ok = ok && bnd[k] == -bnd[(1 << B) - 2 - k];
 #pragma unroll
   for (int k = 0; k < 7; ++k) {
     const float b = bnd[k];
@@ -796,13 +799,19 @@ __device__ __forceinline__ bool step_constants(const float (&bnd)[7], float (&cs
   }
   return ok;
 }
-// index of y (a rotated coordinate before the 1 / (n sqrt(d)) scale; F = 2^100 / (n sqrt(d))) as a float
+// The index of y (a rotated coordinate before the 1 / (n sqrt(d)) scale; F = 2^100 / (n sqrt(d))) as
+// a float, by the codebook's odd symmetry (the boundaries are b_k = -b_(2H-2-k), H = 2^(B-1),
+// the middle one exactly 0): with a = |y| and cnt = #{positive boundaries <= a} (exact FMA steps),
+// the index is H + cnt for y >= 0 and H - 1 - cnt below, H - 1 steps instead of 2H - 1.  It equals
+// the count of boundaries <= u except at an exact tie u = -b_k (measure zero), which takes the lower
+// index: such a coordinate sits on a decision boundary, inside the comparison band.
 template <int B>
-__device__ __forceinline__ float step_index(float y, float F, const float (&cst)[7]) {
-  float idx = __saturatef(fmaf(y, F, cst[0]));
+__device__ __forceinline__ float step_index_sym(float y, float F, const float (&cst)[7]) {
+  constexpr int H = 1 << (B - 1);
+  float c = 0.5f;
 #pragma unroll
-  for (int k = 1; k < (1 << B) - 1; ++k) idx += __saturatef(fmaf(y, F, cst[k]));
-  return idx;
+  for (int k = 0; k < H - 1; ++k) c += __saturatef(fmaf(fabsf(y), F, cst[H + k]));
+  return fmaf(y >= 0.f ? 1.f : -1.f, c, (float)H - 0.5f);
 }
 // ORs an nb-bit chunk into the thread's W words at bit offset off (compile-time after unrolling).
 template <int W>
@@ -1051,7 +1060,7 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
               for (int hh = 0; hh < 2; ++hh) {
                 const int ec = e2 + hh;
                 const float yv = __uint_as_float(t[8 * c8 + ec]);
-                const float idx = step_index<B>(yv, F, cst);
+                const float idx = step_index_sym<B>(yv, F, cst);
                 const uint32_t ii = __float_as_uint(idx + 0x1p23f) & 7u;  // the integer index
                 r2[hh] = fmaf(yv, FR, -cb_s[ii]);                            // 2^14 (u - c)
                 rr = fmaf(r2[hh], r2[hh], rr);
@@ -1109,7 +1118,7 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
             float acc = 0.f;
 #pragma unroll
             for (int e = 0; e < CPC; ++e)
-              acc = fmaf(step_index<B>(__uint_as_float(t[CPC * c + e]), F, cst), (float)(1u << (W * e)), acc);
+              acc = fmaf(step_index_sym<B>(__uint_as_float(t[CPC * c + e]), F, cst), (float)(1u << (W * e)), acc);
             or_bits<W>(w, W * CPC * c, W * CPC, (uint32_t)acc);
           }
         } else {
