@@ -402,12 +402,13 @@ cudaError_t launch_attend_mma_heads(const DecodeKernelArgs& ka, int d, int sm_co
   return cudaErrorInvalidValue;
 }
 
-// Up to 8 query heads per KV head: one work item per (layer x sequence, KV head, split).  9 to 16:
-// each item runs twice, on the two halves of the KV head's query heads (ceil(G/2) and the rest),
+// Up to 8 query heads per KV head, or up to 16 at d <= 128: one work item per (layer x sequence,
+// KV head, split), all heads scored from each dequantised tile.  9 to 16 at d = 256: each item
+// runs twice, on the two halves of the KV head's query heads (ceil(G/2) and the rest),
 // as consecutive values of the work counter, so the two halves of an item run at about the same
 // time and the second read of each tile is served by L2: the cache is read from HBM about once.
 cudaError_t launch_attend_mma(const DecodeKernelArgs& ka, int d, int sm_count, cudaStream_t s) {
-  if (ka.G <= 8) return launch_attend_mma_heads(ka, d, sm_count, s);
+  if (ka.G <= 8 || d <= 128) return launch_attend_mma_heads(ka, d, sm_count, s);  // d <= 128: 16 heads at once
   DecodeKernelArgs two = ka;
   two.g_off = 0;
   two.g_cnt = (ka.G + 1) / 2;

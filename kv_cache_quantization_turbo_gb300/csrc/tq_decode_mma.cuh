@@ -1,9 +1,9 @@
 // Split-K decode attention on tensor cores, parameterised by the cache formats: turbo K with
 // W-bit codes (W - 1 index bits + the QJL sign bit; turbo2/3/4), turbo-MSE V with W-bit indices
-// (turbo2/3/4_mse), and q8_0 K or V, at head_dim 64, 128 or 256, up to 8 query heads per KV head
-// per work item (query heads g_off .. g_off + g_cnt - 1 of each KV head's G; with 9 to 16 every
-// item runs twice, on the two halves, as consecutive work-counter values).  One partial (m, l,
-// acc) per query row and split, combined afterwards.
+// (turbo2/3/4_mse), and q8_0 K or V, at head_dim 64, 128 or 256, up to 16 query heads per KV head
+// per work item at d <= 128 (up to 8 at d = 256: with 9 to 16 every item runs twice there, on the
+// two halves of the heads, as consecutive work-counter values).  One partial (m, l, acc) per query
+// row and split, combined afterwards.
 //
 // Why tensor cores: at HBM speed one 16-token tile of one KV head (1888 B for turbo4 / turbo4_mse
 // at d = 128) leaves ~350 warp instructions per SM, and scoring it on CUDA cores takes ~3 G d
@@ -110,8 +110,8 @@ struct Fmt {
   static constexpr uint32_t Big = KLut > VLut ? KLut : VLut, Small = KLut > VLut ? VLut : KLut;
 };
 
-// Launch shape of one kernel: NQ 8-column products per part (1: up to 4 query heads per KV head,
-// 2: up to 8); per warp a block of two P' tiles and the query fragments (8 bytes per lane, product
+// Launch shape of one kernel: NQ 8-column products per part (1: up to 4 query heads per KV head as
+// high / low parts, 2: up to 8, 4: up to 16); per warp a block of P' tiles and the query fragments (8 bytes per lane, product
 // and k step); the two tables.  Shared layout (attend_mma_kernel): the larger table on the first
 // boundary of its size, the smaller table right below it (else right above), as many warp blocks
 // as fit below that from the start, the others above the tables; whatever the start's alignment,
@@ -119,22 +119,24 @@ struct Fmt {
 // gap below the larger table holds every warp block.  16 warps (d = 256: 8, for its ~180
 // registers a thread), halved until the shared memory fits.
 constexpr int kSmemLimit = 227 * 1024;
-template <class F, bool HILO>
+template <class F, int NQ_>
 struct Shape {
-  static constexpr int NQ = HILO ? 1 : 2;
+  static constexpr int NQ = NQ_;
+  static constexpr bool HILO = NQ == 1;
+  static constexpr int NV = HILO ? 1 : NQ / 2;  // 8-column V products (P' tiles) per tile
   // Tiles a warp works on at once: two (two independent chains of loads, lookups and products,
   // one query-fragment read for both) where the registers allow it, that is with up to 4 query
   // heads per KV head at d <= 128, run with 12 warps of up to 168 registers; else one.
   static constexpr int NT = (HILO && F::D <= 128) ? 2 : 1;
   static constexpr int QfBytes = F::KS * 256 * (F::KQ8 ? 1 : 2) * NQ;
-  static constexpr int PsBytes = 512 * NT;
+  static constexpr int PsBytes = 512 * NT * NV;
   static constexpr int Block = PsBytes + QfBytes;
   static constexpr int smem(int warps) {
     const int packed = (int)(F::Big + F::Small) + warps * Block + ((int)F::Small > Block ? (int)F::Small : Block);
     const int gap = (int)(2 * F::Big + F::Small);
     return packed > gap ? packed : gap;
   }
-  static constexpr int W0 = F::D == 256 ? 8 : (NT == 2 ? 12 : 16);
+  static constexpr int W0 = F::D == 256 ? 8 : (NT == 2 ? 12 : (NQ == 4 ? 8 : 16));
   static constexpr int Warps = smem(W0) <= kSmemLimit ? W0 : smem(W0 / 2) <= kSmemLimit ? W0 / 2 : W0 / 4;
   static constexpr int Threads = 32 * Warps;
   static constexpr int Smem = smem(Warps);
@@ -192,10 +194,12 @@ struct Cursor {
   bool ok;                                 // page in range
 };
 
-template <class F, bool HILO>
+template <class F, int NQ>
 struct MmaWarp {
   static constexpr int D = F::D, KS = F::KS;
-  static constexpr int NH = HILO ? 1 : 2;  // query heads per thread: t (and t + 4); = 8-column products per part
+  static constexpr bool HILO = NQ == 1;
+  // head slots per thread (heads t, t + 4, t + 8, t + 12) = 8-column products per part; V products
+  static constexpr int NH = NQ, NV = Shape<F, NQ>::NV;
 
   struct KTile {
     uint32_t a[F::KLoad], b[F::KLoad];  // tokens g, g + 8
@@ -223,7 +227,10 @@ struct MmaWarp {
   Cursor c;
   KTile kn[2];  // the next pair's K and V, loaded one phase ahead (pipelined pair steps)
   VTile vn[2];
-  float oacc[KS][4];
+  // V accumulators of product v: entries 0, 1 = row g, columns 2t, 2t + 1; 2, 3 = row g + 8.  Up to
+  // 4 heads: the columns are head t's high and low parts; more: column 2t = head slot 2v (head
+  // t + 8v), column 2t + 1 = head slot 2v + 1 (head t + 8v + 4).
+  float oacc[NV][KS][4];
   float m[NH], l[NH];
 
   __device__ __forceinline__ MmaWarp(const DecodeLaunch& k_) : k(k_) {}
@@ -390,10 +397,10 @@ struct MmaWarp {
       for (int mt = 0; mt < KS; ++mt) {
         if (HILO) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) oacc[mt][e] *= al;
+          for (int e = 0; e < 4; ++e) oacc[0][mt][e] *= al;
         } else {
-          oacc[mt][h] *= al;
-          oacc[mt][2 + h] *= al;
+          oacc[h >> 1][mt][h & 1] *= al;
+          oacc[h >> 1][mt][2 + (h & 1)] *= al;
         }
       }
       m[h] = mn;
@@ -470,8 +477,8 @@ struct MmaWarp {
     }
   }
 
-  // V product of a tile with the P' fragments bp.
-  __device__ __forceinline__ void accumulate_v(const VTile& V, uint2 bp) {
+  // V products of a tile with the P' fragments bp[v] of product v.
+  __device__ __forceinline__ void accumulate_v(const VTile& V, const uint2 (&bp)[NV]) {
     if constexpr (F::VQ8) {
       const __half2 d01 = u32_as_h2(V.h0), d23 = u32_as_h2(V.h1);
 #pragma unroll
@@ -484,7 +491,8 @@ struct MmaWarp {
         const uint32_t a1 = h2_as_u32(__hmul2(u32_as_h2(i8x2_to_h2<0x4342>(x01)), d01));
         const uint32_t a2 = h2_as_u32(__hmul2(u32_as_h2(i8x2_to_h2<0x4140>(x23)), d23));
         const uint32_t a3 = h2_as_u32(__hmul2(u32_as_h2(i8x2_to_h2<0x4342>(x23)), d23));
-        mma_16816(oacc[mt], a0, a1, a2, a3, bp.x, bp.y);
+#pragma unroll
+        for (int v = 0; v < NV; ++v) mma_16816(oacc[v][mt], a0, a1, a2, a3, bp[v].x, bp[v].y);
       }
     } else {
       constexpr int N = 2 * F::WV;
@@ -497,8 +505,10 @@ struct MmaWarp {
 #pragma unroll
         for (int q = 0; q < 4; ++q) e[q] = lds32(run_addr<N, 7>(r[q], 2 * mt * F::WV, ylv));
         // a0/a1: slots 2t, 2t+1 = tokens t, t+8 at coordinate 2mt / 2mt+1; a2/a3: tokens t+4, t+12
-        mma_16816(oacc[mt], __byte_perm(e[0], e[1], 0x5410), __byte_perm(e[0], e[1], 0x7632),
-                  __byte_perm(e[2], e[3], 0x5410), __byte_perm(e[2], e[3], 0x7632), bp.x, bp.y);
+        const uint32_t a0 = __byte_perm(e[0], e[1], 0x5410), a1 = __byte_perm(e[0], e[1], 0x7632);
+        const uint32_t a2 = __byte_perm(e[2], e[3], 0x5410), a3 = __byte_perm(e[2], e[3], 0x7632);
+#pragma unroll
+        for (int v = 0; v < NV; ++v) mma_16816(oacc[v][mt], a0, a1, a2, a3, bp[v].x, bp[v].y);
       }
     }
   }
@@ -616,21 +626,31 @@ struct MmaWarp {
     for (int j = 0; j < NT; ++j) {
       float2 nv = make_float2(1.f, 1.f);
       if constexpr (!F::VQ8) nv = __half22float2(u32_as_h2(vc[j].h0));
-      const uint32_t buf = kBuf + 256 * j;
       if (HILO) {
+        const uint32_t buf = kBuf + 256 * j;
         const float w0 = p[j][0][0] * nv.x, w1 = p[j][0][1] * nv.y;
         const __half2 hi = __floats2half2_rn(w0, w1);
         const float2 hf = __half22float2(hi);
         sts32(psw0 + buf, h2_as_u32(hi));
         sts32(psw1 + buf, h2_as_u32(__floats2half2_rn(w0 - hf.x, w1 - hf.y)));
       } else {
-        sts32(psw0 + buf, h2_as_u32(__floats2half2_rn(p[j][0][0] * nv.x, p[j][0][1] * nv.y)));
-        sts32(psw1 + buf, h2_as_u32(__floats2half2_rn(p[j][NH - 1][0] * nv.x, p[j][NH - 1][1] * nv.y)));
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {  // P' tile v: head slots 2v (column 2t) and 2v + 1 (column 2t + 1)
+          const uint32_t buf = kBuf + 256 * (j * NV + v);
+          sts32(psw0 + buf, h2_as_u32(__floats2half2_rn(p[j][2 * v][0] * nv.x, p[j][2 * v][1] * nv.y)));
+          sts32(psw1 + buf,
+                h2_as_u32(__floats2half2_rn(p[j][2 * v + 1][0] * nv.x, p[j][2 * v + 1][1] * nv.y)));
+        }
       }
     }
     __syncwarp();
 #pragma unroll
-    for (int j = 0; j < NT; ++j) accumulate_v(vc[j], lds64_v(psr + kBuf + 256 * j));
+    for (int j = 0; j < NT; ++j) {
+      uint2 bp[NV];
+#pragma unroll
+      for (int v = 0; v < NV; ++v) bp[v] = lds64_v(psr + kBuf + 256 * (j * NV + v));
+      accumulate_v(vc[j], bp);
+    }
   }
 
   // A pair of whole tiles whose K and V were loaded into kn / vn by the previous step; their
@@ -715,7 +735,10 @@ struct MmaWarp {
       }
       __syncwarp();
 #pragma unroll
-      for (int j = 0; j < 2; ++j) accumulate_v(vc[j], lds64_v(psr + kBuf + 256 * j));
+      for (int j = 0; j < 2; ++j) {
+        const uint2 bp[1] = {lds64_v(psr + kBuf + 256 * j)};
+        accumulate_v(vc[j], bp);
+      }
     }
     __syncwarp();
     if (MORE) {
@@ -790,7 +813,10 @@ struct MmaWarp {
     }
     __syncwarp();
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
+    for (int v = 0; v < NV; ++v) {
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) oacc[v][mt][0] = oacc[v][mt][1] = oacc[v][mt][2] = oacc[v][mt][3] = 0.f;
+    }
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
       m[h] = -INFINITY;
@@ -808,9 +834,9 @@ struct MmaWarp {
       // step's writes never meet the previous step's reads
       // (every step call uses buf, then flips it)
       uint32_t buf = 0;
-      constexpr uint32_t kHalf = 256 * Shape<F, HILO>::NT;
+      constexpr uint32_t kHalf = 256 * Shape<F, NQ>::NT * Shape<F, NQ>::NV;
       int tile = 0;
-      if constexpr (Shape<F, HILO>::NT == 2) {
+      if constexpr (Shape<F, NQ>::NT == 2) {
         // leading pairs of whole tiles, pipelined; the rest (at most two tiles, the last one
         // possibly ragged) runs below
         const int np = (last_valid == 16 ? ntiles : ntiles - 1) / 2;
@@ -849,7 +875,7 @@ struct MmaWarp {
           break;
         }
         const bool last = tile + 2 >= ntiles;
-        if constexpr (Shape<F, HILO>::NT == 2) {
+        if constexpr (Shape<F, NQ>::NT == 2) {
           Cursor c1 = c;
           advance(c1);
           if (c.ok && c1.ok) {
@@ -891,11 +917,11 @@ struct MmaWarp {
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) {
         if (HILO) {
-          v[2 * mt] = (oacc[mt][0] + oacc[mt][1]) * inv_lam;
-          v[2 * mt + 1] = (oacc[mt][2] + oacc[mt][3]) * inv_lam;
+          v[2 * mt] = (oacc[0][mt][0] + oacc[0][mt][1]) * inv_lam;
+          v[2 * mt + 1] = (oacc[0][mt][2] + oacc[0][mt][3]) * inv_lam;
         } else {
-          v[2 * mt] = oacc[mt][h] * inv_lam;
-          v[2 * mt + 1] = oacc[mt][2 + h] * inv_lam;
+          v[2 * mt] = oacc[h >> 1][mt][h & 1] * inv_lam;
+          v[2 * mt + 1] = oacc[h >> 1][mt][2 + (h & 1)] * inv_lam;
         }
       }
       float* dst = k.partial + ((row0 + gof + head) * k.n_splits + split) * (D + 4);
@@ -918,9 +944,9 @@ struct MmaWarp {
   }
 };
 
-template <class F, bool HILO>
-__global__ void __launch_bounds__(Shape<F, HILO>::Threads, 1) attend_mma_kernel(DecodeLaunch k) {
-  using L = Shape<F, HILO>;
+template <class F, int NQ>
+__global__ void __launch_bounds__(Shape<F, NQ>::Threads, 1) attend_mma_kernel(DecodeLaunch k) {
+  using L = Shape<F, NQ>;
   extern __shared__ __align__(16) unsigned char sm[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -962,7 +988,7 @@ __global__ void __launch_bounds__(Shape<F, HILO>::Threads, 1) attend_mma_kernel(
   }
   __syncthreads();
 
-  MmaWarp<F, HILO> w(k);
+  MmaWarp<F, NQ> w(k);
   w.init_lane(lane);
   w.ylk = (sbase + kofs) | ((uint32_t)lane << 2);
   w.ylv = (sbase + vofs) | ((uint32_t)lane << 2);
@@ -985,16 +1011,16 @@ __global__ void __launch_bounds__(Shape<F, HILO>::Threads, 1) attend_mma_kernel(
   }
 }
 
-template <class F, bool HILO>
+template <class F, int NQ>
 cudaError_t launch_shape(const DecodeLaunch& k, long long items, int sm_count, cudaStream_t s) {
-  using L = Shape<F, HILO>;
+  using L = Shape<F, NQ>;
   long long grid = sm_count;  // one persistent CTA per SM
   if (items < grid * L::Warps) grid = (items + L::Warps - 1) / L::Warps;
   if (grid < 1) grid = 1;
   const cudaError_t e =
-      cudaFuncSetAttribute(attend_mma_kernel<F, HILO>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::Smem);
+      cudaFuncSetAttribute(attend_mma_kernel<F, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::Smem);
   if (e != cudaSuccess) return e;
-  attend_mma_kernel<F, HILO><<<(unsigned)grid, L::Threads, L::Smem, s>>>(k);
+  attend_mma_kernel<F, NQ><<<(unsigned)grid, L::Threads, L::Smem, s>>>(k);
   return cudaGetLastError();
 }
 
@@ -1002,7 +1028,13 @@ template <class F>
 cudaError_t launch_mma(const DecodeLaunch& k, int sm_count, cudaStream_t s) {
   const long long items = (long long)k.a.n_layers * k.a.batch * k.a.k.H * k.n_splits * k.g_halves;
   if (items >= (1LL << 32)) return cudaErrorInvalidValue;
-  return k.g_cnt <= 4 ? launch_shape<F, true>(k, items, sm_count, s) : launch_shape<F, false>(k, items, sm_count, s);
+  if (k.g_cnt <= 4) return launch_shape<F, 1>(k, items, sm_count, s);
+  if constexpr (F::D > 128) {
+    return launch_shape<F, 2>(k, items, sm_count, s);
+  } else {
+    if (k.g_cnt <= 8) return launch_shape<F, 2>(k, items, sm_count, s);
+    return launch_shape<F, 4>(k, items, sm_count, s);  // 9 to 16 heads: each tile dequantised once for all
+  }
 }
 
 }  // namespace mmad

@@ -316,12 +316,13 @@ def _mma_oracle(ctx, fmt, is_k):
     return _mma_codes[key]
 
 
-@pytest.mark.parametrize("G", [4, 8])
+@pytest.mark.parametrize("G", [4, 8, 16])
 @pytest.mark.parametrize("vfmt", MMA_V)
 @pytest.mark.parametrize("kfmt", MMA_K)
 def test_decode_tensor_core_format_pairs_paged(ctx, kfmt, vfmt, G):
     """Every K x V format pair of the tensor-core decode kernels at head_dim 64/128/256, with
-    4 query heads per KV head (high/low fp16 query columns) and 8 (two heads per column pair):
+    4 query heads per KV head (high/low fp16 query columns), 8 (two heads per column pair) and 16
+    (four query products, two V products; at d 256 two head halves per work item):
     16-token pages in shuffled order, lengths 0, 1, 17, 300, 613 (ragged tiles, several
     256-token splits), Sparse V at 1e-6; identical codes on both sides."""
     d, H, P = ctx.d, 2, 16
