@@ -8,9 +8,10 @@
 // tcgen05.mma with the accumulators in tensor memory.
 //
 // One CTA = 128 query rows of one KV head (row r = chunk token r / G, query head r % G of the
-// KV head's group), four warps, one row per thread.  Per tile of 64 keys:
-//   1. every thread dequantises half of one token: the codebook part lambda_K c[idx] and the
-//      QJL sign part +-1 of K into two K-major operand tiles [64 tokens x 128], and V^T (the
+// KV head's group), eight warps: warps 0-3 hold one row per thread.  Per tile of 64 keys:
+//   1. every thread dequantises a quarter of one token: the codebook part lambda_K c[idx] and the
+//      QJL sign part +-1 of K (turbo4: one table read per code byte) into two K-major operand
+//      tiles [64 tokens x 128], and V^T (the
 //      operand of the value product, lambda_V c_V[idx]) into [128 coordinates x 64 tokens]; the
 //      per-token norms go to small arrays;
 //   2. thread 0 issues the score products S_cb = (q'_hi + q'_lo) K_cb^T and
@@ -39,7 +40,7 @@ namespace pf {
 constexpr int D = 128;        // head_dim of this kernel
 constexpr int M = 128;        // query rows per CTA
 constexpr int NK = 64;        // keys per tile
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // warps 0-3: one query row per thread; all 8 warps dequantise
 constexpr uint32_t kTmemCols = 256;  // S_cb [0, 64), S_qjl [64, 128), O [128, 256)
 constexpr float kLazy = 8.0f;  // log2 units: rescale O when the row max passes the reference by this
 
@@ -64,7 +65,8 @@ struct Smem {  // byte offsets from a 1024-byte boundary
   static constexpr int p = vt + D * NK * 2;     // [128 x 64]
   static constexpr int hdr = p + M * NK * 2;    // float kn[64], kr[64], vn[64]
   static constexpr int tab = hdr + 3 * NK * 4;  // fp16 cb_k[8], cb_v[8]
-  static constexpr int bar = tab + 32;          // mbarriers: scores done, values done
+  static constexpr int kbt = tab + 32;          // turbo4 K: uint2 [256] per code byte: codebook pair, sign pair
+  static constexpr int bar = kbt + 256 * 8;     // mbarriers: scores done, values done
   static constexpr int slot = bar + 16;         // tensor-memory address
   static constexpr int total = slot + 16;
   static constexpr int alloc = total + 1024;    // room to align the base
@@ -89,6 +91,11 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 __device__ __forceinline__ float lo_part(float x) { return x - __half2float(__float2half_rn(x)); }
+__device__ __forceinline__ float fast_ex2(float x) {  // 2^x; -inf -> 0
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // Code of coordinate c (compile-time after unrolling) in the little-endian stream w of W-bit codes.
 template <int W, int NW>
@@ -128,13 +135,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     cbk[tid] = __float2half_rn(tid < (1 << BK) ? a.tab.f16_scale[BK - 1] * a.tab.centroids[(BK - 1) * 8 + tid] : 0.f);
     cbv[tid] = __float2half_rn(tid < (1 << WV) ? a.tab.f16_scale[WV - 1] * a.tab.centroids[(WV - 1) * 8 + tid] : 0.f);
   }
+  if constexpr (WK == 4) {  // a byte of turbo4 K codes = two coordinates: their codebook pair and sign pair
+    const float lam = a.tab.f16_scale[BK - 1];
+    const float* cb = a.tab.centroids + (BK - 1) * 8;
+    const uint32_t b = tid;  // 256 threads, 256 bytes
+    const __half2 c2 = __floats2half2_rn(lam * cb[b & 7u], lam * cb[(b >> 4) & 7u]);
+    const __half2 s2 = __floats2half2_rn((b & 8u) ? 1.f : -1.f, (b & 128u) ? 1.f : -1.f);
+    *reinterpret_cast<uint2*>(sm + Smem::kbt + 8 * b) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&c2), *reinterpret_cast<const uint32_t*>(&s2));
+  }
 
-  // ---- the query operands: thread = row, high and low fp16 parts of q' and S q' ----
-  const int r = tid;
+  // ---- the query operands: thread = row (warps 0-3), high and low fp16 parts of q' and S q' ----
+  const bool row_warp = warp < 4;
+  const int r = tid & (M - 1);
   const int rho = row0 + r, ti = rho / G, gi = rho - ti * G;
-  const bool row_ok = ti < a.n_tokens;
+  const bool row_ok = row_warp && ti < a.n_tokens;
   const int pos = a.start + ti;  // this row's position: it attends to keys 0 .. pos
-  {
+  if (row_warp) {
     const float* qp = a.qprep + ((long long)ti * Hq + kvh * G + gi) * 2 * D;
 #pragma unroll 1
     for (int c8 = 0; c8 < D / 8; ++c8) {
@@ -173,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *slot;
-  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;  // a warp's tensor-memory lane quarter
   const uint32_t t_cb = tmem, t_q = tmem + 64, t_o = tmem + 128;
 
   // keys this CTA reads: up to the last row's position; keys beyond the chunk are never attended
@@ -186,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
   float m = -INFINITY, l = 0.f;
   bool ok = true;  // every bounded wait so far completed
-  const int tt = tid & (NK - 1), half = tid >> 6;  // dequantisation: token tt of the tile, coordinates 64 half ..
+  const int tt = tid & (NK - 1), qt = tid >> 6;  // dequantisation: token tt of the tile, coordinates 32 qt ..
   for (int jt = 0; jt < n_tiles && ok; ++jt) {
     // the previous value product has read P and V^T before they are overwritten; every wait's
     // outcome is made CTA-uniform, so that no thread leaves the loop while others wait at a barrier
@@ -204,17 +221,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (a.block_table) {
           page = lp < a.max_blocks ? a.block_table[lp] : -1;
           if (page < 0 || page >= K.num_pages) {
-            if (half == 0) atomicOr(a.tab.status, kFlagBlockTable);
+            if (qt == 0) atomicOr(a.tab.status, kFlagBlockTable);
             valid = false;
           }
         }
         vec = (long long)a.layer * vec_layer + (page * K.H + kvh) * K.page_size + (j - lp * K.page_size);
       }
-      constexpr int NWK = 2 * WK, NWV = 2 * WV;  // 32-bit words of 64 codes
+      constexpr int NWK = WK, NWV = WV;  // 32-bit words of this thread's 32 codes
       uint32_t wk[NWK], wv[NWV];
       if (valid) {
-        const uint32_t* pk = reinterpret_cast<const uint32_t*>(K.payload + vec * K.pay_bytes) + half * NWK;
-        const uint32_t* pv = reinterpret_cast<const uint32_t*>(V.payload + vec * V.pay_bytes) + half * NWV;
+        const uint32_t* pk = reinterpret_cast<const uint32_t*>(K.payload + vec * K.pay_bytes) + qt * NWK;
+        const uint32_t* pv = reinterpret_cast<const uint32_t*>(V.payload + vec * V.pay_bytes) + qt * NWV;
 #pragma unroll
         for (int i = 0; i < NWK; ++i) wk[i] = __ldg(pk + i);
 #pragma unroll
@@ -227,22 +244,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
       const __half hz = __float2half_rn(0.f), hp1 = __float2half_rn(1.f), hm1 = __float2half_rn(-1.f);
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {  // coordinates 64 half + 8 c8 .. + 7
-        __half cbv8[8], sgv8[8];
+      for (int c8 = 0; c8 < 4; ++c8) {  // coordinates 32 qt + 8 c8 .. + 7
+        uint4 kcb, ksg;
+        if constexpr (WK == 4) {  // one table read per code byte (two coordinates)
+          uint2 e[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) e[b] = *reinterpret_cast<const uint2*>(sm + Smem::kbt + 8 * ((wk[c8] >> (8 * b)) & 255u));
+          kcb = make_uint4(e[0].x, e[1].x, e[2].x, e[3].x);
+          ksg = make_uint4(e[0].y, e[1].y, e[2].y, e[3].y);
+          if (!valid) kcb = ksg = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          __half cbv8[8], sgv8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t code = code_at<WK, NWK>(wk, 8 * c8 + e);
+            cbv8[e] = valid ? cbk[code & ((1u << BK) - 1u)] : hz;
+            sgv8[e] = valid ? (((code >> BK) & 1u) ? hp1 : hm1) : hz;
+          }
+          kcb = *reinterpret_cast<const uint4*>(cbv8);
+          ksg = *reinterpret_cast<const uint4*>(sgv8);
+        }
+        const int o = swz<NK>(tt, 32 * qt + 8 * c8);
+        *reinterpret_cast<uint4*>(sm + Smem::kcb + o) = kcb;
+        *reinterpret_cast<uint4*>(sm + Smem::ksg + o) = ksg;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const uint32_t code = code_at<WK, NWK>(wk, 8 * c8 + e);
-          cbv8[e] = valid ? cbk[code & ((1u << BK) - 1u)] : hz;
-          sgv8[e] = valid ? (((code >> BK) & 1u) ? hp1 : hm1) : hz;
           const uint32_t vc = code_at<WV, NWV>(wv, 8 * c8 + e);
-          const int c = 64 * half + 8 * c8 + e;
-          *reinterpret_cast<__half*>(sm + Smem::vt + swz<D>(c, tt)) = valid ? cbv[vc] : hz;
+          *reinterpret_cast<__half*>(sm + Smem::vt + swz<D>(32 * qt + 8 * c8 + e, tt)) = valid ? cbv[vc] : hz;
         }
-        const int o = swz<NK>(tt, 64 * half + 8 * c8);
-        *reinterpret_cast<uint4*>(sm + Smem::kcb + o) = *reinterpret_cast<const uint4*>(cbv8);
-        *reinterpret_cast<uint4*>(sm + Smem::ksg + o) = *reinterpret_cast<const uint4*>(sgv8);
       }
-      if (half == 0) {
+      if (qt == 0) {
         float n = 0.f, rn = 0.f, nv = 0.f;
         if (valid) {
           const __half* hk = reinterpret_cast<const __half*>(K.header + vec * K.hdr_bytes);
@@ -276,7 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     ok = __syncthreads_and(tc::mbar_wait(bar_s, (uint32_t)jt & 1u));
     if (!ok) break;
     tc::fence_after_sync();
-    // ---- 3. online softmax of this row; P into the value product's A operand ----
+    // ---- 3. online softmax of this row (warps 0-3, warp-uniform); P into the value product's A operand ----
+    if (row_warp) {
     float s[NK];
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {
@@ -321,13 +353,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
       for (int e2 = 0; e2 < 4; ++e2) {
         const int j0 = 8 * c8 + 2 * e2;
-        const float p0 = s[j0] == -INFINITY ? 0.f : exp2f(s[j0] - m);
-        const float p1 = s[j0 + 1] == -INFINITY ? 0.f : exp2f(s[j0 + 1] - m);
+        const float p0 = s[j0] == -INFINITY ? 0.f : fast_ex2(s[j0] - m);
+        const float p1 = s[j0 + 1] == -INFINITY ? 0.f : fast_ex2(s[j0 + 1] - m);
         l += p0 + p1;
         pk[e2] = pack_h2(p0 * vn_s[j0], p1 * vn_s[j0 + 1]);
       }
       *reinterpret_cast<uint4*>(sm + Smem::p + swz<M>(r, 8 * c8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
+    }  // row warps
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
@@ -346,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   ok = __syncthreads_and(ok);
   tc::fence_after_sync();
   // ---- epilogue: O / l / lambda_V, then diag(s) H (the inverse rotation), one row per thread ----
-  if (ok && n_tiles > 0) {  // CTA-uniform: the tensor-memory loads below are warp-collective
+  if (ok && n_tiles > 0 && row_warp) {  // warp-uniform: the tensor-memory loads below are warp-collective
     float o[D];
 #pragma unroll
     for (int c32 = 0; c32 < D / 32; ++c32) {
