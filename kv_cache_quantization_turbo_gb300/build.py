@@ -17,7 +17,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtq.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["tq_api.cpp", "tq_encode.cu", "tq_decode.cu", "tq_decode_mma64.cu", "tq_decode_mma128.cu",
-           "tq_decode_mma256.cu", "tq_decode_tc.cu", "tq_decode_static.cu", "tq_dequant.cu", "tq_persist.cpp",
+           "tq_decode_mma256.cu", "tq_decode_static.cu", "tq_dequant.cu", "tq_persist.cpp",
            "tq_prefill.cu"]
 
 

@@ -16,7 +16,6 @@
 //   3. combine (one CTA of 4 warps per query row): log-sum-exp merge of the
 //      partials, acc / l, then diag(s) H back to the original space for turbo V.
 #include <cmath>
-#include <cstdlib>
 
 #include <cuda_fp16.h>
 
@@ -393,23 +392,6 @@ bool attend_mma_supported(const DecodeKernelArgs& ka, int d) {
   return false;
 }
 
-// The kernel with the score products on tcgen05 (tq_decode_tc.cu) takes turbo K (QJL) with
-// turbo-MSE V at head_dim 128, up to 16 query heads per KV head, splits of whole 32-token tiles,
-// pages of a multiple of 16 tokens.  Opt-in (TQ_DECODE_TC=1 in the environment): measured slower
-// than the mma.sync kernel on the 32K-context workloads.
-bool attend_tc_supported(const DecodeKernelArgs& ka, int d) {
-  static const bool on = [] {
-    const char* e = std::getenv("TQ_DECODE_TC");
-    return e != nullptr && e[0] == '1';
-  }();
-  if (!on || d != 128) return false;
-  const DecodeArgs& a = ka.a;
-  if (ka.G < 1 || ka.G > 16 || ka.split_tokens % 32 != 0) return false;
-  if (a.block_table != nullptr && a.k.page_size % 16 != 0) return false;
-  const int wk = mma_k_width(a.k), wv = mma_v_width(a.v);
-  return wk >= 0 && wv >= 0 && tc_decode_has(wk, wv);
-}
-
 cudaError_t launch_attend_mma_heads(const DecodeKernelArgs& ka, int d, int sm_count, cudaStream_t s) {
   const int wk = mma_k_width(ka.a.k), wv = mma_v_width(ka.a.v);
   switch (d) {
@@ -439,12 +421,6 @@ cudaError_t launch_decode_dim(const DecodeKernelArgs& ka, int sm_count, cudaStre
   const DecodeArgs& a = ka.a;
   const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
   qprep_kernel<D><<<(unsigned)rows, D, 0, s>>>(ka);
-  if (attend_tc_supported(ka, D)) {
-    const cudaError_t e = tc_decode_launch(ka, mma_k_width(a.k), mma_v_width(a.v), sm_count, s);
-    if (e != cudaSuccess) return e;
-    combine_kernel<D><<<(unsigned)rows, 32 * kCombineWarps, 0, s>>>(ka);
-    return cudaGetLastError();
-  }
   if (attend_mma_supported(ka, D)) {
     const cudaError_t e = launch_attend_mma(ka, D, sm_count, s);
     if (e != cudaSuccess) return e;

@@ -142,10 +142,6 @@ struct DecodeLaunch {
 // Split-K attention on tensor cores (tq_decode_mma.cuh), parameterised by the formats: K code width wk
 // (q8_0 = 0, turbo K = index bits + 1), V code width wv (q8_0 = 0, turbo-MSE V = index bits),
 // one translation unit per head_dim.
-// Split-K attention at head_dim 128 with the score products on tcgen05 (tq_decode_tc.cu): turbo K
-// code width wk (2..4), turbo-MSE V code width wv (1..3), up to 16 query heads per KV head.
-bool tc_decode_has(int wk, int wv);
-cudaError_t tc_decode_launch(const DecodeLaunch& k, int wk, int wv, int sm_count, cudaStream_t s);
 bool mma_has_d64(int wk, int wv);
 bool mma_has_d128(int wk, int wv);
 bool mma_has_d256(int wk, int wv);
