@@ -131,9 +131,19 @@ struct Shape {
   static constexpr int QfBytes = F::KS * 256 * (F::KQ8 ? 1 : 2) * NQ;
   static constexpr int PsBytes = 512 * NT * NV;
   static constexpr int Block = PsBytes + QfBytes;
+  // turbo-MSE V of 2 or 3 bits with up to 4 query heads: a 64 KB V table of byte-indexed entries
+  // (two tables in one: the code pair in a byte's low bits at + 0, in its high bits at + 128), so
+  // that every lookup address is one byte permute of the codes (accumulate_v)
+  static constexpr bool DualV = HILO && !F::VQ8 && (F::WV == 2 || F::WV == 3);
+  static constexpr uint32_t VLut = DualV ? 65536u : F::VLut;
+  static constexpr uint32_t Big = F::KLut > VLut ? F::KLut : VLut, Small = F::KLut > VLut ? VLut : F::KLut;
   static constexpr int smem(int warps) {
-    const int packed = (int)(F::Big + F::Small) + warps * Block + ((int)F::Small > Block ? (int)F::Small : Block);
-    const int gap = (int)(2 * F::Big + F::Small);
+    if (Small == Big) {  // the second table right above the first; warp blocks below, then above
+      const int blocks = (warps + 1) * Block;
+      return (int)(2 * Big) + (blocks > (int)Big ? blocks : (int)Big);
+    }
+    const int packed = (int)(Big + Small) + warps * Block + ((int)Small > Block ? (int)Small : Block);
+    const int gap = (int)(2 * Big + Small);
     return packed > gap ? packed : gap;
   }
   static constexpr int W0 = F::D == 256 ? 8 : (NT == 2 ? 12 : (NQ == 4 ? 8 : 16));
@@ -200,6 +210,7 @@ struct MmaWarp {
   static constexpr bool HILO = NQ == 1;
   // head slots per thread (heads t, t + 4, t + 8, t + 12) = 8-column products per part; V products
   static constexpr int NH = NQ, NV = Shape<F, NQ>::NV;
+  static constexpr bool DualV = Shape<F, NQ>::DualV;
 
   struct KTile {
     uint32_t a[F::KLoad], b[F::KLoad];  // tokens g, g + 8
@@ -499,11 +510,41 @@ struct MmaWarp {
       uint32_t r[4][F::VRun];
 #pragma unroll
       for (int q = 0; q < 4; ++q) make_run<F::VLoad, F::VRun, F::VShift>(V.w[q], r[q], vsh);
+      // byte-indexed table (3 bits: the run and the run shifted by 4 bits give every pair of
+      // coordinates as the low or high 6 bits of a byte; 2 bits: as a byte's low or high nibble)
+      uint32_t r4[4][F::VRun];
+      if constexpr (DualV && F::WV == 3) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+          for (int j = 0; j < F::VRun; ++j)
+            r4[q][j] = j + 1 < F::VRun ? __funnelshift_r(r[q][j], r[q][j + 1 < F::VRun ? j + 1 : j], 4) : r[q][j] >> 4;
+        }
+      }
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) {
         uint32_t e[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) e[q] = lds32(run_addr<N, 7>(r[q], 2 * mt * F::WV, ylv));
+        for (int q = 0; q < 4; ++q) {
+          if constexpr (DualV) {
+            // pair mt: byte, half (high: + 128) and source (the run or the run >> 4)
+            int byte, hi;
+            bool shifted = false;
+            if constexpr (F::WV == 3) {
+              const int m = mt >> 2, i = mt & 3;
+              byte = 3 * m + (i == 2 ? 1 : i == 3 ? 2 : 0);
+              hi = i & 1;
+              shifted = i == 1 || i == 2;
+            } else {
+              byte = mt >> 1;
+              hi = mt & 1;
+            }
+            const uint32_t src = shifted ? r4[q][byte >> 2] : r[q][byte >> 2];
+            e[q] = lds32(__byte_perm(src, ylv, 0x7604u | ((uint32_t)(byte & 3) << 4)) + 128u * hi);
+          } else {
+            e[q] = lds32(run_addr<N, 7>(r[q], 2 * mt * F::WV, ylv));
+          }
+        }
         // a0/a1: slots 2t, 2t+1 = tokens t, t+8 at coordinate 2mt / 2mt+1; a2/a3: tokens t+4, t+12
         const uint32_t a0 = __byte_perm(e[0], e[1], 0x5410), a1 = __byte_perm(e[0], e[1], 0x7632);
         const uint32_t a2 = __byte_perm(e[2], e[3], 0x5410), a3 = __byte_perm(e[2], e[3], 0x7632);
@@ -955,13 +996,13 @@ __global__ void __launch_bounds__(Shape<F, NQ>::Threads, 1) attend_mma_kernel(De
   // above; warp blocks (two P' tiles, then the query fragments) from the start up to the smaller
   // table, the rest above the tables ----
   const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(sm));
-  const uint32_t bofs = F::Big ? ((F::Big - (sbase & (F::Big - 1u))) & (F::Big - 1u)) : 0u;
-  const bool small_below = bofs >= F::Small;
-  const uint32_t sofs = small_below ? bofs - F::Small : bofs + F::Big;
+  const uint32_t bofs = L::Big ? ((L::Big - (sbase & (L::Big - 1u))) & (L::Big - 1u)) : 0u;
+  const bool small_below = bofs >= L::Small;
+  const uint32_t sofs = small_below ? bofs - L::Small : bofs + L::Big;
   const uint32_t n_below = (small_below ? sofs : bofs) / (uint32_t)L::Block;
-  const uint32_t above = bofs + F::Big + (small_below ? 0u : F::Small);
-  const uint32_t kofs = F::KLut >= F::VLut ? bofs : sofs;
-  const uint32_t vofs = F::KLut >= F::VLut ? sofs : bofs;
+  const uint32_t above = bofs + L::Big + (small_below ? 0u : L::Small);
+  const uint32_t kofs = F::KLut >= L::VLut ? bofs : sofs;
+  const uint32_t vofs = F::KLut >= L::VLut ? sofs : bofs;
   const uint32_t wofs = (uint32_t)warp < n_below ? warp * (uint32_t)L::Block
                                                  : above + (warp - n_below) * (uint32_t)L::Block;
   if constexpr (!F::KQ8) {
@@ -976,7 +1017,20 @@ __global__ void __launch_bounds__(Shape<F, NQ>::Threads, 1) attend_mma_kernel(De
           h2_as_u32(__floats2half2_rn((c0 >> (W - 1)) ? 1.f : -1.f, (c1 >> (W - 1)) ? 1.f : -1.f));
     }
   }
-  if constexpr (!F::VQ8) {
+  if constexpr (L::DualV) {
+    // entry e (a byte of codes): the pair in its low 2W bits at + 0, the pair in its high 2W bits
+    // at + 128
+    constexpr int W = F::WV, cm = (1 << W) - 1, pm = (1 << (2 * W)) - 1;
+    const float* cb = k.tab.centroids + (W - 1) * 8;
+    const float lam = k.tab.f16_scale[W - 1];
+    for (int i = tid; i < 256 * 32; i += L::Threads) {
+      const int e = i >> 5, r = i & 31, lo = e & pm, hi = e >> (8 - 2 * W);
+      *reinterpret_cast<uint32_t*>(sm + vofs + e * 256 + r * 4) =
+          h2_as_u32(__floats2half2_rn(lam * cb[lo & cm], lam * cb[lo >> W]));
+      *reinterpret_cast<uint32_t*>(sm + vofs + e * 256 + 128 + r * 4) =
+          h2_as_u32(__floats2half2_rn(lam * cb[hi & cm], lam * cb[hi >> W]));
+    }
+  } else if constexpr (!F::VQ8) {
     constexpr int W = F::WV, n = 1 << (2 * W), cm = (1 << W) - 1;
     const float* cb = k.tab.centroids + (W - 1) * 8;
     const float lam = k.tab.f16_scale[W - 1];
