@@ -95,6 +95,31 @@ def source_hash(paths):
     return h.hexdigest()[:16]
 
 
+def profiled_field(kernel_srcs, record, key):
+    """Field `key` of a committed ncu record under profiles/, or None when the record is missing or
+    the kernel sources changed since its counters were taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", record)) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256_16") != source_hash(kernel_srcs):
+        return None
+    return rec.get(key)
+
+
+def issue_roofline(instr_per_layer, layers, seconds, sm_mhz):
+    """Warp instructions issued per second against the issue limit of the GPU: one warp instruction
+    per clock on each of the 4 sub-partitions of the 152 SMs, at the median SM clock sampled
+    during the timed region."""
+    if instr_per_layer is None or not sm_mhz:
+        return None
+    achieved = instr_per_layer * layers / seconds / 1e9
+    peak = 4 * 152 * sm_mhz / 1e3
+    return {"achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "G warp instructions/s",
+            "frac": round(achieved / peak, 4)}
+
+
 def profiled_traffic(kernel_srcs, record="decode_traffic.json"):
     """DRAM bytes per call from a committed ncu summary under profiles/ (decode call:
     decode_traffic.json; encode call: encode_traffic.json), or None when the kernel
@@ -435,6 +460,10 @@ def main():
                "sample": f"{nl} of {wl.n_layers} layers (8 KV heads x {wl.ctx} tokens each): oracle dequantisation"
                          f" + fp64 attention, {secs:.1f} s timed"}
     clk = clocks.summary()
+    csrc = os.path.join(ROOT, "kv_cache_quantization_turbo_gb300", "csrc")
+    dec_srcs = [os.path.join(csrc, f) for f in ("tq_decode_mma.cuh", "tq_decode_mma128.cu", "tq_decode.cu",
+                                                 "tq_warp_mma.cuh")]
+    enc_srcs = [os.path.join(csrc, f) for f in ("tq_encode.cu", "tq_tc.cuh")]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 4), "higher_is_better": True, "scaling": "weak",
@@ -455,17 +484,22 @@ def main():
                      "frac": round(achieved / hbm, 4), "peak_source": f"{peak_src} hbm_gbs",
                      "kernel": "decode attention call (prologue + split-K attention + combine), one launch set "
                                f"over all {wl.n_layers} layers",
-                     "traffic": profiled_traffic([os.path.join(ROOT, "kv_cache_quantization_turbo_gb300", "csrc", f)
-                                                  for f in ("tq_decode_mma.cuh", "tq_decode_mma128.cu", "tq_decode.cu",
-                                                            "tq_warp_mma.cuh")])},
+                     "traffic": profiled_traffic(dec_srcs)},
         "roofline_encode": {"bound": "hbm", "achieved": round(encode_bytes(tq, wl) / t_enc / 1e9, 2), "peak": hbm,
                             "unit": "GB/s", "frac": round(encode_bytes(tq, wl) / t_enc / 1e9 / hbm, 4),
                             "peak_source": f"{peak_src} hbm_gbs",
-                            "traffic": profiled_traffic([os.path.join(ROOT, "kv_cache_quantization_turbo_gb300", "csrc", f)
-                                                         for f in ("tq_encode.cu", "tq_tc.cuh")],
-                                                        "encode_traffic.json"),
+                            "traffic": profiled_traffic(enc_srcs, "encode_traffic.json"),
                             "kernel": f"encode call (K and V kernels) of the {wl.encode_chunk}-token chunk over all "
                                       f"{wl.n_layers} layers: fp16 input read, codes and headers written"},
+        "roofline_issue": {
+            "bound": "issue",
+            "decode": issue_roofline(profiled_field(dec_srcs, "decode_traffic.json", "warp_instructions_per_layer"),
+                                     wl.n_layers, t_dec, clk.get("sm_mhz")),
+            "encode": issue_roofline(profiled_field(enc_srcs, "encode_traffic.json", "warp_instructions_per_layer"),
+                                     wl.n_layers, t_enc, clk.get("sm_mhz")),
+            "what": "warp instructions per call (smsp__inst_executed.sum of the attention kernel / of the two "
+                    "encode kernels, from the ncu records under profiles/, null once the kernels changed) over "
+                    "the call's time; the pipe that binds both calls"},
         "e2e": {"value": round(weak_scaling_value(dbytes, world, t_e2e), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(t_e2e * 1e3, 3),
                 "what": "per step: H2D of the 4096-token K/V chunk (all layers) and q from pinned memory, encode,"
