@@ -18,7 +18,7 @@
 // lazily: only when a score passes it by 2^8 are the sums and accumulators rescaled), Sparse V
 // (a tile whose every weight is below the threshold skips V; inside a kept tile weights below it
 // are zeroed), P' into a per-warp shared tile, V loads, V products.  Memory: every second tile one
-// lane requests the two tiles 4-5 ahead into L2 (cp.async.bulk.prefetch; contiguous caches: the
+// lane requests the two tiles 3-4 ahead into L2 (cp.async.bulk.prefetch; contiguous caches: the
 // tiles of a page), so a tile's own register loads meet L2; cache loads carry an evict-first L2
 // policy so that the partials stay in L2 for the combine.
 //
@@ -67,7 +67,7 @@ namespace mmad {
 
 using namespace wm;
 
-constexpr int kPrefetchTiles = 4;  // L2 prefetch distance in tiles
+constexpr int kPrefetchTiles = 3;  // L2 prefetch distance in tiles
 
 // Most 32-bit words that cover bits [s, s + n) for the starts s = i n, i < count.
 constexpr int cover_words(int n, int count) {
