@@ -105,3 +105,44 @@ def test_prefill_rejects_bad_arguments(ctx128):
     assert call(kv, tq.alloc_view("q8_0", d, 2, page_size=64, num_pages=1), 10, 0) == tq.TQ_ERR_UNSUPPORTED
     assert call(kv, vv, 10, 0, wsb=16) == tq.TQ_ERR_WORKSPACE
     torch.cuda.synchronize()
+
+
+def test_prefill_full_size_sampled_rows(ctx128):
+    """The timed configuration: a 4096-token chunk at the end of a 32768-token context, 8 KV heads,
+    GQA 4 (32 query heads), turbo4 / turbo4_mse, one call as the timing runs it.  Sampled rows
+    (chunk token, query head): the first and last tokens, 128-row tile boundaries (32 tokens of a
+    KV head's 4 query heads), 64-key tile boundaries of the causal edge, on three KV heads, against
+    the oracle over the codes the GPU stored for those heads."""
+    d, H, G, n, start = 128, 8, 4, 4096, 28672
+    T, Hq = start + n, H * G
+    k = W.kv_tensor(T, H, d, seed=41, device="cuda", outlier_frac=0.01)
+    v = W.kv_tensor(T, H, d, seed=42, device="cuda", outlier_frac=0.01)
+    kv = tq.alloc_view("turbo4", d, H, page_size=T, num_pages=1)
+    vv = tq.alloc_view("turbo4_mse", d, H, page_size=T, num_pages=1)
+    assert tq.tq_encode_kv(ctx128.h, kv, k, vv, v, 0, 1, T, T * H * d, H * d, None) == tq.TQ_OK
+    del k, v
+    q = W.normal_tensor((n, Hq, d), seed=43, device="cuda")
+    ws_bytes = tq.tq_prefill_workspace_bytes(ctx128.h, n, Hq)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.full((n, Hq, d), float("nan"), dtype=torch.float32, device="cuda")
+    st = tq.tq_prefill_attention(ctx128.h, q, 0, n, Hq, kv, vv, 0, 0, None, 0, start, 1 / math.sqrt(d), ws,
+                                 ws_bytes, out)
+    assert st == tq.TQ_OK, tq.tq_status_string(st)
+    torch.cuda.synchronize()
+    assert tq.tq_get_status(ctx128.h)[0] == tq.TQ_OK
+    got_all = out.cpu().numpy()
+    assert np.isfinite(got_all).all()
+    kp, kh = C.read_vectors(kv)
+    vp, vh = C.read_vectors(vv)
+    qn = q.cpu().numpy().astype(np.float64)
+    tokens = [0, 1, 31, 32, 63, 64, 95, 96, 127, 128, 2047, 2048, 4063, 4064, 4094, 4095]
+    errs = []
+    for kvh in (0, 3, 7):
+        kt = C.oracle_dequant("turbo4", C.gpu_codes("turbo4", d, kp[0, kvh], kh[0, kvh]), ctx128.signs, ctx128.S)
+        vt = C.oracle_dequant("turbo4_mse", C.gpu_codes("turbo4_mse", d, vp[0, kvh], vh[0, kvh]), ctx128.signs,
+                              ctx128.S)
+        for j, i in enumerate(tokens):
+            h = kvh * G + (j + kvh) % G
+            want = O.prefill_attention(qn[i:i + 1, h:h + 1], kt[:, None], vt[:, None], start + i, 1 / math.sqrt(d))
+            errs.append(C.rel_err_per_head(got_all[i, h][None], want[0, 0][None])[0])
+    assert max(errs) < C.ATTN_RTOL, max(errs)
