@@ -31,8 +31,8 @@ static int next_pow2(long long v) {
 
 DecodePlan plan_decode(int sm_count, int d, int n_layers, int batch, int n_q_heads, int max_ctx) {
   DecodePlan p{};
-  // Split size: aim at ~12 work items per warp of the tensor-core kernel (16 warps per SM,
-  // query heads shared by about 4 per KV head), between 256 and 4096 tokens.  Timed on
+  // Split size: aim at ~12 work items per warp of the tensor-core kernel (counted at 16 warps
+  // per SM, query heads shared by about 4 per KV head), between 256 and 4096 tokens.  Timed on
   // the 32-layer x 32K bench workload: 512-token splits beat 1024 (item count vs. load
   // balance) and 256 (per-item overhead and partial traffic).
   const long long work = (long long)max_ctx * n_layers * batch * n_q_heads;
@@ -141,8 +141,8 @@ __device__ __forceinline__ long long token_vector(const DecodeArgs& a, const Dev
 
 // ---------------------------------------------------------------------------
 // 2. split-K attention on CUDA cores, for what the tensor-core kernel does not
-//    take (9 to 16 query heads per KV head, a turbo-MSE format used as K, block
-//    tables over pages that are not a multiple of 16 tokens): one warp per CTA;
+//    take (a turbo-MSE format used as K, block tables over pages that are not a
+//    multiple of 16 tokens): one warp per CTA;
 //    lane = token while scoring, lane = coordinates while accumulating V.
 // ---------------------------------------------------------------------------
 constexpr int kGMax = 16;
