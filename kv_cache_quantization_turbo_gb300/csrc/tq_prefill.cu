@@ -73,19 +73,20 @@ __host__ __device__ constexpr uint32_t kstep(int ks) {
   return (uint32_t)((ks >> 2) * (128 * R) + (ks & 3) * 32);
 }
 
-struct Smem {  // byte offsets from a 1024-byte boundary; [2] = the two tile buffers
-  static constexpr int kcb = 0;                       // [2][64 x 128]
-  static constexpr int ksg = kcb + 2 * NK * D * 2;    // [2][64 x 128]
-  static constexpr int vt = ksg + 2 * NK * D * 2;     // [2][64 tokens x 128], MN-major (swz_v)
-  static constexpr int p = vt + 2 * D * NK * 2;       // [2][128 x 64]
-  static constexpr int hdr = p + 2 * M * NK * 2;      // [2] float kn[64], kr[64], vn[64]
-  static constexpr int tab = hdr + 2 * 3 * NK * 4;    // fp16 cb_k[8], cb_v[8]
+constexpr int NB = 3;  // K / V tile buffers (P: two)
+struct Smem {  // byte offsets from a 1024-byte boundary; [NB] = the K / V tile buffers
+  static constexpr int kcb = 0;                       // [NB][64 x 128]
+  static constexpr int ksg = kcb + NB * NK * D * 2;   // [NB][64 x 128]
+  static constexpr int vt = ksg + NB * NK * D * 2;    // [NB][64 tokens x 128], MN-major (swz_v)
+  static constexpr int p = vt + NB * D * NK * 2;      // [2][128 x 64]
+  static constexpr int hdr = p + 2 * M * NK * 2;      // [NB] float kn[64], kr[64], vn[64]
+  static constexpr int tab = hdr + NB * 3 * NK * 4;   // fp16 cb_k[8], cb_v[8]
   static constexpr int kbt = tab + 32;                // turbo4 K: uint2 [256] per code byte: codebook pair, sign pair
   static constexpr int vpt = kbt + 256 * 8;           // V: f16 pair per code pair (2 W_V bits) and lane: [64][32] words
   static constexpr int xch = vpt + 64 * 32 * 4;       // float [2][128]: half-tile row maxima, then half sums
-  static constexpr int inval = xch + 2 * M * 4;       // uint32 [2][4]: a producer warp's tile holds keys that are not there
-  static constexpr int bar = inval + 32;              // mbarriers: kv_full[2], s_done, s_free, p_full[2], pv_done[2]
-  static constexpr int slot = bar + 8 * 8;            // tensor-memory address
+  static constexpr int inval = xch + 2 * M * 4;       // uint32 [NB][4]: a producer warp's tile holds keys that are not there
+  static constexpr int bar = inval + 16 * NB;         // mbarriers: kv_full[NB], s_done, s_free, p_full[2], pv_done[NB]
+  static constexpr int slot = bar + 10 * 8;           // tensor-memory address
   static constexpr int total = slot + 16;
   static constexpr int alloc = total + 1024;          // room to align the base
 };
@@ -124,6 +125,36 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[NW], int c) {
   return x & ((1u << W) - 1u);
 }
 
+// True if the phase of the given parity of the mbarrier has completed (a non-blocking test).
+__device__ __forceinline__ bool test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(done)
+      : "r"(tc::smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// The four score products of one K step (16 coordinates): the codebook accumulator d_cb += (q'_hi +
+// q'_lo) K_cb and the QJL accumulator d_qj += (S q'_hi + S q'_lo) K_sign, A from tensor memory, B
+// from the shared-memory descriptors {b_cb_lo, b_hi} and {b_sg_lo, b_hi}; acc = 0 starts both sums.
+__device__ __forceinline__ void mma_kstep(uint32_t d_cb, uint32_t d_qj, uint32_t a_hi, uint32_t a_lo, uint32_t a_shi,
+                                          uint32_t a_slo, uint32_t b_cb_lo, uint32_t b_sg_lo, uint32_t b_hi,
+                                          uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b64 bc, bs;\n\t"
+      "setp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 t, %10, %10;\n\t"
+      "mov.b64 bc, {%6, %8};\n\tmov.b64 bs, {%7, %8};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], bc, %9, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], bc, %9, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%4], bs, %9, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [%5], bs, %9, t;\n\t}\n" ::"r"(d_cb),
+      "r"(d_qj), "r"(a_hi), "r"(a_lo), "r"(a_shi), "r"(a_slo), "r"(b_cb_lo), "r"(b_sg_lo), "r"(b_hi), "r"(idesc),
+      "r"((uint32_t)acc));
+}
+
 // One arrival per warp after the whole warp's shared-memory stores: made visible to the tensor
 // core, then lane 0 arrives.
 __device__ __forceinline__ void warp_arrive_smem(uint64_t* bar, int lane) {
@@ -142,11 +173,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   __half* cbk = reinterpret_cast<__half*>(sm + Smem::tab);
   __half* cbv = cbk + 8;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Smem::bar);
-  uint64_t* kv_full = bars;      // [2] tile buffer b dequantised (4 producer warps)
-  uint64_t* s_done = bars + 2;   // the score products of a tile completed (commit)
-  uint64_t* s_free = bars + 3;   // the row warps have read a tile's scores (4 row warps)
-  uint64_t* p_full = bars + 4;   // [2] P of tile buffer b written (4 row warps)
-  uint64_t* pv_done = bars + 6;  // [2] the value product of tile buffer b completed (commit)
+  uint64_t* kv_full = bars;       // [NB] K / V tile buffer b dequantised (4 producer warps)
+  uint64_t* s_done = bars + 3;    // the score products of a tile completed (commit)
+  uint64_t* s_free = bars + 4;    // the row warps have read a tile's scores (8 row warps)
+  uint64_t* p_full = bars + 5;    // [2] P buffer b written (8 row warps)
+  uint64_t* pv_done = bars + 7;   // [NB] the value product of the tile in K / V buffer b completed (commit)
   uint32_t* slot = reinterpret_cast<uint32_t*>(sm + Smem::slot);
 
   const int kvh = blockIdx.y, G = a.G, Hq = a.n_q_heads;
@@ -156,12 +187,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (lane == 0) {
       tc::mbar_init(kv_full, kProdWarps);
       tc::mbar_init(kv_full + 1, kProdWarps);
+      tc::mbar_init(kv_full + 2, kProdWarps);
       tc::mbar_init(s_done, 1);
       tc::mbar_init(s_free, kRowWarps);  // one arrival per row warp (each reads half of the scores)
       tc::mbar_init(p_full, kRowWarps);
       tc::mbar_init(p_full + 1, kRowWarps);
       tc::mbar_init(pv_done, 1);
       tc::mbar_init(pv_done + 1, 1);
+      tc::mbar_init(pv_done + 2, 1);
     }
   }
   if (tid < 8) {
@@ -289,9 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     Codes cur, nxt;
     if (n_tiles > 0) load_codes(0, cur);
     for (int jt = 0; jt < n_tiles && ok; ++jt) {
-      const int bf = jt & 1;
+      const int bf = jt % NB;
       if (jt + 1 < n_tiles) load_codes(jt + 1, nxt);  // in flight while this tile is dequantised
-      if (jt >= 2) ok = tc::mbar_wait(pv_done + bf, (uint32_t)((jt - 2) >> 1) & 1u);  // buffer read by tile jt - 2
+      if (jt >= NB) ok = tc::mbar_wait(pv_done + bf, (uint32_t)(jt / NB - 1) & 1u);  // buffer read by tile jt - NB
       if (!ok) break;
       tc::fence_after_sync();
       unsigned char* kcb_b = sm + Smem::kcb + bf * NK * D * 2;
@@ -350,55 +383,57 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
   } else if (warp == kIssuerWarp) {
     // ================= MMA issue (one thread) =================
+    // Whichever is ready first: the value product of the oldest scored tile (it frees a P and a K / V
+    // buffer), else the score products of the next tile (its tiles dequantised, the previous scores
+    // read).  Polls are non-blocking; their total is bounded (about a second).
     if (lane == 0) {
       constexpr uint32_t id64 = tc::idesc_f16_f32(M, NK);
       constexpr uint32_t id128v = tc::idesc_f16_f32(M, D) | (1u << 16);  // B (V) MN-major
-      int issued_s = 0, issued_pv = 0;
-      auto scores = [&](int jt) {  // S_cb = (q'_hi + q'_lo) K_cb^T, S_qjl = (S q'_hi + S q'_lo) K_sign^T
-        const int bf = jt & 1;
-        const uint64_t dkc = tc::desc_sw128(sb + Smem::kcb + bf * NK * D * 2);
-        const uint64_t dks = tc::desc_sw128(sb + Smem::ksg + bf * NK * D * 2);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t kb = kstep<NK>(ks) >> 4;
-          tc::mma_f16_ts(t_cb, t_q + 8 * ks, dkc + kb, id64, ks > 0);
-          tc::mma_f16_ts(t_cb, t_q + 64 + 8 * ks, dkc + kb, id64, true);
-          tc::mma_f16_ts(t_qj, t_q + 128 + 8 * ks, dks + kb, id64, ks > 0);
-          tc::mma_f16_ts(t_qj, t_q + 192 + 8 * ks, dks + kb, id64, true);
-        }
-        tc::commit(s_done);
-        issued_s = jt + 1;
-      };
-      if (n_tiles > 0) {
-        ok = tc::mbar_wait(kv_full, 0u);
-        if (ok) {
+      const uint32_t kDescHi = (uint32_t)(tc::desc_sw128(0) >> 32);  // a 128-byte-swizzle K-major descriptor's high word
+      int ns = 0, np = 0;  // score / value products issued
+      long long idle = 0;
+      while (np < n_tiles) {
+        bool did = false;
+        if (np < ns && test_wait(p_full + (np & 1), (uint32_t)(np >> 1) & 1u)) {  // O += P V of tile np
           tc::fence_after_sync();
-          scores(0);
-        }
-      }
-      for (int jt = 0; jt < n_tiles && ok; ++jt) {
-        const int bf = jt & 1;
-        if (jt + 1 < n_tiles) {  // the next tile's scores once its tiles are in and tile jt's scores were read
-          ok = tc::mbar_wait(kv_full + ((jt + 1) & 1), (uint32_t)((jt + 1) >> 1) & 1u);
-          if (ok) ok = tc::mbar_wait(s_free, (uint32_t)jt & 1u);
-          if (!ok) break;
-          tc::fence_after_sync();
-          scores(jt + 1);
-        }
-        ok = tc::mbar_wait(p_full + bf, (uint32_t)(jt >> 1) & 1u);  // P of tile jt written
-        if (!ok) break;
-        tc::fence_after_sync();
-        const uint64_t dp = tc::desc_sw128(sb + Smem::p + bf * M * NK * 2);
-        const uint64_t dv = tc::desc_sw128_mn(sb + Smem::vt + bf * D * NK * 2, 8192);
+          const uint64_t dp = tc::desc_sw128(sb + Smem::p + (np & 1) * M * NK * 2);
+          const uint64_t dv = tc::desc_sw128_mn(sb + Smem::vt + (np % NB) * D * NK * 2, 8192);
 #pragma unroll
-        for (int ks = 0; ks < NK / 16; ++ks)  // 16 tokens = two 1024-byte groups of V
-          tc::mma_f16(t_o, dp + (kstep<M>(ks) >> 4), dv + (uint64_t)(ks * (2048 >> 4)), id128v, jt > 0 || ks > 0);
-        tc::commit(pv_done + bf);
-        issued_pv = jt + 1;
+          for (int ks = 0; ks < NK / 16; ++ks)  // 16 tokens = two 1024-byte groups of V
+            tc::mma_f16(t_o, dp + (kstep<M>(ks) >> 4), dv + (uint64_t)(ks * (2048 >> 4)), id128v, np > 0 || ks > 0);
+          tc::commit(pv_done + np % NB);
+          ++np;
+          did = true;
+        } else if (ns < n_tiles && test_wait(kv_full + ns % NB, (uint32_t)(ns / NB) & 1u) &&
+                   (ns == 0 || test_wait(s_free, (uint32_t)(ns - 1) & 1u))) {
+          // S_cb = (q'_hi + q'_lo) K_cb^T, S_qjl = (S q'_hi + S q'_lo) K_sign^T: one instruction block per
+          // k step, the operand descriptors' low words stepped in 32 bits
+          tc::fence_after_sync();
+          const uint32_t lcb = (uint32_t)tc::desc_sw128(sb + Smem::kcb + (ns % NB) * NK * D * 2);
+          const uint32_t lsg = (uint32_t)tc::desc_sw128(sb + Smem::ksg + (ns % NB) * NK * D * 2);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t kb = kstep<NK>(ks) >> 4;
+            mma_kstep(t_cb, t_qj, t_q + 8 * ks, t_q + 64 + 8 * ks, t_q + 128 + 8 * ks, t_q + 192 + 8 * ks, lcb + kb,
+                      lsg + kb, kDescHi, id64, ks > 0);
+          }
+          tc::commit(s_done);
+          ++ns;
+          did = true;
+        }
+        if (did) {
+          idle = 0;
+        } else {
+          if (++idle > (1 << 24)) {  // about a second of polls with nothing to issue
+            ok = false;
+            break;
+          }
+          __nanosleep(32);
+        }
       }
       if (!ok) {  // bounded waits for the products still in flight before the tensor memory is freed
-        if (issued_s > 0) tc::mbar_wait(s_done, (uint32_t)(issued_s - 1) & 1u, 1 << 10);
-        if (issued_pv > 0) tc::mbar_wait(pv_done + ((issued_pv - 1) & 1), (uint32_t)((issued_pv - 1) >> 1) & 1u, 1 << 10);
+        if (ns > 0) tc::mbar_wait(s_done, (uint32_t)(ns - 1) & 1u, 1 << 10);
+        if (np > 0) tc::mbar_wait(pv_done + (np - 1) % NB, (uint32_t)((np - 1) / NB) & 1u, 1 << 10);
       }
     }
     __syncwarp();
@@ -411,9 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int pair_bar = 1 + (warp & 3);
     float* xch = reinterpret_cast<float*>(sm + Smem::xch);
     for (int jt = 0; jt < n_tiles && ok; ++jt) {
-      const int bf = jt & 1;
+      const int bf = jt % NB, bp = jt & 1;  // K / V buffer, P buffer
       bool w_ok = tc::mbar_wait(s_done, (uint32_t)jt & 1u);
-      if (w_ok) w_ok = tc::mbar_wait(kv_full + bf, (uint32_t)(jt >> 1) & 1u);  // (complete: the tile's norms)
+      if (w_ok) w_ok = tc::mbar_wait(kv_full + bf, (uint32_t)(jt / NB) & 1u);  // (complete: the tile's norms)
       ok = tc::bar_sync_and(pair_bar, 64, w_ok);
       if (!ok) break;
       tc::fence_after_sync();
@@ -465,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const float al = mn == -INFINITY ? 1.f : (m == -INFINITY ? 0.f : exp2f(m - mn));
         l *= al;
         if (jt > 0) {
-          w_ok = tc::mbar_wait(pv_done + ((jt - 1) & 1), (uint32_t)((jt - 1) >> 1) & 1u);
+          w_ok = tc::mbar_wait(pv_done + (jt - 1) % NB, (uint32_t)((jt - 1) / NB) & 1u);
           ok = tc::bar_sync_and(pair_bar, 64, w_ok);
           if (!ok) break;
           tc::fence_after_sync();
@@ -482,13 +517,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
         m = mn;
       }
-      // P into buffer bf once the value product of tile jt - 2 has read it
+      // P into buffer bp once the value product of tile jt - 2 has read it
       if (jt >= 2) {
-        w_ok = tc::mbar_wait(pv_done + bf, (uint32_t)((jt - 2) >> 1) & 1u);
+        w_ok = tc::mbar_wait(pv_done + (jt - 2) % NB, (uint32_t)((jt - 2) / NB) & 1u);
         ok = tc::bar_sync_and(pair_bar, 64, w_ok);
         if (!ok) break;
       }
-      unsigned char* p_b = sm + Smem::p + bf * M * NK * 2;
+      unsigned char* p_b = sm + Smem::p + bp * M * NK * 2;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
@@ -504,14 +539,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         *reinterpret_cast<uint4*>(p_b + swz<M>(r, 32 * kh + 8 * c8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      warp_arrive_smem(p_full + bf, lane);
+      warp_arrive_smem(p_full + bp, lane);
     }
     // ---- epilogue: O / l / lambda_V, then diag(s) H (the inverse rotation); warp w's threads take
     // coordinates 64 kh .. 64 kh + 63 of their rows: a 64-point transform of their half, then the
     // last butterfly with the other half through shared memory (the V and P buffers, free now) ----
     if (ok && n_tiles > 0) {
       const bool w_ok =
-          tc::mbar_wait(pv_done + ((n_tiles - 1) & 1), (uint32_t)((n_tiles - 1) >> 1) & 1u);
+          tc::mbar_wait(pv_done + (n_tiles - 1) % NB, (uint32_t)((n_tiles - 1) / NB) & 1u);
       ok = tc::bar_sync_and(pair_bar, 64, w_ok);
     }
     tc::fence_after_sync();
