@@ -56,58 +56,111 @@ using DecodeKernelArgs = DecodeLaunch;
 // ---------------------------------------------------------------------------
 // 1. query prologue
 // ---------------------------------------------------------------------------
-// One CTA of D threads per query row: warp 0 rotates q (signs, WHT, softmax scale) into shared
-// memory, then thread j forms (S q')_j = sum_i S_T[i][j] q'_i with four partial sums (coalesced rows
-// of S_T, several products in flight).
+// One CTA of D threads per kQprepRows query rows: warp w rotates rows w, w + D/32, ... (signs, WHT,
+// softmax scale) into shared memory, then thread j forms (S q')_j = sum_i S_T[i][j] q'_i of every
+// row, so each element of S is read once per CTA and used for all its rows.  S_T streams through
+// shared memory in 16 KB chunks of rows (asynchronous copies, two chunks in flight), so the reads
+// are in flight together rather than one dependent load per product.  The grid lets the attention
+// kernel that follows launch at once (programmatic dependent launch): that kernel builds its tables
+// meanwhile and waits for this grid before it reads anything written here.
+constexpr int kQprepRows = 8;
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 template <int D>
 __global__ void __launch_bounds__(D) qprep_kernel(DecodeKernelArgs ka) {
-  constexpr int E = D / 32;
+  constexpr int E = D / 32, NW = D / 32, RQ = kQprepRows;
+  constexpr int CH = 4096 / D, NC = D / CH;  // S_T rows per chunk (16 KB), chunks
+  pdl_launch_dependents();
   const DecodeArgs& a = ka.a;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const long long row = blockIdx.x;  // (layer, batch, q head)
+  const long long row0 = (long long)blockIdx.x * RQ;
   const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
-  if (row == 0 && threadIdx.x < 2) ka.counter[threadIdx.x] = 0u;  // work counters of the attention launches
-  if (row >= rows) return;  // block-uniform
-  __shared__ float q_s[D];
-  float* dst = ka.qprep + row * 2 * D;
-  const bool q8 = a.k.format == TQ_FMT_Q8_0;  // q8_0 K scores the unrotated q, and needs no S q
-  if (w == 0) {
+  if (blockIdx.x == 0 && threadIdx.x < 2) ka.counter[threadIdx.x] = 0u;  // work counters of the attention launches
+  __shared__ __align__(16) float q_s[D][RQ];      // q'_i of the CTA's rows: row r at [i][r]
+  __shared__ __align__(16) float s_s[2][CH * D];  // chunks of S_T
+  const bool q8 = a.k.format == TQ_FMT_Q8_0;      // q8_0 K scores the unrotated q, and needs no S q
+  auto stage = [&](int c) {
+    const float* src = ka.tab.S_T + (size_t)c * CH * D;
+    float* dst = s_s[c & 1];
+#pragma unroll
+    for (int p = threadIdx.x; p < CH * D / 4; p += D) cp_async16(dst + 4 * p, src + 4 * p);
+    cp_async_commit();
+  };
+  if (!q8) stage(0);
+  for (int r = w; r < RQ; r += NW) {
+    const long long row = row0 + r;
     float x[E];
-    if (a.q_is_fp16) {
-      const __half* q = static_cast<const __half*>(a.q) + io_row_of(a, row) * D;
+    if (row < rows) {  // warp-uniform
+      if (a.q_is_fp16) {
+        const __half* q = static_cast<const __half*>(a.q) + io_row_of(a, row) * D;
 #pragma unroll
-      for (int e = 0; e < E; ++e) x[e] = __half2float(q[E * lane + e]);
+        for (int e = 0; e < E; ++e) x[e] = __half2float(q[E * lane + e]);
+      } else {
+        const float* q = static_cast<const float*>(a.q) + io_row_of(a, row) * D;
+#pragma unroll
+        for (int e = 0; e < E; ++e) x[e] = q[E * lane + e];
+      }
+      if (!q8) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) x[e] *= (float)ka.tab.signs[E * lane + e];
+        warp_wht<D>(x, lane);
+      }
+      float* dst = ka.qprep + row * 2 * D;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        x[e] *= a.softmax_scale;
+        dst[E * lane + e] = x[e];
+      }
     } else {
-      const float* q = static_cast<const float*>(a.q) + io_row_of(a, row) * D;
 #pragma unroll
-      for (int e = 0; e < E; ++e) x[e] = q[E * lane + e];
-    }
-    if (!q8) {
-#pragma unroll
-      for (int e = 0; e < E; ++e) x[e] *= (float)ka.tab.signs[E * lane + e];
-      warp_wht<D>(x, lane);
+      for (int e = 0; e < E; ++e) x[e] = 0.f;
     }
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      x[e] *= a.softmax_scale;
-      q_s[E * lane + e] = x[e];
-      dst[E * lane + e] = x[e];
-    }
+    for (int e = 0; e < E; ++e) q_s[E * lane + e][r] = x[e];
   }
   if (q8) return;  // block-uniform
-  __syncthreads();
   const int j = threadIdx.x;
-  const float* st = ka.tab.S_T + j;
-  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll 4
-  for (int i = 0; i < D; i += 4) {
-    s0 = fmaf(__ldg(st + (i + 0) * D), q_s[i + 0], s0);
-    s1 = fmaf(__ldg(st + (i + 1) * D), q_s[i + 1], s1);
-    s2 = fmaf(__ldg(st + (i + 2) * D), q_s[i + 2], s2);
-    s3 = fmaf(__ldg(st + (i + 3) * D), q_s[i + 3], s3);
+  float acc[RQ];
+#pragma unroll
+  for (int r = 0; r < RQ; ++r) acc[r] = 0.f;
+  for (int c = 0; c < NC; ++c) {
+    if (c + 1 < NC) {
+      stage(c + 1);  // its buffer was last read by chunk c - 1, which every thread finished (barrier below)
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();  // chunk c (and, the first time, q_s) visible to every thread
+    const float* sc = s_s[c & 1] + j;
+#pragma unroll 8
+    for (int k = 0; k < CH; ++k) {
+      const float sv = sc[k * D];
+      const float4 qa = *reinterpret_cast<const float4*>(&q_s[c * CH + k][0]);
+      const float4 qb = *reinterpret_cast<const float4*>(&q_s[c * CH + k][4]);
+      acc[0] = fmaf(sv, qa.x, acc[0]);
+      acc[1] = fmaf(sv, qa.y, acc[1]);
+      acc[2] = fmaf(sv, qa.z, acc[2]);
+      acc[3] = fmaf(sv, qa.w, acc[3]);
+      acc[4] = fmaf(sv, qb.x, acc[4]);
+      acc[5] = fmaf(sv, qb.y, acc[5]);
+      acc[6] = fmaf(sv, qb.z, acc[6]);
+      acc[7] = fmaf(sv, qb.w, acc[7]);
+    }
+    __syncthreads();  // every thread is done with buffer c & 1 before chunk c + 2 is copied into it
   }
-  dst[D + j] = (s0 + s1) + (s2 + s3);
+#pragma unroll
+  for (int r = 0; r < RQ; ++r) {
+    if (row0 + r < rows) ka.qprep[(row0 + r) * 2 * D + D + j] = acc[r];
+  }
 }
+static_assert(kQprepRows == 8, "the S q' loop reads the rows as two float4");
+inline long long qprep_blocks(long long rows) { return (rows + kQprepRows - 1) / kQprepRows; }
 
 // ---------------------------------------------------------------------------
 // token addressing of the generic kernel
@@ -303,14 +356,17 @@ __global__ void __launch_bounds__(32) attend_generic_kernel(DecodeKernelArgs ka)
 // 3. combine
 // ---------------------------------------------------------------------------
 // One CTA of kCombineWarps warps per query row: warp w merges the splits w, w + kCombineWarps, ...
-// (several splits' partials in flight per warp), the warps' sums meet in shared memory, and warp 0
-// finishes the row.
+// in batches of CB whose loads are all in flight together, keeping its own running maximum (a batch
+// rescales what came before it only when it raises that maximum); the warps' (max, sum, acc) meet
+// in shared memory and warp 0 finishes the row.  Small enough (<= 64 registers) that one wave of
+// CTAs covers a few thousand rows.
 constexpr int kCombineWarps = 4;
 template <int D>
-__global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(DecodeKernelArgs ka) {
-  constexpr int E = D / 32;
+__global__ void __launch_bounds__(32 * kCombineWarps, 8) combine_kernel(DecodeKernelArgs ka) {
+  constexpr int E = D / 32, CB = D <= 128 ? 8 : 4;
   __shared__ float xs[kCombineWarps][D];
-  __shared__ float ls[kCombineWarps];
+  __shared__ float ms[kCombineWarps], ls[kCombineWarps];
+  pdl_wait();  // launched as a dependent of the attention grid: its partials are complete and visible
   const DecodeArgs& a = ka.a;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const long long row = blockIdx.x;
@@ -318,39 +374,83 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(DecodeKerne
   if (row >= rows) return;  // block-uniform
   const int ns = ka.n_splits;
   const float* part = ka.partial + row * ns * (D + 4);
-  // split maxima, lane-parallel (every warp)
-  float M = -INFINITY;
-  for (int s = lane; s < ns; s += 32) M = fmaxf(M, part[s * (D + 4)]);
-  M = warp_max(M);
-  float x[E];
+  float M = -INFINITY, L = 0.f, x[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) x[e] = 0.f;
-  float L = 0.f;
-  if (M != -INFINITY) {
-#pragma unroll 4
-    for (int s = w; s < ns; s += kCombineWarps) {
-      const float* p = part + s * (D + 4);
-      const float ms = p[0];  // empty splits: m = -inf, weight 0
-      float wj = 0.f;
-      if (ms != -INFINITY) {
-        wj = expf(ms - M);
-        L = fmaf(p[1], wj, L);
-      }
+  for (int s0 = w; s0 < ns; s0 += kCombineWarps * CB) {
+    float mv[CB], lv[CB], xv[CB][E];
 #pragma unroll
-      for (int e = 0; e < E; ++e) x[e] = fmaf(p[4 + E * lane + e], wj, x[e]);
+    for (int c = 0; c < CB; ++c) {
+      const int sp = s0 + kCombineWarps * c;
+      mv[c] = -INFINITY;  // a split past the end, or an empty one (m = -inf), weighs 0
+      lv[c] = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) xv[c][e] = 0.f;
+      if (sp < ns) {
+        const float* p = part + (long long)sp * (D + 4);
+        mv[c] = p[0];
+        lv[c] = p[1];
+        if constexpr (E % 4 == 0) {  // rows of D + 4 floats: 16-byte aligned at D = 128, 256
+#pragma unroll
+          for (int e = 0; e < E; e += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(p + 4 + E * lane + e);
+            xv[c][e] = v.x;
+            xv[c][e + 1] = v.y;
+            xv[c][e + 2] = v.z;
+            xv[c][e + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; e += 2) {
+            const float2 v = *reinterpret_cast<const float2*>(p + 4 + E * lane + e);
+            xv[c][e] = v.x;
+            xv[c][e + 1] = v.y;
+          }
+        }
+      }
+    }
+    float mb = M;
+#pragma unroll
+    for (int c = 0; c < CB; ++c) mb = fmaxf(mb, mv[c]);
+    if (mb == -INFINITY) continue;  // warp-uniform: nothing in this batch or before it
+    if (mb > M) {
+      const float al = M == -INFINITY ? 0.f : expf(M - mb);
+      L *= al;
+#pragma unroll
+      for (int e = 0; e < E; ++e) x[e] *= al;
+      M = mb;
+    }
+#pragma unroll
+    for (int c = 0; c < CB; ++c) {
+      const float wj = mv[c] == -INFINITY ? 0.f : expf(mv[c] - M);
+      L = fmaf(lv[c], wj, L);
+#pragma unroll
+      for (int e = 0; e < E; ++e) x[e] = fmaf(xv[c][e], wj, x[e]);
     }
   }
-  if (lane == 0) ls[w] = L;
+  if (lane == 0) {
+    ms[w] = M;
+    ls[w] = L;
+  }
 #pragma unroll
   for (int e = 0; e < E; ++e) xs[w][E * lane + e] = x[e];
   __syncthreads();
   if (w != 0) return;
-  L = ls[0];
+  float Mr = ms[0];
 #pragma unroll
-  for (int q = 1; q < kCombineWarps; ++q) {
-    L += ls[q];
+  for (int q = 1; q < kCombineWarps; ++q) Mr = fmaxf(Mr, ms[q]);
+  L = 0.f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) x[e] += xs[q][E * lane + e];
+  for (int e = 0; e < E; ++e) x[e] = 0.f;
+  if (Mr != -INFINITY) {
+#pragma unroll
+    for (int q = 0; q < kCombineWarps; ++q) {
+      if (ms[q] == -INFINITY) continue;
+      const float wq = expf(ms[q] - Mr);
+      L = fmaf(ls[q], wq, L);
+#pragma unroll
+      for (int e = 0; e < E; ++e) x[e] = fmaf(xs[q][E * lane + e], wq, x[e]);
+    }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
@@ -420,12 +520,11 @@ template <int D>
 cudaError_t launch_decode_dim(const DecodeKernelArgs& ka, int sm_count, cudaStream_t s) {
   const DecodeArgs& a = ka.a;
   const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
-  qprep_kernel<D><<<(unsigned)rows, D, 0, s>>>(ka);
+  qprep_kernel<D><<<(unsigned)qprep_blocks(rows), D, 0, s>>>(ka);
   if (attend_mma_supported(ka, D)) {
     const cudaError_t e = launch_attend_mma(ka, D, sm_count, s);
     if (e != cudaSuccess) return e;
-    combine_kernel<D><<<(unsigned)rows, 32 * kCombineWarps, 0, s>>>(ka);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel<D>, dim3((unsigned)rows), dim3(32 * kCombineWarps), 0, s, ka);
   }
   dim3 grid(ka.n_splits, a.k.H, a.n_layers * a.batch);
   const size_t smem = (3 * (size_t)ka.G * D + 16) * sizeof(float);
@@ -435,8 +534,7 @@ cudaError_t launch_decode_dim(const DecodeKernelArgs& ka, int sm_count, cudaStre
     if (e != cudaSuccess) return e;
   }
   attend_generic_kernel<D><<<grid, 32, smem, s>>>(ka);
-  combine_kernel<D><<<(unsigned)rows, 32 * kCombineWarps, 0, s>>>(ka);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel<D>, dim3((unsigned)rows), dim3(32 * kCombineWarps), 0, s, ka);
 }
 
 }  // namespace
@@ -451,9 +549,9 @@ cudaError_t launch_qprep(const DevTables& t, const DecodeArgs& a, float* qprep, 
   const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
   if (rows <= 0) return cudaSuccess;
   switch (t.d) {
-    case 64: qprep_kernel<64><<<(unsigned)rows, 64, 0, s>>>(ka); break;
-    case 128: qprep_kernel<128><<<(unsigned)rows, 128, 0, s>>>(ka); break;
-    case 256: qprep_kernel<256><<<(unsigned)rows, 256, 0, s>>>(ka); break;
+    case 64: qprep_kernel<64><<<(unsigned)qprep_blocks(rows), 64, 0, s>>>(ka); break;
+    case 128: qprep_kernel<128><<<(unsigned)qprep_blocks(rows), 128, 0, s>>>(ka); break;
+    case 256: qprep_kernel<256><<<(unsigned)qprep_blocks(rows), 256, 0, s>>>(ka); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

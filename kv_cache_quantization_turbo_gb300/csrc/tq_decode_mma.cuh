@@ -1009,12 +1009,12 @@ __global__ void __launch_bounds__(Shape<F, NQ>::Threads, 1) attend_mma_kernel(De
     constexpr int W = F::WK, n = 1 << (2 * W), cm = (1 << W) - 1, im = (1 << (W - 1)) - 1;
     const float* cb = k.tab.centroids + (W - 2) * 8;
     const float lam = k.tab.f16_scale[W - 2];
-    for (int i = tid; i < n * 32; i += L::Threads) {
-      const int e = i >> 5, r = i & 31, c0 = e & cm, c1 = e >> W;
-      *reinterpret_cast<uint32_t*>(sm + kofs + e * 256 + r * 4) =
-          h2_as_u32(__floats2half2_rn(lam * cb[c0 & im], lam * cb[c1 & im]));
-      *reinterpret_cast<uint32_t*>(sm + kofs + e * 256 + 128 + r * 4) =
-          h2_as_u32(__floats2half2_rn((c0 >> (W - 1)) ? 1.f : -1.f, (c1 >> (W - 1)) ? 1.f : -1.f));
+    for (int i = tid; i < n * 8; i += L::Threads) {  // four lanes' copies per 16-byte store
+      const int e = i >> 3, r = i & 7, c0 = e & cm, c1 = e >> W;
+      const uint32_t x = h2_as_u32(__floats2half2_rn(lam * cb[c0 & im], lam * cb[c1 & im]));
+      const uint32_t y = h2_as_u32(__floats2half2_rn((c0 >> (W - 1)) ? 1.f : -1.f, (c1 >> (W - 1)) ? 1.f : -1.f));
+      *reinterpret_cast<uint4*>(sm + kofs + e * 256 + r * 16) = make_uint4(x, x, x, x);
+      *reinterpret_cast<uint4*>(sm + kofs + e * 256 + 128 + r * 16) = make_uint4(y, y, y, y);
     }
   }
   if constexpr (L::DualV) {
@@ -1023,24 +1023,26 @@ __global__ void __launch_bounds__(Shape<F, NQ>::Threads, 1) attend_mma_kernel(De
     constexpr int W = F::WV, cm = (1 << W) - 1, pm = (1 << (2 * W)) - 1;
     const float* cb = k.tab.centroids + (W - 1) * 8;
     const float lam = k.tab.f16_scale[W - 1];
-    for (int i = tid; i < 256 * 32; i += L::Threads) {
-      const int e = i >> 5, r = i & 31, lo = e & pm, hi = e >> (8 - 2 * W);
-      *reinterpret_cast<uint32_t*>(sm + vofs + e * 256 + r * 4) =
-          h2_as_u32(__floats2half2_rn(lam * cb[lo & cm], lam * cb[lo >> W]));
-      *reinterpret_cast<uint32_t*>(sm + vofs + e * 256 + 128 + r * 4) =
-          h2_as_u32(__floats2half2_rn(lam * cb[hi & cm], lam * cb[hi >> W]));
+    for (int i = tid; i < 256 * 8; i += L::Threads) {
+      const int e = i >> 3, r = i & 7, lo = e & pm, hi = e >> (8 - 2 * W);
+      const uint32_t x = h2_as_u32(__floats2half2_rn(lam * cb[lo & cm], lam * cb[lo >> W]));
+      const uint32_t y = h2_as_u32(__floats2half2_rn(lam * cb[hi & cm], lam * cb[hi >> W]));
+      *reinterpret_cast<uint4*>(sm + vofs + e * 256 + r * 16) = make_uint4(x, x, x, x);
+      *reinterpret_cast<uint4*>(sm + vofs + e * 256 + 128 + r * 16) = make_uint4(y, y, y, y);
     }
   } else if constexpr (!F::VQ8) {
     constexpr int W = F::WV, n = 1 << (2 * W), cm = (1 << W) - 1;
     const float* cb = k.tab.centroids + (W - 1) * 8;
     const float lam = k.tab.f16_scale[W - 1];
-    for (int i = tid; i < n * 32; i += L::Threads) {
-      const int e = i >> 5, r = i & 31;
-      *reinterpret_cast<uint32_t*>(sm + vofs + e * 128 + r * 4) =
-          h2_as_u32(__floats2half2_rn(lam * cb[e & cm], lam * cb[e >> W]));
+    for (int i = tid; i < n * 8; i += L::Threads) {
+      const int e = i >> 3, r = i & 7;
+      const uint32_t x = h2_as_u32(__floats2half2_rn(lam * cb[e & cm], lam * cb[e >> W]));
+      *reinterpret_cast<uint4*>(sm + vofs + e * 128 + r * 16) = make_uint4(x, x, x, x);
     }
   }
   __syncthreads();
+  pdl_wait();            // the query prologue (prepared queries, zeroed work counter) has completed
+  pdl_launch_dependents();  // the combine may be scheduled as soon as SMs free up; it waits for this grid
 
   MmaWarp<F, NQ> w(k);
   w.init_lane(lane);
@@ -1074,8 +1076,8 @@ cudaError_t launch_shape(const DecodeLaunch& k, long long items, int sm_count, c
   const cudaError_t e =
       cudaFuncSetAttribute(attend_mma_kernel<F, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::Smem);
   if (e != cudaSuccess) return e;
-  attend_mma_kernel<F, NQ><<<(unsigned)grid, L::Threads, L::Smem, s>>>(k);
-  return cudaGetLastError();
+  // a dependent of the query prologue: the tables are built while it runs
+  return launch_pdl(attend_mma_kernel<F, NQ>, dim3((unsigned)grid), dim3(L::Threads), (size_t)L::Smem, s, k);
 }
 
 template <class F>

@@ -65,6 +65,29 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start while the kernel
+// before it in the stream is still running, once every CTA of that kernel has called
+// pdl_launch_dependents (or exited); before it reads anything that kernel writes it calls
+// pdl_wait, which returns when that kernel has completed and its writes are visible.  Both are
+// no-ops for kernels launched the ordinary way.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <class... P, class... A>
+cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, A&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<A&&>(args)...);
+}
+
 // Index of vector (layer, slot, head) in a view, or -1 if the slot is outside
 // the layer's pages.
 __device__ __forceinline__ long long view_vector_index(const DevView& v, int layer, long long slot, int head) {
