@@ -56,46 +56,51 @@ using DecodeKernelArgs = DecodeLaunch;
 // ---------------------------------------------------------------------------
 // 1. query prologue
 // ---------------------------------------------------------------------------
-// One CTA of D threads per kQprepRows query rows: warp w rotates rows w, w + D/32, ... (signs, WHT,
-// softmax scale) into shared memory, then thread j forms (S q')_j = sum_i S_T[i][j] q'_i of every
-// row, so each element of S is read once per CTA and used for all its rows.  S_T streams through
-// shared memory in 16 KB chunks of rows (asynchronous copies, two chunks in flight), so the reads
-// are in flight together rather than one dependent load per product.  The grid lets the attention
-// kernel that follows launch at once (programmatic dependent launch): that kernel builds its tables
-// meanwhile and waits for this grid before it reads anything written here.
-constexpr int kQprepRows = 8;
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
-               : "memory");
+// One CTA of 4 D threads per kQprepRows query rows.  Warp w < kQprepRows rotates row w (signs,
+// WHT, softmax scale) into shared memory; then thread (part p, j) forms the partial sums over
+// i in [p d/4, (p + 1) d/4) of (S q')_j = sum_i S_T[i][j] q'_i for every row, and the four parts
+// are added in a fixed order, so each element of S is read once per CTA and used for all its rows.
+// At d <= 128 all of S_T comes into shared memory by asynchronous copies requested before the
+// rotation starts (its reads in flight together); at d = 256 (256 KB) the parts read it from
+// global memory.  The grid lets the attention kernel that follows launch at once (programmatic
+// dependent launch): that kernel builds its tables meanwhile and waits for this grid before it
+// reads anything written here.
+constexpr int kQprepRows = 8, kQprepParts = 4;
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+template <int D>
+__host__ __device__ constexpr int qprep_smem() {
+  return D <= 128 ? D * D * 4 : 0;  // S_T staged whole
+}
 
 template <int D>
-__global__ void __launch_bounds__(D) qprep_kernel(DecodeKernelArgs ka) {
-  constexpr int E = D / 32, NW = D / 32, RQ = kQprepRows;
-  constexpr int CH = 4096 / D, NC = D / CH;  // S_T rows per chunk (16 KB), chunks
+__global__ void __launch_bounds__(kQprepParts * D) qprep_kernel(DecodeKernelArgs ka) {
+  constexpr int E = D / 32, RQ = kQprepRows, NP = kQprepParts, T = NP * D, IP = D / NP;
+  constexpr bool STAGE = qprep_smem<D>() > 0;
+  static_assert(T / 32 >= RQ, "one warp per row");
   pdl_launch_dependents();
   const DecodeArgs& a = ka.a;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const long long row0 = (long long)blockIdx.x * RQ;
   const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
   if (blockIdx.x == 0 && threadIdx.x < 2) ka.counter[threadIdx.x] = 0u;  // work counters of the attention launches
-  __shared__ __align__(16) float q_s[D][RQ];      // q'_i of the CTA's rows: row r at [i][r]
-  __shared__ __align__(16) float s_s[2][CH * D];  // chunks of S_T
-  const bool q8 = a.k.format == TQ_FMT_Q8_0;      // q8_0 K scores the unrotated q, and needs no S q
-  auto stage = [&](int c) {
-    const float* src = ka.tab.S_T + (size_t)c * CH * D;
-    float* dst = s_s[c & 1];
+  __shared__ __align__(16) float q_s[D][RQ];       // q'_i of the CTA's rows: row r at [i][r]
+  __shared__ __align__(16) float red[NP][RQ][D];   // the parts' partial sums
+  extern __shared__ __align__(16) float s_s[];     // S_T (d <= 128)
+  const bool q8 = a.k.format == TQ_FMT_Q8_0;       // q8_0 K scores the unrotated q, and needs no S q
+  if (STAGE && !q8) {
+    const uint32_t dst = (uint32_t)__cvta_generic_to_shared(s_s);
+    const char* src = reinterpret_cast<const char*>(ka.tab.S_T);
 #pragma unroll
-    for (int p = threadIdx.x; p < CH * D / 4; p += D) cp_async16(dst + 4 * p, src + 4 * p);
-    cp_async_commit();
-  };
-  if (!q8) stage(0);
-  for (int r = w; r < RQ; r += NW) {
-    const long long row = row0 + r;
+    for (int p = threadIdx.x; p < D * D / 4; p += T) cp_async16(dst + 16 * p, src + 16 * p);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  if (w < RQ) {
+    const long long row = row0 + w;
     float x[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) x[e] = 0.f;
     if (row < rows) {  // warp-uniform
       if (a.q_is_fp16) {
         const __half* q = static_cast<const __half*>(a.q) + io_row_of(a, row) * D;
@@ -117,50 +122,59 @@ __global__ void __launch_bounds__(D) qprep_kernel(DecodeKernelArgs ka) {
         x[e] *= a.softmax_scale;
         dst[E * lane + e] = x[e];
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < E; ++e) x[e] = 0.f;
     }
 #pragma unroll
-    for (int e = 0; e < E; ++e) q_s[E * lane + e][r] = x[e];
+    for (int e = 0; e < E; ++e) q_s[E * lane + e][w] = x[e];
   }
   if (q8) return;  // block-uniform
-  const int j = threadIdx.x;
+  if (STAGE) asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncthreads();  // q_s and S_T visible to every thread
+  const int j = threadIdx.x % D, part = threadIdx.x / D;
   float acc[RQ];
 #pragma unroll
   for (int r = 0; r < RQ; ++r) acc[r] = 0.f;
-  for (int c = 0; c < NC; ++c) {
-    if (c + 1 < NC) {
-      stage(c + 1);  // its buffer was last read by chunk c - 1, which every thread finished (barrier below)
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();  // chunk c (and, the first time, q_s) visible to every thread
-    const float* sc = s_s[c & 1] + j;
 #pragma unroll 8
-    for (int k = 0; k < CH; ++k) {
-      const float sv = sc[k * D];
-      const float4 qa = *reinterpret_cast<const float4*>(&q_s[c * CH + k][0]);
-      const float4 qb = *reinterpret_cast<const float4*>(&q_s[c * CH + k][4]);
-      acc[0] = fmaf(sv, qa.x, acc[0]);
-      acc[1] = fmaf(sv, qa.y, acc[1]);
-      acc[2] = fmaf(sv, qa.z, acc[2]);
-      acc[3] = fmaf(sv, qa.w, acc[3]);
-      acc[4] = fmaf(sv, qb.x, acc[4]);
-      acc[5] = fmaf(sv, qb.y, acc[5]);
-      acc[6] = fmaf(sv, qb.z, acc[6]);
-      acc[7] = fmaf(sv, qb.w, acc[7]);
-    }
-    __syncthreads();  // every thread is done with buffer c & 1 before chunk c + 2 is copied into it
+  for (int k = 0; k < IP; ++k) {
+    const int i = part * IP + k;
+    const float sv = STAGE ? s_s[i * D + j] : __ldg(ka.tab.S_T + (size_t)i * D + j);
+    const float4 qa = *reinterpret_cast<const float4*>(&q_s[i][0]);
+    const float4 qb = *reinterpret_cast<const float4*>(&q_s[i][4]);
+    acc[0] = fmaf(sv, qa.x, acc[0]);
+    acc[1] = fmaf(sv, qa.y, acc[1]);
+    acc[2] = fmaf(sv, qa.z, acc[2]);
+    acc[3] = fmaf(sv, qa.w, acc[3]);
+    acc[4] = fmaf(sv, qb.x, acc[4]);
+    acc[5] = fmaf(sv, qb.y, acc[5]);
+    acc[6] = fmaf(sv, qb.z, acc[6]);
+    acc[7] = fmaf(sv, qb.w, acc[7]);
   }
 #pragma unroll
-  for (int r = 0; r < RQ; ++r) {
-    if (row0 + r < rows) ka.qprep[(row0 + r) * 2 * D + D + j] = acc[r];
+  for (int r = 0; r < RQ; ++r) red[part][r][j] = acc[r];
+  __syncthreads();
+  // thread t < RQ D: row t / D, output j, the parts added in order
+  for (int t = threadIdx.x; t < RQ * D; t += T) {
+    const int r = t / D, jj = t % D;
+    if (row0 + r < rows) {
+      float v = red[0][r][jj];
+#pragma unroll
+      for (int p = 1; p < NP; ++p) v += red[p][r][jj];
+      ka.qprep[(row0 + r) * 2 * D + D + jj] = v;
+    }
   }
 }
 static_assert(kQprepRows == 8, "the S q' loop reads the rows as two float4");
 inline long long qprep_blocks(long long rows) { return (rows + kQprepRows - 1) / kQprepRows; }
+// The prologue over `rows` query rows (its dynamic shared memory holds the chunks of S_T).
+template <int D>
+cudaError_t launch_qprep_dim(const DecodeKernelArgs& ka, long long rows, cudaStream_t s) {
+  constexpr int smem = qprep_smem<D>();
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(qprep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  qprep_kernel<D><<<(unsigned)qprep_blocks(rows), kQprepParts * D, smem, s>>>(ka);
+  return cudaGetLastError();
+}
 
 // ---------------------------------------------------------------------------
 // token addressing of the generic kernel
@@ -452,6 +466,15 @@ __global__ void __launch_bounds__(32 * kCombineWarps, 8) combine_kernel(DecodeKe
       for (int e = 0; e < E; ++e) x[e] = fmaf(xs[q][E * lane + e], wq, x[e]);
     }
   }
+  // the row's partials are dead now: drop the 128-byte lines that lie wholly inside them from L2
+  // without writing them back
+  {
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(part), b1 = b0 + (uintptr_t)ns * (D + 4) * 4;
+    for (uintptr_t ln = (b0 + 127) & ~(uintptr_t)127; ln + 128 <= b1; ln += 32 * 128) {
+      const uintptr_t at = ln + 128 * lane;
+      if (at + 128 <= b1) asm volatile("discard.global.L2 [%0], 128;" ::"l"(at) : "memory");
+    }
+  }
   const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
   for (int e = 0; e < E; ++e) x[e] *= inv;
@@ -520,7 +543,8 @@ template <int D>
 cudaError_t launch_decode_dim(const DecodeKernelArgs& ka, int sm_count, cudaStream_t s) {
   const DecodeArgs& a = ka.a;
   const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
-  qprep_kernel<D><<<(unsigned)qprep_blocks(rows), D, 0, s>>>(ka);
+  const cudaError_t eq = launch_qprep_dim<D>(ka, rows, s);
+  if (eq != cudaSuccess) return eq;
   if (attend_mma_supported(ka, D)) {
     const cudaError_t e = launch_attend_mma(ka, D, sm_count, s);
     if (e != cudaSuccess) return e;
@@ -549,9 +573,9 @@ cudaError_t launch_qprep(const DevTables& t, const DecodeArgs& a, float* qprep, 
   const long long rows = (long long)a.n_layers * a.batch * a.n_q_heads;
   if (rows <= 0) return cudaSuccess;
   switch (t.d) {
-    case 64: qprep_kernel<64><<<(unsigned)qprep_blocks(rows), 64, 0, s>>>(ka); break;
-    case 128: qprep_kernel<128><<<(unsigned)qprep_blocks(rows), 128, 0, s>>>(ka); break;
-    case 256: qprep_kernel<256><<<(unsigned)qprep_blocks(rows), 256, 0, s>>>(ka); break;
+    case 64: return launch_qprep_dim<64>(ka, rows, s);
+    case 128: return launch_qprep_dim<128>(ka, rows, s);
+    case 256: return launch_qprep_dim<256>(ka, rows, s);
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -231,7 +231,8 @@ struct MmaWarp {
   int vhdr;                  // byte offset of this lane's V header entry (q8_0: its block's scale)
   int vwo[F::VLoad];         // byte offsets of the V words from the first (clamped to the payload)
   bool pf_k, pf_v, pf_h;     // bulk prefetch allowed (16-byte aligned tile starts)
-  uint64_t pol;
+  uint64_t pol;              // cache loads: evict first
+  uint64_t pol_keep;         // partials: evict last (the combine reads them from L2, then drops them)
 
   int layer, layer_v, b, kvh, ntiles, last_valid;  // layer: of the K view; layer_v: of the V view
   int gof, gcn;  // this item's query heads: [gof, gof + gcn) of the KV head's G
@@ -968,11 +969,8 @@ struct MmaWarp {
       float* dst = k.partial + ((row0 + gof + head) * k.n_splits + split) * (D + 4);
       float4* dv = reinterpret_cast<float4*>(dst + 4 + g * (D / 8));
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) dv[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      if (g == 0) {
-        dst[0] = m[h] == -INFINITY ? -INFINITY : m[h] * kLn2;
-        dst[1] = l[h];
-      }
+      for (int q = 0; q < D / 32; ++q) st_keep_v4(dv + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]), pol_keep);
+      if (g == 0) st_keep_v2(dst, make_float2(m[h] == -INFINITY ? -INFINITY : m[h] * kLn2, l[h]), pol_keep);
     }
   }
 
@@ -1054,6 +1052,7 @@ __global__ void __launch_bounds__(Shape<F, NQ>::Threads, 1) attend_mma_kernel(De
   w.psr = ps + 4 * ps_word(w.g, w.t);
   w.qf = ps + L::PsBytes + lane * (F::KQ8 ? 8 : 16);
   asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(w.pol));
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(w.pol_keep));
 
   const DecodeArgs& a = k.a;
   const unsigned int n_items = (unsigned int)((long long)a.n_layers * a.batch * a.k.H * k.n_splits * k.g_halves);
