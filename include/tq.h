@@ -235,8 +235,15 @@ size_t tq_decode_workspace_bytes(const tq_context* ctx, int n_layers, int batch,
  *   skip_threshold: V terms whose weight exp(s - running max) is below it are
  *     not accumulated (Sparse V); 0 keeps every term.  The softmax denominator
  *     keeps every token.
+ *   workspace: device scratch of tq_decode_workspace_bytes() bytes, 256-byte
+ *     aligned; its contents are undefined after the call (the combine drops the
+ *     split partials from L2 without writing them back).
  *   K formats: turbo (with or without QJL) or Q8_0.  V formats: turbo _MSE or
  *   Q8_0.  A sequence of length 0 yields zeros.
+ *   The call is three kernels on `stream`: the query prologue, the split-K
+ *   attention (launched as a programmatic dependent of the prologue) and the
+ *   combine (a dependent of the attention); work queued after it on the stream
+ *   sees the finished result, as after any kernel.
  */
 tq_status tq_decode_attention(const tq_context* ctx,
                               const void* q, int q_is_fp16,
