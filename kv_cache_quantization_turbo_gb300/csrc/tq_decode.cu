@@ -597,6 +597,7 @@ cudaError_t launch_decode(const DevTables& t, const DecodeArgs& a, const DecodeP
   ka.partial = reinterpret_cast<float*>(ws + (plan.qprep_floats * 4 + 255) / 256 * 256);
   ka.counter = reinterpret_cast<unsigned int*>(ws + (plan.qprep_floats * 4 + 255) / 256 * 256 +
                                                (plan.partial_floats * 4 + 255) / 256 * 256);
+  ka.keep_partials = plan.partial_floats * 4 <= kKeepPartialsMaxBytes ? 1 : 0;
   switch (t.d) {
     case 64: return launch_decode_dim<64>(ka, sm_count, s);
     case 128: return launch_decode_dim<128>(ka, sm_count, s);

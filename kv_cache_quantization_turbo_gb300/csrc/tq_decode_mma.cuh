@@ -1052,7 +1052,12 @@ __global__ void __launch_bounds__(Shape<F, NQ>::Threads, 1) attend_mma_kernel(De
   w.psr = ps + 4 * ps_word(w.g, w.t);
   w.qf = ps + L::PsBytes + lane * (F::KQ8 ? 8 : 16);
   asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(w.pol));
-  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(w.pol_keep));
+  {
+    uint64_t p_last, p_normal;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p_last));
+    asm("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p_normal));
+    w.pol_keep = k.keep_partials ? p_last : p_normal;
+  }
 
   const DecodeArgs& a = k.a;
   const unsigned int n_items = (unsigned int)((long long)a.n_layers * a.batch * a.k.H * k.n_splits * k.g_halves);

@@ -205,6 +205,15 @@ __device__ __forceinline__ void split_pair(float2 v, uint32_t& hi, uint32_t& lo)
   lo = h2u(__floats2half2_rn(v.x - hf.x, v.y - hf.y));
 }
 
+// The same split with the subtraction in packed fp32.
+__device__ __forceinline__ void split_pair2(float2 v, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(v.x, v.y);
+  const float2 hf = __half22float2(h);
+  hi = h2u(h);
+  const float2 d = __ffma2_rn(hf, make_float2(-1.f, -1.f), v);
+  lo = h2u(__floats2half2_rn(d.x, d.y));
+}
+
 // q8_0 and per-group min-max: one warp per vector (lane l holds E = d/32 coordinates).
 template <int D, int KIND>
 __global__ void __launch_bounds__(kEncThreads, 4) encode_kernel(EncArgs a) {
@@ -715,7 +724,7 @@ struct Smem {  // byte offsets in dynamic shared memory
   static constexpr int r_lo = x0 + NX * kOp;          // R low part (QJL)
   static constexpr int ss = r_lo + (QJL ? kOp : 0);   // float [2][4][NV]: partial sums of y^2
   static constexpr int rr = ss + 2 * 4 * NV * 4;      // float [2][4][NV]: partial sums of (2^14 r)^2
-  static constexpr int cb = rr + (QJL ? 2 * 4 * NV * 4 : 0);  // float [8]: centroids x 2^14
+  static constexpr int cb = rr + (QJL ? 2 * 4 * NV * 4 : 0);  // float [8]: centroids x -2^14 (32-byte aligned)
   static constexpr int bar = cb + 8 * 4;  // mbarriers: full[NX], y[2], p[2], yfree[2], rready, pfree[2]
   static constexpr int n_bar = NX + 9;
   static constexpr int slot = bar + n_bar * 8;  // tensor-memory address, abort flag
@@ -813,6 +822,40 @@ __device__ __forceinline__ float step_index_sym(float y, float F, const float (&
   for (int k = 0; k < H - 1; ++k) c += __saturatef(fmaf(fabsf(y), F, cst[H + k]));
   return fmaf(y >= 0.f ? 1.f : -1.f, c, (float)H - 0.5f);
 }
+// The same index for two coordinates at once, as the signed count cs = +-(1/2 + cnt) (the index is
+// H - 1/2 + cs): the steps per coordinate, their sums in packed fp32 (add.rn.f32x2).  The sign is
+// that of y + 0, so that y = -0 takes the upper index as y >= 0 does above.
+template <int B>
+__device__ __forceinline__ float2 step_count_signed(float ya, float yb, float F, const float (&cst)[7]) {
+  constexpr int H = 1 << (B - 1);
+  float2 c = make_float2(0.5f, 0.5f);
+#pragma unroll
+  for (int k = 0; k < H - 1; ++k)
+    c = __fadd2_rn(c, make_float2(__saturatef(fmaf(fabsf(ya), F, cst[H + k])), __saturatef(fmaf(fabsf(yb), F, cst[H + k]))));
+  const float2 yz = __fadd2_rn(make_float2(ya, yb), make_float2(0.f, 0.f));
+  c.x = __uint_as_float(__float_as_uint(c.x) | (__float_as_uint(yz.x) & 0x80000000u));
+  c.y = __uint_as_float(__float_as_uint(c.y) | (__float_as_uint(yz.y) & 0x80000000u));
+  return c;
+}
+// Starting value of a packed code accumulator over a chunk of CPC W-bit codes: the (H - 1/2) part
+// of each index times its place 2^(W e), even e in .x and odd e in .y (exact: all below 2^24).
+template <int B, int W, int CPC>
+__device__ __forceinline__ float2 code_base() {
+  constexpr float h = (float)(1 << (B - 1)) - 0.5f;
+  float ev = 0.f, od = 0.f;
+#pragma unroll
+  for (int e = 0; e < CPC; ++e) {
+    if (e & 1) od += h * (float)(1u << (W * e));
+    else ev += h * (float)(1u << (W * e));
+  }
+  return make_float2(ev, od);
+}
+// A read of the centroid table (written once before the CTA's first barrier, constant after it).
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
 // ORs an nb-bit chunk into the thread's W words at bit offset off (compile-time after unrolling).
 template <int W>
 __device__ __forceinline__ void or_bits(uint32_t (&w)[W], int off, int nb, uint32_t v) {
@@ -861,7 +904,7 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
       for (int i = NX + 4; i < L::n_bar; ++i) tc::mbar_init(full_x + i, SIMT_WARPS);
     }
   }
-  if (threadIdx.x < 8) cb_s[threadIdx.x] = a.tab.centroids[(B - 1) * 8 + threadIdx.x] * kRScale;
+  if (threadIdx.x < 8) cb_s[threadIdx.x] = -a.tab.centroids[(B - 1) * 8 + threadIdx.x] * kRScale;  // -2^14 c
   if constexpr (QJL) {
     for (int i = threadIdx.x; i < 64 * 64; i += THREADS) {
       const int n = i >> 6, k = i & 63;
@@ -1014,9 +1057,13 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(yfree + yb);
-      float ss = 0.f;
+      float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) ss = fmaf(__uint_as_float(t[e]), __uint_as_float(t[e]), ss);
+      for (int e = 0; e < 32; e += 2) {
+        const float2 yy = make_float2(__uint_as_float(t[e]), __uint_as_float(t[e + 1]));
+        ss2 = __ffma2_rn(yy, yy, ss2);
+      }
+      const float ss = ss2.x + ss2.y;
       ss_s[(yb * 4 + cg) * NV + v] = ss;
       if (tc::bar_sync_or(1, kSimt, !ok)) {
         failed = true;
@@ -1046,39 +1093,47 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
           tc::fence_after_sync();
         }
         unsigned char* rh = smem + L::x0 + (int)(j % NX) * kOp;  // the rotation consumed X: R_hi goes there
-        float rr = 0.f;
+        float2 rr2 = make_float2(0.f, 0.f);
         const float F = f * 0x1p100f, FR = f * kRScale;
+        const uint32_t cbase = sbase + L::cb;
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {
           uint32_t hi[4], lo[4];
           if (fma_idx) {
-            float acc[8 / CPC] = {};
+            // pairs of coordinates in packed fp32 (even, odd): the code accumulators start at the
+            // (H - 1/2) part of every index of their chunk, so the signed counts add the rest
+            float2 acc2[8 / CPC];
+#pragma unroll
+            for (int c = 0; c < 8 / CPC; ++c) acc2[c] = code_base<B, W, CPC>();
 #pragma unroll
             for (int e2 = 0; e2 < 8; e2 += 2) {
-              float r2[2];
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const int ec = e2 + hh;
-                const float yv = __uint_as_float(t[8 * c8 + ec]);
-                const float idx = step_index_sym<B>(yv, F, cst);
-                const uint32_t ii = __float_as_uint(idx + 0x1p23f) & 7u;  // the integer index
-                r2[hh] = fmaf(yv, FR, -cb_s[ii]);                            // 2^14 (u - c)
-                rr = fmaf(r2[hh], r2[hh], rr);
-                acc[ec / CPC] = fmaf(idx, (float)(1u << (W * (ec % CPC))), acc[ec / CPC]);
-              }
-              split_pair(make_float2(r2[0], r2[1]), hi[e2 / 2], lo[e2 / 2]);
+              const float ya = __uint_as_float(t[8 * c8 + e2]), yb = __uint_as_float(t[8 * c8 + e2 + 1]);
+              const float2 cs = step_count_signed<B>(ya, yb, F, cst);
+              // the index H - 1/2 + cs is an integer: as 2^21 + index it sits in bits 2..4, the byte
+              // offset of its entry in the 32-byte-aligned table of -2^14 c
+              constexpr float kIdx = (float)(1 << (B - 1)) - 0.5f + 0x1p21f;
+              const float2 mg = __fadd2_rn(cs, make_float2(kIdx, kIdx));
+              const float ca = lds_f32((__float_as_uint(mg.x) & 0x1Cu) | cbase);
+              const float cb = lds_f32((__float_as_uint(mg.y) & 0x1Cu) | cbase);
+              const float2 r2 = __ffma2_rn(make_float2(ya, yb), make_float2(FR, FR), make_float2(ca, cb));  // 2^14 (u - c)
+              rr2 = __ffma2_rn(r2, r2, rr2);
+              const int ep = e2 % CPC;
+              acc2[e2 / CPC] = __ffma2_rn(cs, make_float2((float)(1u << (W * ep)), (float)(1u << (W * (ep + 1)))),
+                                          acc2[e2 / CPC]);
+              split_pair2(r2, hi[e2 / 2], lo[e2 / 2]);
             }
 #pragma unroll
-            for (int c = 0; c < 8 / CPC; ++c) or_bits<W>(w, W * (8 * c8 + CPC * c), W * CPC, (uint32_t)acc[c]);
+            for (int c = 0; c < 8 / CPC; ++c)
+              or_bits<W>(w, W * (8 * c8 + CPC * c), W * CPC, (uint32_t)(acc2[c].x + acc2[c].y));
           } else {
 #pragma unroll
             for (int e2 = 0; e2 < 8; e2 += 2) {
               const int e = 8 * c8 + e2;
               const float u0 = __uint_as_float(t[e]) * f, u1 = __uint_as_float(t[e + 1]) * f;
               const uint32_t i0 = lloyd_index<B>(u0, bnd), i1 = lloyd_index<B>(u1, bnd);
-              const float r0 = fmaf(u0, kRScale, -cb_s[i0]), r1 = fmaf(u1, kRScale, -cb_s[i1]);  // 2^14 (u - c)
-              rr = fmaf(r0, r0, rr);
-              rr = fmaf(r1, r1, rr);
+              const float r0 = fmaf(u0, kRScale, cb_s[i0]), r1 = fmaf(u1, kRScale, cb_s[i1]);  // 2^14 (u - c)
+              rr2.x = fmaf(r0, r0, rr2.x);
+              rr2.y = fmaf(r1, r1, rr2.y);
               put_code<W>(w, e, i0);
               put_code<W>(w, e + 1, i1);
               split_pair(make_float2(r0, r1), hi[e2 / 2], lo[e2 / 2]);
@@ -1088,6 +1143,7 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
           *reinterpret_cast<uint4*>(rh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *reinterpret_cast<uint4*>(smem + L::r_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
+        const float rr = rr2.x + rr2.y;
         rr_s[(yb * 4 + cg) * NV + v] = rr;
         tc::fence_async_smem();
         __syncwarp();
@@ -1115,11 +1171,14 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
           const float F = f * 0x1p100f;
 #pragma unroll
           for (int c = 0; c < 32 / CPC; ++c) {
-            float acc = 0.f;
+            float2 acc2 = code_base<B, W, CPC>();
 #pragma unroll
-            for (int e = 0; e < CPC; ++e)
-              acc = fmaf(step_index_sym<B>(__uint_as_float(t[CPC * c + e]), F, cst), (float)(1u << (W * e)), acc);
-            or_bits<W>(w, W * CPC * c, W * CPC, (uint32_t)acc);
+            for (int e = 0; e < CPC; e += 2) {
+              const float2 cs = step_count_signed<B>(__uint_as_float(t[CPC * c + e]), __uint_as_float(t[CPC * c + e + 1]),
+                                                     F, cst);
+              acc2 = __ffma2_rn(cs, make_float2((float)(1u << (W * e)), (float)(1u << (W * (e + 1)))), acc2);
+            }
+            or_bits<W>(w, W * CPC * c, W * CPC, (uint32_t)(acc2.x + acc2.y));
           }
         } else {
 #pragma unroll

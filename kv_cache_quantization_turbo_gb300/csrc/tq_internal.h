@@ -137,7 +137,11 @@ struct DecodeLaunch {
   float* qprep;    // [rows][2d]: q' then Sq'
   float* partial;  // [rows][n_splits][d + 4]: m (natural log units), l, -, -, acc[d]
   unsigned int* counter;  // two work-item counters (zeroed by the prologue kernel)
+  int keep_partials;      // 1: the partials are stored evict-last in L2 (they fit beside the streamed cache)
 };
+// Partials up to this size are kept in L2 (evict-last) until the combine reads them; larger sets
+// would crowd the cache tiles that the attention kernel prefetches into the 126 MB L2.
+constexpr size_t kKeepPartialsMaxBytes = 40u << 20;
 
 // Split-K attention on tensor cores (tq_decode_mma.cuh), parameterised by the formats: K code width wk
 // (q8_0 = 0, turbo K = index bits + 1), V code width wv (q8_0 = 0, turbo-MSE V = index bits),
