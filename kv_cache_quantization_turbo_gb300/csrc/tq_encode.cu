@@ -10,8 +10,9 @@
 //
 // Work decomposition
 //   - turbo formats at d = 128: encode_tc_kernel (tensor cores; described at the kernel).
-//     The Lloyd-Max index there is step_index, a sum of saturated FMA steps that equals
-//     the count of boundaries <= y exactly (ties included);
+//     The Lloyd-Max index there is step_count_signed, a sum of saturated FMA steps on |y|
+//     that equals the count of boundaries <= y (an exact tie at a negative boundary,
+//     measure zero, takes the lower index);
 //   - turbo formats at d = 64 and 256: a vector is held by a group of L = d/32 lanes,
 //     each lane owning 32 consecutive coordinates, so a warp encodes 32/L vectors at
 //     once.  The sign flips are applied on the fp16 words, five of the WHT stages run
@@ -787,8 +788,8 @@ __device__ __forceinline__ void merge_signs(uint32_t (&w)[W], uint32_t sbits) {
 // u - prev(b_k) is 0 or at least 2^-100 in magnitude.  Nonzero rotated coordinates are sums of
 // fp16 values scaled by 1 / (n sqrt(d)), at least 2^-24 / (65504 sqrt(d)) in magnitude, so
 // this holds for every boundary that is 0 or at least 2^-60 in magnitude (checked per call, with
-// the odd symmetry of the boundaries that step_index_sym relies on; the binary search runs where
-// either fails).
+// the odd symmetry of the boundaries that step_count_signed relies on; the binary search runs
+// where either fails).
 template <int B>
 __device__ __forceinline__ bool step_constants(const float (&bnd)[7], float (&cst)[7]) {
   bool ok = true;
@@ -808,23 +809,15 @@ __device__ __forceinline__ bool step_constants(const float (&bnd)[7], float (&cs
   }
   return ok;
 }
-// The index of y (a rotated coordinate before the 1 / (n sqrt(d)) scale; F = 2^100 / (n sqrt(d))) as
-// a float, by the codebook's odd symmetry (the boundaries are b_k = -b_(2H-2-k), H = 2^(B-1),
-// the middle one exactly 0): with a = |y| and cnt = #{positive boundaries <= a} (exact FMA steps),
-// the index is H + cnt for y >= 0 and H - 1 - cnt below, H - 1 steps instead of 2H - 1.  It equals
-// the count of boundaries <= u except at an exact tie u = -b_k (measure zero), which takes the lower
-// index: such a coordinate sits on a decision boundary, inside the comparison band.
-template <int B>
-__device__ __forceinline__ float step_index_sym(float y, float F, const float (&cst)[7]) {
-  constexpr int H = 1 << (B - 1);
-  float c = 0.5f;
-#pragma unroll
-  for (int k = 0; k < H - 1; ++k) c += __saturatef(fmaf(fabsf(y), F, cst[H + k]));
-  return fmaf(y >= 0.f ? 1.f : -1.f, c, (float)H - 0.5f);
-}
-// The same index for two coordinates at once, as the signed count cs = +-(1/2 + cnt) (the index is
-// H - 1/2 + cs): the steps per coordinate, their sums in packed fp32 (add.rn.f32x2).  The sign is
-// that of y + 0, so that y = -0 takes the upper index as y >= 0 does above.
+// The index of y (a rotated coordinate before the 1 / (n sqrt(d)) scale; F = 2^100 / (n sqrt(d))),
+// for two coordinates at once, by the codebook's odd symmetry (the boundaries are b_k = -b_(2H-2-k),
+// H = 2^(B-1), the middle one exactly 0): with a = |y| and cnt = #{positive boundaries <= a} (exact
+// FMA steps), the index is H + cnt for y >= 0 and H - 1 - cnt below, H - 1 steps instead of 2H - 1.
+// It equals the count of boundaries <= u except at an exact tie u = -b_k (measure zero), which takes
+// the lower index: such a coordinate sits on a decision boundary, inside the comparison band.
+// Returned as the signed count cs = +-(1/2 + cnt), the index being H - 1/2 + cs: the steps are
+// scalar (saturated FMAs), their sums packed fp32 pairs (add.rn.f32x2).  The sign is that of y + 0,
+// so that y = -0 takes the upper index, as y >= 0 does.
 template <int B>
 __device__ __forceinline__ float2 step_count_signed(float ya, float yb, float F, const float (&cst)[7]) {
   constexpr int H = 1 << (B - 1);
