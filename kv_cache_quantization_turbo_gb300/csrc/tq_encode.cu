@@ -723,11 +723,12 @@ struct Smem {  // byte offsets in dynamic shared memory
   static constexpr int s_lo = s_hi + (QJL ? kOp : 0);
   static constexpr int x0 = s_lo + (QJL ? kOp : 0);  // NX input tiles (batch j in tile j % NX)
   static constexpr int r_lo = x0 + NX * kOp;          // R low part (QJL)
-  static constexpr int ss = r_lo + (QJL ? kOp : 0);   // float [2][4][NV]: partial sums of y^2
-  static constexpr int rr = ss + 2 * 4 * NV * 4;      // float [2][4][NV]: partial sums of (2^14 r)^2
+  static constexpr int NY = QJL ? 2 : 4;             // Y buffers in tensor memory
+  static constexpr int ss = r_lo + (QJL ? kOp : 0);   // float [NY][4][NV]: partial sums of y^2
+  static constexpr int rr = ss + NY * 4 * NV * 4;     // float [2][4][NV]: partial sums of (2^14 r)^2
   static constexpr int cb = rr + (QJL ? 2 * 4 * NV * 4 : 0);  // float [8]: centroids x -2^14 (32-byte aligned)
-  static constexpr int bar = cb + 8 * 4;  // mbarriers: full[NX], y[2], p[2], yfree[2], rready, pfree[2]
-  static constexpr int n_bar = NX + 9;
+  static constexpr int bar = cb + 8 * 4;  // mbarriers: full[NX], y[NY], p[2], yfree[NY], rready, pfree[2]
+  static constexpr int n_bar = NX + 2 * NY + 5;
   static constexpr int slot = bar + n_bar * 8;  // tensor-memory address, abort flag
   static constexpr int total = slot + 16;
 };
@@ -867,7 +868,8 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
   constexpr int NX = L::NX;
   constexpr int W = QJL ? B + 1 : B;
   constexpr int kSimt = 32 * SIMT_WARPS;
-  constexpr uint32_t kCols = QJL ? 512 : 256;  // Y[2] at columns [0, 256), P[2] at [256, 512)
+  constexpr int NY = L::NY;
+  constexpr uint32_t kCols = 512;  // K: Y[2] at columns [0, 256), P[2] at [256, 512); V: Y[4]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   constexpr int THREADS = kThreads<QJL>;
   const bool issuer = warp >= SIMT_WARPS;  // warp SIMT_WARPS: issuer A; SIMT_WARPS + 1: issuer B
@@ -883,9 +885,9 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
   float* cb_s = reinterpret_cast<float*>(smem + L::cb);
   uint64_t* full_x = reinterpret_cast<uint64_t*>(smem + L::bar);  // tile landed (TMA)
   uint64_t* bar_y = full_x + NX;    // rotation of a batch done
-  uint64_t* bar_p = bar_y + 2;      // projection of a batch done
-  uint64_t* yfree = bar_p + 2;      // Y of a batch read by all 16 SIMT warps
-  uint64_t* rready = yfree + 2;     // R of a batch stored by all 16 SIMT warps
+  uint64_t* bar_p = bar_y + NY;     // projection of a batch done
+  uint64_t* yfree = bar_p + 2;      // Y of a batch read by the SIMT warps that take it (K: 16, V: 8)
+  uint64_t* rready = yfree + NY;    // R of a batch stored by all 16 SIMT warps
   uint64_t* pfree = rready + 1;     // P of a batch read by all 16 SIMT warps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::slot);
   const uint32_t sbase = tc::smem_addr(smem);
@@ -893,8 +895,8 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
   if (warp == SIMT_WARPS) {
     tc::tmem_alloc(tmem_slot, kCols);
     if (lane == 0) {
-      for (int i = 0; i < NX + 4; ++i) tc::mbar_init(full_x + i, 1);
-      for (int i = NX + 4; i < L::n_bar; ++i) tc::mbar_init(full_x + i, SIMT_WARPS);
+      for (int i = 0; i < NX + NY + 2; ++i) tc::mbar_init(full_x + i, 1);
+      for (int i = NX + NY + 2; i < L::n_bar; ++i) tc::mbar_init(full_x + i, QJL ? SIMT_WARPS : SIMT_WARPS / 2);
     }
   }
   if (threadIdx.x < 8) cb_s[threadIdx.x] = -a.tab.centroids[(B - 1) * 8 + threadIdx.x] * kRScale;  // -2^14 c
@@ -950,7 +952,7 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
       const uint64_t dg = tc::desc_sw128(sbase + L::g);
       auto issue_mma1 = [&](long long jj) {
         const uint64_t dx = tc::desc_sw128(sbase + L::x0 + (uint32_t)(jj % NX) * kOp);
-        const uint32_t d0 = tmem + (uint32_t)(jj & 1) * 128;
+        const uint32_t d0 = tmem + (uint32_t)(jj % NY) * 128;
         if constexpr (QJL) {
           constexpr uint32_t id64 = tc::idesc_f16_f32(128, 64);
 #pragma unroll
@@ -968,7 +970,7 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
           for (int ks = 0; ks < D / 16; ++ks)
             tc::mma_f16(d0, dx + (kstep<NV>(ks) >> 4), dg + (kstep<D>(ks) >> 4), id128, ks > 0);
         }
-        tc::commit(bar_y + (jj & 1));
+        tc::commit(bar_y + (int)(jj % NY));
         mma1_done = jj + 1;
       };
       auto issue_mma2 = [&](long long jj) {
@@ -992,10 +994,10 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
         // issuer A: tiles and rotations
         for (long long jj = 0; jj < NX && jj < nj; ++jj) issue_tma(jj);
         for (long long j = 0; ok && j <= nj; ++j) {
-          // rotation of batch j: its tile landed, and Y[j & 1] (batch j - 2) was read
+          // rotation of batch j: its tile landed, and Y[j % NY] (batch j - NY) was read
           if (j < nj) {
             ok = tc::mbar_wait(full_x + (int)(j % NX), (uint32_t)(j / NX) & 1u);
-            if (ok && j >= 2) ok = tc::mbar_wait(yfree + (j & 1), (uint32_t)((j - 2) >> 1) & 1u);
+            if (ok && j >= NY) ok = tc::mbar_wait(yfree + (int)(j % NY), (uint32_t)((j - NY) / NY) & 1u);
             if (!ok) break;
             tc::fence_after_sync();
             issue_mma1(j);
@@ -1004,7 +1006,7 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
           const long long jp = j - 1;
           if (jp >= 0 && jp + NX < nj) {
             ok = QJL ? tc::mbar_wait(bar_p + (jp & 1), (uint32_t)(jp >> 1) & 1u)
-                     : tc::mbar_wait(bar_y + (jp & 1), (uint32_t)(jp >> 1) & 1u);
+                     : tc::mbar_wait(bar_y + (int)(jp % NY), (uint32_t)(jp / NY) & 1u);
             if (ok) issue_tma(jp + NX);
           }
         }
@@ -1023,7 +1025,7 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
         // bounded waits for whatever this issuer still has in flight
         for (long long jj = mma1_done; jj < next_tma; ++jj)
           tc::mbar_wait(full_x + (int)(jj % NX), (uint32_t)(jj / NX) & 1u);
-        if (mma1_done > 0) tc::mbar_wait(bar_y + ((mma1_done - 1) & 1), (uint32_t)((mma1_done - 1) >> 1) & 1u);
+        if (mma1_done > 0) tc::mbar_wait(bar_y + (int)((mma1_done - 1) % NY), (uint32_t)((mma1_done - 1) / NY) & 1u);
         if (mma2_done > 0) tc::mbar_wait(bar_p + ((mma2_done - 1) & 1), (uint32_t)((mma2_done - 1) >> 1) & 1u);
       }
     }
@@ -1040,6 +1042,75 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
     long long vid_prev = -1;
     float n_prev = 0.f;
     bool ok = true;
+    if constexpr (!QJL) {
+      // turbo-MSE V: two groups of 8 SIMT warps take alternate batches (group g the batches j with
+      // j % 2 == g, in Y[j % 4]), so that one group's dependent steps overlap the other's; warp w of
+      // a group reads lane quarter w % 4 and the column groups 2 hq, 2 hq + 1 (two passes of 32
+      // columns, each read from tensor memory twice: for the norm, then for the codes), and the
+      // group meets on its own named barrier (1 + g, 256 threads) for the norm exchange
+      const int g = warp >> 3, hq = (warp >> 2) & 1;
+      for (long long j = g; j < nj; j += 2) {
+        const int yb = (int)(j % NY);
+        ok = tc::mbar_wait(bar_y + yb, (uint32_t)(j / NY) & 1u) && ok;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int ps = 0; ps < 2; ++ps) {
+          const int cgp = 2 * hq + ps;
+          uint32_t t[32];
+          tc::tmem_ld32(tmem + lane_base + yb * 128 + 32 * cgp, t);
+          float2 ss2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 yy = make_float2(__uint_as_float(t[e]), __uint_as_float(t[e + 1]));
+            ss2 = __ffma2_rn(yy, yy, ss2);
+          }
+          ss_s[(yb * 4 + cgp) * NV + v] = ss2.x + ss2.y;
+        }
+        if (tc::bar_sync_or(1 + g, kSimt / 2, !ok)) {
+          failed = true;
+          break;
+        }
+        const uint32_t bt = (uint32_t)(blockIdx.x + j * gridDim.x);
+        const uint32_t l = fdiv(bt, sh.div_tb), tb = bt - l * sh.n_tb;
+        const int tok = (int)(tb * sh.TB) + tt;
+        long long vid = -1;
+        if (v < sh.rows && tok < a.n_tokens) vid = vid_at(a, (int)l, tok, h, hq == 0);
+        const float* sp = ss_s + yb * 4 * NV + v;
+        const float n = sqrtf((sp[0] + sp[NV] + sp[2 * NV] + sp[3 * NV]) * (1.f / D));  // |x| = |H D x| / sqrt(d)
+        const float f = n > 0.f ? __fdividef(inv_sqrt_dim<D>(), n) : 0.f;
+#pragma unroll
+        for (int ps = 0; ps < 2; ++ps) {
+          const int cgp = 2 * hq + ps;
+          uint32_t t[32];
+          tc::tmem_ld32(tmem + lane_base + yb * 128 + 32 * cgp, t);
+          uint32_t w[W] = {};
+          if (fma_idx) {
+            const float F = f * 0x1p100f;
+#pragma unroll
+            for (int c = 0; c < 32 / CPC; ++c) {
+              float2 acc2 = code_base<B, W, CPC>();
+#pragma unroll
+              for (int e = 0; e < CPC; e += 2) {
+                const float2 cs = step_count_signed<B>(__uint_as_float(t[CPC * c + e]),
+                                                       __uint_as_float(t[CPC * c + e + 1]), F, cst);
+                acc2 = __ffma2_rn(cs, make_float2((float)(1u << (W * e)), (float)(1u << (W * (e + 1)))), acc2);
+              }
+              or_bits<W>(w, W * CPC * c, W * CPC, (uint32_t)(acc2.x + acc2.y));
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) put_code<W>(w, e, lloyd_index<B>(__uint_as_float(t[e]) * f, bnd));
+          }
+          if (vid >= 0) {
+            if (cgp == 0) *reinterpret_cast<__half*>(V.header + vid * V.hdr_bytes) = __float2half_rn(n);
+            store_words<W>(reinterpret_cast<uint32_t*>(V.payload + vid * V.pay_bytes) + W * cgp, w);
+          }
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(yfree + yb);
+      }
+    } else {
     for (long long j = 0; j < nj; ++j) {
       const int yb = (int)(j & 1);
       // (a) Y of batch j: partial sum of squares of this thread's 32 coordinates
@@ -1182,6 +1253,7 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
           store_words<W>(reinterpret_cast<uint32_t*>(V.payload + vid * V.pay_bytes) + W * cg, w);
         }
       }
+    }
     }
     if constexpr (QJL) {
       // the last batch: its header and sign bits
