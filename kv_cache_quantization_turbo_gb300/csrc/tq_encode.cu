@@ -1111,149 +1111,127 @@ __global__ void __launch_bounds__(etc::kThreads<QJL>, 1)
         if (lane == 0) tc::mbar_arrive(yfree + yb);
       }
     } else {
-    for (long long j = 0; j < nj; ++j) {
-      const int yb = (int)(j & 1);
-      // (a) Y of batch j: partial sum of squares of this thread's 32 coordinates
-      ok = tc::mbar_wait(bar_y + yb, (uint32_t)(j >> 1) & 1u) && ok;
-      tc::fence_after_sync();
-      uint32_t t[32];
-      tc::tmem_ld32(tmem + lane_base + yb * 128 + 32 * cg, t);
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(yfree + yb);
-      float2 ss2 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const float2 yy = make_float2(__uint_as_float(t[e]), __uint_as_float(t[e + 1]));
-        ss2 = __ffma2_rn(yy, yy, ss2);
-      }
-      const float ss = ss2.x + ss2.y;
-      ss_s[(yb * 4 + cg) * NV + v] = ss;
-      if (tc::bar_sync_or(1, kSimt, !ok)) {
-        failed = true;
-        break;
-      }
-      // (b) norm, destination
-      const uint32_t bt = (uint32_t)(blockIdx.x + j * gridDim.x);
-      const uint32_t l = fdiv(bt, sh.div_tb), tb = bt - l * sh.n_tb;
-      const int tok = (int)(tb * sh.TB) + tt;
-      long long vid = -1;
-      if (v < sh.rows && tok < a.n_tokens) vid = vid_at(a, (int)l, tok, h, cg == 0);
-      const float* sp = ss_s + yb * 4 * NV + v;
-      const float n = sqrtf((sp[0] + sp[NV] + sp[2 * NV] + sp[3 * NV]) * (1.f / D));  // |x| = |H D x| / sqrt(d)
-      const float f = n > 0.f ? __fdividef(inv_sqrt_dim<D>(), n) : 0.f;
-      uint32_t w[W] = {};
-      if constexpr (QJL) {
-        // header of batch j - 1 (its residual partial sums were stored before the barrier)
-        if (j > 0 && cg == 0 && vid_prev >= 0) {
-          const float* rp = rr_s + (1 - yb) * 4 * NV + v;
-          const float rs = (rp[0] + rp[NV] + rp[2 * NV] + rp[3 * NV]) * (1.f / (kRScale * kRScale));
-          *reinterpret_cast<__half2*>(V.header + vid_prev * V.hdr_bytes) =
-              __halves2half2(__float2half_rn(n_prev), __float2half_rn(n_prev * sqrtf(rs)));
-        }
-        // (c) index and residual; R_lo is free once the projection of batch j - 1 completed
-        if (j > 0) {
-          ok = tc::mbar_wait(bar_p + (1 - yb), (uint32_t)((j - 1) >> 1) & 1u) && ok;
-          tc::fence_after_sync();
-        }
-        unsigned char* rh = smem + L::x0 + (int)(j % NX) * kOp;  // the rotation consumed X: R_hi goes there
-        float2 rr2 = make_float2(0.f, 0.f);
-        const float F = f * 0x1p100f, FR = f * kRScale;
-        const uint32_t cbase = sbase + L::cb;
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          uint32_t hi[4], lo[4];
-          if (fma_idx) {
-            // pairs of coordinates in packed fp32 (even, odd): the code accumulators start at the
-            // (H - 1/2) part of every index of their chunk, so the signed counts add the rest
-            float2 acc2[8 / CPC];
-#pragma unroll
-            for (int c = 0; c < 8 / CPC; ++c) acc2[c] = code_base<B, W, CPC>();
-#pragma unroll
-            for (int e2 = 0; e2 < 8; e2 += 2) {
-              const float ya = __uint_as_float(t[8 * c8 + e2]), yb = __uint_as_float(t[8 * c8 + e2 + 1]);
-              const float2 cs = step_count_signed<B>(ya, yb, F, cst);
-              // the index H - 1/2 + cs is an integer: as 2^21 + index it sits in bits 2..4, the byte
-              // offset of its entry in the 32-byte-aligned table of -2^14 c
-              constexpr float kIdx = (float)(1 << (B - 1)) - 0.5f + 0x1p21f;
-              const float2 mg = __fadd2_rn(cs, make_float2(kIdx, kIdx));
-              const float ca = lds_f32((__float_as_uint(mg.x) & 0x1Cu) | cbase);
-              const float cb = lds_f32((__float_as_uint(mg.y) & 0x1Cu) | cbase);
-              const float2 r2 = __ffma2_rn(make_float2(ya, yb), make_float2(FR, FR), make_float2(ca, cb));  // 2^14 (u - c)
-              rr2 = __ffma2_rn(r2, r2, rr2);
-              const int ep = e2 % CPC;
-              acc2[e2 / CPC] = __ffma2_rn(cs, make_float2((float)(1u << (W * ep)), (float)(1u << (W * (ep + 1)))),
-                                          acc2[e2 / CPC]);
-              split_pair2(r2, hi[e2 / 2], lo[e2 / 2]);
-            }
-#pragma unroll
-            for (int c = 0; c < 8 / CPC; ++c)
-              or_bits<W>(w, W * (8 * c8 + CPC * c), W * CPC, (uint32_t)(acc2[c].x + acc2[c].y));
-          } else {
-#pragma unroll
-            for (int e2 = 0; e2 < 8; e2 += 2) {
-              const int e = 8 * c8 + e2;
-              const float u0 = __uint_as_float(t[e]) * f, u1 = __uint_as_float(t[e + 1]) * f;
-              const uint32_t i0 = lloyd_index<B>(u0, bnd), i1 = lloyd_index<B>(u1, bnd);
-              const float r0 = fmaf(u0, kRScale, cb_s[i0]), r1 = fmaf(u1, kRScale, cb_s[i1]);  // 2^14 (u - c)
-              rr2.x = fmaf(r0, r0, rr2.x);
-              rr2.y = fmaf(r1, r1, rr2.y);
-              put_code<W>(w, e, i0);
-              put_code<W>(w, e + 1, i1);
-              split_pair(make_float2(r0, r1), hi[e2 / 2], lo[e2 / 2]);
-            }
-          }
-          const int off = swz<NV>(v, 32 * cg + 8 * c8);
-          *reinterpret_cast<uint4*>(rh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(smem + L::r_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-        const float rr = rr2.x + rr2.y;
-        rr_s[(yb * 4 + cg) * NV + v] = rr;
-        tc::fence_async_smem();
+      for (long long j = 0; j < nj; ++j) {
+        const int yb = (int)(j & 1);
+        // (a) Y of batch j: partial sum of squares of this thread's 32 coordinates
+        ok = tc::mbar_wait(bar_y + yb, (uint32_t)(j >> 1) & 1u) && ok;
+        tc::fence_after_sync();
+        uint32_t t[32];
+        tc::tmem_ld32(tmem + lane_base + yb * 128 + 32 * cg, t);
+        tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(rready);
-        // (e) sign bits of batch j - 1: its projection completed (waited above)
-        if (j > 0) {
-          uint32_t tp[32];
-          tc::tmem_ld32(tmem + lane_base + 256 + (1 - yb) * 128 + 32 * cg, tp);
-          tc::fence_before_sync();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(pfree + (1 - yb));
-          uint32_t sbits = 0;
+        if (lane == 0) tc::mbar_arrive(yfree + yb);
+        float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) sbits |= (__uint_as_float(tp[e]) > 0.f ? 1u : 0u) << e;
-          merge_signs<W, B>(w_prev, sbits);
-          if (vid_prev >= 0)
-            store_words<W>(reinterpret_cast<uint32_t*>(V.payload + vid_prev * V.pay_bytes) + W * cg, w_prev);
+        for (int e = 0; e < 32; e += 2) {
+          const float2 yy = make_float2(__uint_as_float(t[e]), __uint_as_float(t[e + 1]));
+          ss2 = __ffma2_rn(yy, yy, ss2);
         }
-#pragma unroll
-        for (int k = 0; k < W; ++k) w_prev[k] = w[k];
-        vid_prev = vid;
-        n_prev = n;
-      } else {
-        if (fma_idx) {
-          const float F = f * 0x1p100f;
-#pragma unroll
-          for (int c = 0; c < 32 / CPC; ++c) {
-            float2 acc2 = code_base<B, W, CPC>();
-#pragma unroll
-            for (int e = 0; e < CPC; e += 2) {
-              const float2 cs = step_count_signed<B>(__uint_as_float(t[CPC * c + e]), __uint_as_float(t[CPC * c + e + 1]),
-                                                     F, cst);
-              acc2 = __ffma2_rn(cs, make_float2((float)(1u << (W * e)), (float)(1u << (W * (e + 1)))), acc2);
-            }
-            or_bits<W>(w, W * CPC * c, W * CPC, (uint32_t)(acc2.x + acc2.y));
+        const float ss = ss2.x + ss2.y;
+        ss_s[(yb * 4 + cg) * NV + v] = ss;
+        if (tc::bar_sync_or(1, kSimt, !ok)) {
+          failed = true;
+          break;
+        }
+        // (b) norm, destination
+        const uint32_t bt = (uint32_t)(blockIdx.x + j * gridDim.x);
+        const uint32_t l = fdiv(bt, sh.div_tb), tb = bt - l * sh.n_tb;
+        const int tok = (int)(tb * sh.TB) + tt;
+        long long vid = -1;
+        if (v < sh.rows && tok < a.n_tokens) vid = vid_at(a, (int)l, tok, h, cg == 0);
+        const float* sp = ss_s + yb * 4 * NV + v;
+        const float n = sqrtf((sp[0] + sp[NV] + sp[2 * NV] + sp[3 * NV]) * (1.f / D));  // |x| = |H D x| / sqrt(d)
+        const float f = n > 0.f ? __fdividef(inv_sqrt_dim<D>(), n) : 0.f;
+        uint32_t w[W] = {};
+        if constexpr (QJL) {
+          // header of batch j - 1 (its residual partial sums were stored before the barrier)
+          if (j > 0 && cg == 0 && vid_prev >= 0) {
+            const float* rp = rr_s + (1 - yb) * 4 * NV + v;
+            const float rs = (rp[0] + rp[NV] + rp[2 * NV] + rp[3 * NV]) * (1.f / (kRScale * kRScale));
+            *reinterpret_cast<__half2*>(V.header + vid_prev * V.hdr_bytes) =
+                __halves2half2(__float2half_rn(n_prev), __float2half_rn(n_prev * sqrtf(rs)));
           }
-        } else {
+          // (c) index and residual; R_lo is free once the projection of batch j - 1 completed
+          if (j > 0) {
+            ok = tc::mbar_wait(bar_p + (1 - yb), (uint32_t)((j - 1) >> 1) & 1u) && ok;
+            tc::fence_after_sync();
+          }
+          unsigned char* rh = smem + L::x0 + (int)(j % NX) * kOp;  // the rotation consumed X: R_hi goes there
+          float2 rr2 = make_float2(0.f, 0.f);
+          const float F = f * 0x1p100f, FR = f * kRScale;
+          const uint32_t cbase = sbase + L::cb;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) put_code<W>(w, e, lloyd_index<B>(__uint_as_float(t[e]) * f, bnd));
-        }
-        if (vid >= 0) {
-          if (cg == 0) *reinterpret_cast<__half*>(V.header + vid * V.hdr_bytes) = __float2half_rn(n);
-          store_words<W>(reinterpret_cast<uint32_t*>(V.payload + vid * V.pay_bytes) + W * cg, w);
+          for (int c8 = 0; c8 < 4; ++c8) {
+            uint32_t hi[4], lo[4];
+            if (fma_idx) {
+              // pairs of coordinates in packed fp32 (even, odd): the code accumulators start at the
+              // (H - 1/2) part of every index of their chunk, so the signed counts add the rest
+              float2 acc2[8 / CPC];
+#pragma unroll
+              for (int c = 0; c < 8 / CPC; ++c) acc2[c] = code_base<B, W, CPC>();
+#pragma unroll
+              for (int e2 = 0; e2 < 8; e2 += 2) {
+                const float ya = __uint_as_float(t[8 * c8 + e2]), yb = __uint_as_float(t[8 * c8 + e2 + 1]);
+                const float2 cs = step_count_signed<B>(ya, yb, F, cst);
+                // the index H - 1/2 + cs is an integer: as 2^21 + index it sits in bits 2..4, the byte
+                // offset of its entry in the 32-byte-aligned table of -2^14 c
+                constexpr float kIdx = (float)(1 << (B - 1)) - 0.5f + 0x1p21f;
+                const float2 mg = __fadd2_rn(cs, make_float2(kIdx, kIdx));
+                const float ca = lds_f32((__float_as_uint(mg.x) & 0x1Cu) | cbase);
+                const float cb = lds_f32((__float_as_uint(mg.y) & 0x1Cu) | cbase);
+                const float2 r2 = __ffma2_rn(make_float2(ya, yb), make_float2(FR, FR), make_float2(ca, cb));  // 2^14 (u - c)
+                rr2 = __ffma2_rn(r2, r2, rr2);
+                const int ep = e2 % CPC;
+                acc2[e2 / CPC] = __ffma2_rn(cs, make_float2((float)(1u << (W * ep)), (float)(1u << (W * (ep + 1)))),
+                                            acc2[e2 / CPC]);
+                split_pair2(r2, hi[e2 / 2], lo[e2 / 2]);
+              }
+#pragma unroll
+              for (int c = 0; c < 8 / CPC; ++c)
+                or_bits<W>(w, W * (8 * c8 + CPC * c), W * CPC, (uint32_t)(acc2[c].x + acc2[c].y));
+            } else {
+#pragma unroll
+              for (int e2 = 0; e2 < 8; e2 += 2) {
+                const int e = 8 * c8 + e2;
+                const float u0 = __uint_as_float(t[e]) * f, u1 = __uint_as_float(t[e + 1]) * f;
+                const uint32_t i0 = lloyd_index<B>(u0, bnd), i1 = lloyd_index<B>(u1, bnd);
+                const float r0 = fmaf(u0, kRScale, cb_s[i0]), r1 = fmaf(u1, kRScale, cb_s[i1]);  // 2^14 (u - c)
+                rr2.x = fmaf(r0, r0, rr2.x);
+                rr2.y = fmaf(r1, r1, rr2.y);
+                put_code<W>(w, e, i0);
+                put_code<W>(w, e + 1, i1);
+                split_pair(make_float2(r0, r1), hi[e2 / 2], lo[e2 / 2]);
+              }
+            }
+            const int off = swz<NV>(v, 32 * cg + 8 * c8);
+            *reinterpret_cast<uint4*>(rh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(smem + L::r_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+          const float rr = rr2.x + rr2.y;
+          rr_s[(yb * 4 + cg) * NV + v] = rr;
+          tc::fence_async_smem();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(rready);
+          // (e) sign bits of batch j - 1: its projection completed (waited above)
+          if (j > 0) {
+            uint32_t tp[32];
+            tc::tmem_ld32(tmem + lane_base + 256 + (1 - yb) * 128 + 32 * cg, tp);
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(pfree + (1 - yb));
+            uint32_t sbits = 0;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sbits |= (__uint_as_float(tp[e]) > 0.f ? 1u : 0u) << e;
+            merge_signs<W, B>(w_prev, sbits);
+            if (vid_prev >= 0)
+              store_words<W>(reinterpret_cast<uint32_t*>(V.payload + vid_prev * V.pay_bytes) + W * cg, w_prev);
+          }
+#pragma unroll
+          for (int k = 0; k < W; ++k) w_prev[k] = w[k];
+          vid_prev = vid;
+          n_prev = n;
         }
       }
-    }
     }
     if constexpr (QJL) {
       // the last batch: its header and sign bits
